@@ -1,0 +1,119 @@
+"""Seeded synthetic inputs for PaTH attention workloads.
+
+This module is shared by the tests, the smoke check and the bench.  It holds
+no arithmetic of the method: it only draws random tensors with the shapes and
+distributions of the workloads and hands them out.  Both the CUDA path and the
+CPU oracle consume what it returns; neither is imported here.
+
+Recipe (every workload):
+  q, k, v ~ N(0, 1);  w ~ N(0, 1) then L2-normalised per (token, head) in fp32;
+  beta = 2 * sigmoid(N(0, 1)) in fp32;  scale = 1/sqrt(d);  causal.
+Options:
+  near_reflection -- a seeded 10% of tokens get beta ~ U[1.9, 2.0)
+  fox             -- log f_t = log(sigmoid(N(2, 1))) in fp32 (PaTH-FoX gate)
+  beta_range      -- draw every beta ~ U[lo, hi) instead (stress cases)
+The shapes follow the B x T x d grid of the PaTH authors' kernel-latency table
+(OpenReview rebuttal, "Efficiency Evaluation"), with H = 16 heads at d = 128
+and H = 32 at d = 64.  No dataset is involved.
+
+The generator lives on ``device`` (CPU by default), so a given seed gives the
+same values on every machine for CPU generation; device generation is faster
+for the large workloads and is deterministic per device type.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field, replace
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    T: int
+    d: int
+    dtype: str = "bf16"          # "bf16" or "f32"
+    near_reflection: bool = False
+    fox: bool = False
+    beta_range: tuple | None = None
+    seed: int = 0
+    note: str = field(default="", compare=False)
+
+    @property
+    def torch_dtype(self):
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+    def with_(self, **kw) -> "Workload":
+        return replace(self, **kw)
+
+
+# The five workloads, named by what they are.
+WORKLOADS = {
+    "tiny_f32": Workload("tiny_f32", 1, 2, 256, 64, "f32",
+                         note="tiny PaTH forward in fp32; oracle runs in full"),
+    "t2k_d128": Workload("t2k_d128", 16, 16, 2048, 128),
+    "t2k_d64": Workload("t2k_d64", 16, 32, 2048, 64),
+    "t4k_d128_refl": Workload("t4k_d128_refl", 8, 16, 4096, 128, near_reflection=True),
+    "t4k_d64_refl": Workload("t4k_d64_refl", 8, 32, 4096, 64, near_reflection=True),
+    "fox_t8k_d128": Workload("fox_t8k_d128", 4, 16, 8192, 128, fox=True),
+    "t16k_d128": Workload("t16k_d128", 2, 16, 16384, 128,
+                          note="long-context headline roofline workload"),
+    "t16k_d64": Workload("t16k_d64", 2, 32, 16384, 64),
+}
+
+
+def make_inputs(wl: Workload, device="cpu"):
+    """Draw the inputs of ``wl``.  Returns a dict with q, k, v, w ([B,H,T,d] in
+    the workload dtype), beta ([B,H,T] fp32), logf ([B,H,T] fp32 or None) and
+    scale (python float)."""
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(wl.seed)
+    shape = (wl.B, wl.H, wl.T, wl.d)
+
+    def normal(shp, mean=0.0):
+        x = torch.randn(shp, generator=g, device=dev, dtype=torch.float32)
+        return x + mean if mean else x
+
+    q = normal(shape)
+    k = normal(shape)
+    v = normal(shape)
+    w = normal(shape)
+    w = w / w.norm(dim=-1, keepdim=True).clamp_min(1e-30)
+    bshape = shape[:-1]
+    if wl.beta_range is not None:
+        lo, hi = wl.beta_range
+        beta = lo + (hi - lo) * torch.rand(bshape, generator=g, device=dev)
+    else:
+        beta = 2.0 * torch.sigmoid(normal(bshape))
+    if wl.near_reflection:
+        pick = torch.rand(bshape, generator=g, device=dev) < 0.10
+        hi_beta = 1.9 + 0.1 * torch.rand(bshape, generator=g, device=dev)
+        beta = torch.where(pick, hi_beta, beta)
+    beta = beta.clamp(0.0, 2.0).contiguous()
+    logf = None
+    if wl.fox:
+        logf = torch.log(torch.sigmoid(normal(bshape, 2.0))).contiguous()
+    dt = wl.torch_dtype
+    return dict(q=q.to(dt).contiguous(), k=k.to(dt).contiguous(),
+                v=v.to(dt).contiguous(), w=w.to(dt).contiguous(),
+                beta=beta, logf=logf, scale=1.0 / math.sqrt(wl.d))
+
+
+def sample_rows(T: int, C: int, n_extra: int, seed: int = 0):
+    """A fixed, seeded set of query rows of one head for sampled parity checks:
+    the first and last rows, chunk boundaries around the first and last four
+    chunks, and ``n_extra`` random rows.  Returned sorted and unique."""
+    g = torch.Generator().manual_seed(seed + 7919)
+    rows = {0, T - 1}
+    n = -(-T // C)
+    for c in list(range(min(4, n))) + list(range(max(0, n - 4), n)):
+        for r in (c * C - 1, c * C, c * C + 1, c * C + C - 1):
+            if 0 <= r < T:
+                rows.add(r)
+    if n_extra > 0:
+        rows.update(torch.randint(0, T, (n_extra,), generator=g).tolist())
+    return sorted(rows)
