@@ -1,0 +1,264 @@
+"""PaTH attention forward pass on one GB300 (sm_103a).
+
+A thin ctypes binding of ``libpathattn.so`` (C ABI in ``include/pathattn.h``).
+It only marshals arguments: every step of the forward pass runs in the
+library's CUDA kernels.  torch is used for device memory and the current
+stream.  If the library is missing, every call raises; there is no fallback.
+
+The operation ("PaTH Attention: Position Encoding via Accumulating Householder
+Transformations", discussion slides, frames "PaTH inserts a learned
+transformation along every path" and "FoX adds a separate mechanism for
+forgetting"):
+
+    s_ij = scale * k_j^T H_{j+1} ... H_i q_i [+ sum_{s=j+1}^{i} log f_s],
+    H_t = I - beta_t w_t w_t^T,   o_i = sum_{j<=i} softmax_j(s_ij) v_j.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "PathAttnError", "load_library", "path_attn_fwd", "path_attn_fwd_host",
+    "path_attn_debug_factors", "path_attn_device_status", "path_attn_workspace_bytes",
+    "path_attn_chunk_size", "path_attn_launches_per_call", "path_attn_timing_enable",
+    "path_attn_timing_read", "path_attn_version", "path_attn_status_string",
+    "LIBRARY_PATH", "HEADER_PATH", "PATH_DTYPE_F32", "PATH_DTYPE_BF16",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIBRARY_PATH = os.path.join(_HERE, "libpathattn.so")
+HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "pathattn.h")
+
+PATH_OK = 0
+PATH_DTYPE_F32 = 0
+PATH_DTYPE_BF16 = 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class PathAttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        detail = ""
+        if _lib is not None:
+            name = _lib.path_attn_status_string(status).decode()
+            last = _lib.path_attn_last_error().decode()
+            detail = f"{name}" + (f" ({last})" if last else "")
+        super().__init__(f"{what} failed: status {status} {detail}")
+
+
+def load_library(path: str | None = None):
+    """Load libpathattn.so (built by ``build.py``); raise if it is absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIBRARY_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"libpathattn.so not found at {p}; build it with "
+                "`python -m householder_softmax_attention_gb300.build`")
+        lib = ctypes.CDLL(p)
+        vp, fp, i, f = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        fwd_args = [vp, vp, vp, vp, fp, fp, f, vp, fp, i, i, i, i, i, vp]
+        lib.path_attn_fwd.argtypes = fwd_args
+        lib.path_attn_fwd.restype = i
+        lib.path_attn_fwd_host.argtypes = fwd_args
+        lib.path_attn_fwd_host.restype = i
+        lib.path_attn_status_string.argtypes = [i]
+        lib.path_attn_status_string.restype = ctypes.c_char_p
+        lib.path_attn_last_error.argtypes = []
+        lib.path_attn_last_error.restype = ctypes.c_char_p
+        lib.path_attn_version.argtypes = []
+        lib.path_attn_version.restype = i
+        lib.path_attn_workspace_bytes.argtypes = [i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
+        lib.path_attn_workspace_bytes.restype = i
+        lib.path_attn_chunk_size.argtypes = [i, i]
+        lib.path_attn_chunk_size.restype = i
+        lib.path_attn_device_status.argtypes = [i, i]
+        lib.path_attn_device_status.restype = i
+        lib.path_attn_timing_enable.argtypes = [i]
+        lib.path_attn_timing_enable.restype = i
+        lib.path_attn_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double),
+                                              ctypes.POINTER(ctypes.c_double),
+                                              ctypes.POINTER(ctypes.c_long)]
+        lib.path_attn_timing_read.restype = i
+        lib.path_attn_launches_per_call.argtypes = [i, i, i]
+        lib.path_attn_launches_per_call.restype = i
+        lib.path_attn_debug_factors.argtypes = [vp, vp, vp, fp, fp, f, i, i, i, i, i,
+                                                vp, vp, vp, vp, vp, vp]
+        lib.path_attn_debug_factors.restype = i
+        _lib = lib
+        return lib
+
+
+def _check(rc: int, what: str):
+    if rc != PATH_OK:
+        raise PathAttnError(rc, what)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return PATH_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return PATH_DTYPE_F32
+    raise TypeError(f"unsupported dtype {t.dtype}; use bfloat16 or float32")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check_inputs(q, k, v, w, beta, logf, device_expected: bool):
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v), ("w", w)):
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be [B, H, T, d]")
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError(f"{name} must match q in shape and dtype")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    for name, t in (("beta", beta), ("logf", logf)):
+        if t is None:
+            continue
+        if t.shape != q.shape[:-1] or t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous float32 [B, H, T] tensor")
+    for t in (q, k, v, w, beta, logf):
+        if t is not None and t.is_cuda != device_expected:
+            raise ValueError("all tensors must be on " + ("the GPU" if device_expected else "the host"))
+    if device_expected:
+        dev = q.device
+        for t in (k, v, w, beta, logf):
+            if t is not None and t.device != dev:
+                raise ValueError("all tensors must be on one device")
+
+
+def path_attn_fwd(q, k, v, w, beta, logf=None, scale=None, out=None, lse=None,
+                  want_lse=True, stream=None):
+    """PaTH(-FoX) forward on CUDA tensors.
+
+    q, k, v, w: ``[B, H, T, d]`` bfloat16 or float32 (one dtype), contiguous;
+    beta (and logf for PaTH-FoX): ``[B, H, T]`` float32.  ``scale`` defaults to
+    ``1/sqrt(d)``.  Returns ``(out, lse)`` (lse is None if ``want_lse`` is
+    false).  Runs on ``stream`` (default: torch's current stream).
+    """
+    import torch
+    lib = load_library()
+    _check_inputs(q, k, v, w, beta, logf, True)
+    B, H, T, d = q.shape
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, T), device=q.device, dtype=torch.float32)
+    st = stream if stream is not None else torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        rc = lib.path_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(beta), _ptr(logf),
+                               float(scale), _ptr(out), _ptr(lse), B, H, T, d,
+                               _dtype_code(q), ctypes.c_void_p(st.cuda_stream))
+    _check(rc, "path_attn_fwd")
+    return out, lse
+
+
+def path_attn_fwd_host(q, k, v, w, beta, logf=None, scale=None, out=None, lse=None,
+                       want_lse=True, stream=None):
+    """The same forward on host (CPU) tensors; copies to and from the current
+    device happen inside the library call, which returns when the results are
+    on the host.  Pinned host tensors make the copies faster."""
+    import torch
+    lib = load_library()
+    _check_inputs(q, k, v, w, beta, logf, False)
+    B, H, T, d = q.shape
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, T), dtype=torch.float32)
+    st = stream if stream is not None else torch.cuda.current_stream()
+    rc = lib.path_attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(beta), _ptr(logf),
+                                float(scale), _ptr(out), _ptr(lse), B, H, T, d,
+                                _dtype_code(q), ctypes.c_void_p(st.cuda_stream))
+    _check(rc, "path_attn_fwd_host")
+    return out, lse
+
+
+def path_attn_chunk_size(d: int, dtype_code: int) -> int:
+    c = load_library().path_attn_chunk_size(d, dtype_code)
+    if c < 0:
+        raise PathAttnError(c, "path_attn_chunk_size")
+    return c
+
+
+def path_attn_debug_factors(q, k, w, beta, logf=None, scale=None, stream=None):
+    """Chunk factors of the preparation step (diagnostics; see the header)."""
+    import torch
+    lib = load_library()
+    _check_inputs(q, k, q, w, beta, logf, True)
+    B, H, T, d = q.shape
+    if scale is None:
+        scale = d ** -0.5
+    code = _dtype_code(q)
+    C = path_attn_chunk_size(d, code)
+    Np = -(-T // C)
+    BH, Tp = B * H, Np * C
+    dev = q.device
+    kr = torch.empty((BH, Tp, d), device=dev, dtype=q.dtype)
+    ql = torch.empty((BH, Tp, d), device=dev, dtype=torch.float32)
+    ngt = torch.empty((BH, Np, d, d), device=dev, dtype=q.dtype)
+    sdt = torch.empty((BH, Np, C, C), device=dev, dtype=torch.float32)
+    lam2 = torch.empty((BH, Tp), device=dev, dtype=torch.float32) if logf is not None else None
+    st = stream if stream is not None else torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        rc = lib.path_attn_debug_factors(_ptr(q), _ptr(k), _ptr(w), _ptr(beta), _ptr(logf),
+                                         float(scale), B, H, T, d, code, _ptr(kr), _ptr(ql),
+                                         _ptr(ngt), _ptr(sdt), _ptr(lam2),
+                                         ctypes.c_void_p(st.cuda_stream))
+    _check(rc, "path_attn_debug_factors")
+    return dict(C=C, kr=kr, ql=ql, ngt=ngt, sdt=sdt, lam2=lam2)
+
+
+def path_attn_device_status(device: int = 0, clear: bool = True) -> int:
+    """0 if no kernel wait expired on ``device`` since the last clear, else a
+    negative status (PATH_ERR_TIMEOUT).  Synchronises the device."""
+    return load_library().path_attn_device_status(device, 1 if clear else 0)
+
+
+def path_attn_workspace_bytes(B, H, T, d, dtype_code, with_gate=False) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load_library().path_attn_workspace_bytes(B, H, T, d, dtype_code, int(with_gate),
+                                                    ctypes.byref(n)),
+           "path_attn_workspace_bytes")
+    return n.value
+
+
+def path_attn_launches_per_call(d, dtype_code, with_gate=False) -> int:
+    n = load_library().path_attn_launches_per_call(d, dtype_code, int(with_gate))
+    if n < 0:
+        raise PathAttnError(n, "path_attn_launches_per_call")
+    return n
+
+
+def path_attn_timing_enable(enable: bool = True):
+    _check(load_library().path_attn_timing_enable(1 if enable else 0), "path_attn_timing_enable")
+
+
+def path_attn_timing_read():
+    """(prep_ms_total, attn_ms_total, calls) since timing was enabled."""
+    p, a, c = ctypes.c_double(0), ctypes.c_double(0), ctypes.c_long(0)
+    _check(load_library().path_attn_timing_read(ctypes.byref(p), ctypes.byref(a), ctypes.byref(c)),
+           "path_attn_timing_read")
+    return p.value, a.value, c.value
+
+
+def path_attn_version() -> int:
+    return load_library().path_attn_version()
+
+
+def path_attn_status_string(status: int) -> str:
+    return load_library().path_attn_status_string(status).decode()

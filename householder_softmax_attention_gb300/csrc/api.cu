@@ -1,0 +1,347 @@
+// api.cu -- the C ABI of libpathattn.so (declared in include/pathattn.h).
+//
+// Argument validation happens before any CUDA call.  Workspace comes from a
+// per-device memory pool owned by the library (stream-ordered, cached across
+// calls).  Kernels report bounded-wait expiry through a per-device status word.
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdio>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/pathattn.h"
+#include "common.cuh"
+
+using namespace pathattn;
+
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;
+  cudaMemPool_t pool = nullptr;
+  int* status = nullptr;  // device int, 0 = fine
+  int cc_major = 0, cc_minor = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+thread_local char g_last_error[256] = "";
+
+struct TimingRec {
+  cudaEvent_t e0, e1, e2;
+};
+bool g_timing = false;
+std::vector<TimingRec> g_timing_recs;
+size_t g_timing_used = 0;
+
+int set_cuda_error(cudaError_t e) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s", cudaGetErrorName(e),
+                cudaGetErrorString(e));
+  return e == cudaErrorMemoryAllocation ? PATH_ERR_OOM : PATH_ERR_CUDA;
+}
+
+// Per-device library state, created on first use with that device current.
+int device_state(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  if (dev < 0 || dev >= kMaxDevices) return PATH_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& s = g_dev[dev];
+  if (!s.ready) {
+    cudaDeviceProp prop;
+    if ((e = cudaGetDeviceProperties(&prop, dev)) != cudaSuccess) return set_cuda_error(e);
+    s.cc_major = prop.major;
+    s.cc_minor = prop.minor;
+    cudaMemPoolProps props;
+    std::memset(&props, 0, sizeof(props));
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    if ((e = cudaMemPoolCreate(&s.pool, &props)) != cudaSuccess) return set_cuda_error(e);
+    uint64_t keep = UINT64_MAX;
+    if ((e = cudaMemPoolSetAttribute(s.pool, cudaMemPoolAttrReleaseThreshold, &keep)) !=
+        cudaSuccess)
+      return set_cuda_error(e);
+    if ((e = cudaMalloc(&s.status, sizeof(int))) != cudaSuccess) return set_cuda_error(e);
+    if ((e = cudaMemset(s.status, 0, sizeof(int))) != cudaSuccess) return set_cuda_error(e);
+    s.ready = true;
+  }
+  *out = &s;
+  return PATH_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int chunk_size(int d, int dtype) {
+  if (dtype != PATH_DTYPE_F32 && dtype != PATH_DTYPE_BF16) return PATH_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return PATH_ERR_UNSUPPORTED;
+  return dtype == PATH_DTYPE_BF16 ? 128 : 64;
+}
+
+// Shape checks shared by every entry point; fills the geometry.
+int make_geom(int B, int H, int T, int d, int dtype, bool gate, Geom* g) {
+  if (B < 1 || H < 1 || T < 1) return PATH_ERR_INVALID_ARG;
+  const int C = chunk_size(d, dtype);
+  if (C < 0) return C;
+  const long long BH = static_cast<long long>(B) * H;
+  const long long Np = (static_cast<long long>(T) + C - 1) / C;
+  const long long Tp = Np * C;
+  // every operand and workspace index stays inside int32 row/column space
+  if (BH * Tp * d > INT_MAX || BH * Np * d * d > INT_MAX || BH * Np > INT_MAX / 4)
+    return PATH_ERR_UNSUPPORTED;
+  g->B = B; g->H = H; g->T = T; g->d = d; g->C = C;
+  g->BH = static_cast<int>(BH);
+  g->Np = static_cast<int>(Np);
+  g->Tp = static_cast<int>(Tp);
+  g->nch = static_cast<int>(BH * Np);
+  g->bf16 = dtype == PATH_DTYPE_BF16;
+  g->gate = gate;
+  return PATH_OK;
+}
+
+int check_device(const DeviceState* s) {
+  // kernels are built for sm_103a only
+  if (s->cc_major != 10 || s->cc_minor != 3) {
+    std::snprintf(g_last_error, sizeof(g_last_error),
+                  "libpathattn is built for sm_103a; this device is sm_%d%d", s->cc_major,
+                  s->cc_minor);
+    return PATH_ERR_UNSUPPORTED;
+  }
+  return PATH_OK;
+}
+
+// Runs prep + attention for device pointers; `ws_base` must hold the layout.
+int run_forward(const Geom& g, const Inputs& in, char* ws_base, DeviceState* s,
+                cudaStream_t st) {
+  Workspace ws;
+  workspace_layout(g, ws_base, &ws);
+  TimingRec* rec = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_timing) {
+      if (g_timing_used == g_timing_recs.size()) {
+        TimingRec r{};
+        if (cudaEventCreate(&r.e0) == cudaSuccess && cudaEventCreate(&r.e1) == cudaSuccess &&
+            cudaEventCreate(&r.e2) == cudaSuccess)
+          g_timing_recs.push_back(r);
+      }
+      if (g_timing_used < g_timing_recs.size()) rec = &g_timing_recs[g_timing_used++];
+    }
+  }
+  cudaError_t e;
+  if (rec) cudaEventRecord(rec->e0, st);
+  if ((e = launch_prep(g, in, ws, st, nullptr)) != cudaSuccess) return set_cuda_error(e);
+  if (rec) cudaEventRecord(rec->e1, st);
+  if (g.bf16)
+    e = launch_attn_tc(g, in, ws, s->status, st, nullptr);
+  else
+    e = launch_attn_f32(g, in, ws, st, nullptr);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  if (rec) cudaEventRecord(rec->e2, st);
+  return PATH_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* path_attn_status_string(int status) {
+  switch (status) {
+    case PATH_OK: return "PATH_OK";
+    case PATH_ERR_INVALID_ARG: return "PATH_ERR_INVALID_ARG";
+    case PATH_ERR_UNSUPPORTED: return "PATH_ERR_UNSUPPORTED";
+    case PATH_ERR_CUDA: return "PATH_ERR_CUDA";
+    case PATH_ERR_TIMEOUT: return "PATH_ERR_TIMEOUT";
+    case PATH_ERR_OOM: return "PATH_ERR_OOM";
+    default: return "PATH_ERR_UNKNOWN";
+  }
+}
+
+const char* path_attn_last_error(void) { return g_last_error; }
+
+int path_attn_version(void) { return kVersion; }
+
+int path_attn_chunk_size(int d, int dtype) { return chunk_size(d, dtype); }
+
+int path_attn_workspace_bytes(int B, int H, int T, int d, int dtype, int with_gate,
+                              size_t* bytes) {
+  if (!bytes) return PATH_ERR_INVALID_ARG;
+  Geom g;
+  const int rc = make_geom(B, H, T, d, dtype, with_gate != 0, &g);
+  if (rc != PATH_OK) return rc;
+  *bytes = workspace_layout(g, nullptr, nullptr);
+  return PATH_OK;
+}
+
+int path_attn_launches_per_call(int d, int dtype, int with_gate) {
+  const int C = chunk_size(d, dtype);
+  if (C < 0) return C;
+  return 11 + (with_gate ? 1 : 0) + 1;
+}
+
+int path_attn_fwd(const void* q, const void* k, const void* v, const void* w,
+                  const float* beta, const float* logf, float scale, void* out, float* lse,
+                  int B, int H, int T, int d, int dtype, void* stream) {
+  if (!q || !k || !v || !w || !beta || !out) return PATH_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(w) || !aligned16(beta) ||
+      !aligned16(out) || (logf && !aligned16(logf)) || (lse && !aligned16(lse)))
+    return PATH_ERR_INVALID_ARG;
+  if (!(scale == scale)) return PATH_ERR_INVALID_ARG;  // NaN scale
+  Geom g;
+  int rc = make_geom(B, H, T, d, dtype, logf != nullptr, &g);
+  if (rc != PATH_OK) return rc;
+  DeviceState* s = nullptr;
+  if ((rc = device_state(&s)) != PATH_OK) return rc;
+  if ((rc = check_device(s)) != PATH_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t bytes = workspace_layout(g, nullptr, nullptr);
+  void* ws = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&ws, bytes, s->pool, st);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  Inputs in{q, k, v, w, beta, logf, scale, out, lse};
+  rc = run_forward(g, in, static_cast<char*>(ws), s, st);
+  e = cudaFreeAsync(ws, st);
+  if (rc == PATH_OK && e != cudaSuccess) rc = set_cuda_error(e);
+  return rc;
+}
+
+int path_attn_fwd_host(const void* q, const void* k, const void* v, const void* w,
+                       const float* beta, const float* logf, float scale, void* out,
+                       float* lse, int B, int H, int T, int d, int dtype, void* stream) {
+  if (!q || !k || !v || !w || !beta || !out) return PATH_ERR_INVALID_ARG;
+  Geom g;
+  int rc = make_geom(B, H, T, d, dtype, logf != nullptr, &g);
+  if (rc != PATH_OK) return rc;
+  DeviceState* s = nullptr;
+  if ((rc = device_state(&s)) != PATH_OK) return rc;
+  if ((rc = check_device(s)) != PATH_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t es = dtype == PATH_DTYPE_BF16 ? 2 : 4;
+  const size_t nx = static_cast<size_t>(g.BH) * T * d * es, nb = static_cast<size_t>(g.BH) * T * 4;
+  size_t off = 0;
+  auto take = [&](size_t n) { size_t o = off; off = align_up(off + n, 256); return o; };
+  const size_t oq = take(nx), ok_ = take(nx), ov = take(nx), ow = take(nx), ob = take(nb),
+               olf = logf ? take(nb) : 0, oo = take(nx), ol = lse ? take(nb) : 0;
+  const size_t io_bytes = off;
+  const size_t ws_bytes = workspace_layout(g, nullptr, nullptr);
+  char* buf = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&buf), io_bytes + ws_bytes,
+                                          s->pool, st);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  auto h2d = [&](size_t o, const void* src, size_t n) {
+    return cudaMemcpyAsync(buf + o, src, n, cudaMemcpyHostToDevice, st);
+  };
+  if ((e = h2d(oq, q, nx)) || (e = h2d(ok_, k, nx)) || (e = h2d(ov, v, nx)) ||
+      (e = h2d(ow, w, nx)) || (e = h2d(ob, beta, nb)) || (logf && (e = h2d(olf, logf, nb)))) {
+    rc = set_cuda_error(e);
+  } else {
+    Inputs in{buf + oq, buf + ok_, buf + ov, buf + ow,
+              reinterpret_cast<float*>(buf + ob),
+              logf ? reinterpret_cast<float*>(buf + olf) : nullptr,
+              scale, buf + oo, lse ? reinterpret_cast<float*>(buf + ol) : nullptr};
+    rc = run_forward(g, in, buf + io_bytes, s, st);
+    if (rc == PATH_OK) {
+      if ((e = cudaMemcpyAsync(out, buf + oo, nx, cudaMemcpyDeviceToHost, st)) ||
+          (lse && (e = cudaMemcpyAsync(lse, buf + ol, nb, cudaMemcpyDeviceToHost, st))))
+        rc = set_cuda_error(e);
+    }
+  }
+  e = cudaFreeAsync(buf, st);
+  if (rc == PATH_OK && e != cudaSuccess) rc = set_cuda_error(e);
+  e = cudaStreamSynchronize(st);
+  if (rc == PATH_OK && e != cudaSuccess) rc = set_cuda_error(e);
+  return rc;
+}
+
+int path_attn_device_status(int device, int clear) {
+  int prev = 0;
+  cudaError_t e = cudaGetDevice(&prev);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  if ((e = cudaSetDevice(device)) != cudaSuccess) return set_cuda_error(e);
+  DeviceState* s = nullptr;
+  int rc = device_state(&s);
+  int word = 0;
+  if (rc == PATH_OK) {
+    if ((e = cudaDeviceSynchronize()) != cudaSuccess ||
+        (e = cudaMemcpy(&word, s->status, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess ||
+        (clear && (e = cudaMemset(s->status, 0, sizeof(int))) != cudaSuccess))
+      rc = set_cuda_error(e);
+  }
+  cudaSetDevice(prev);
+  if (rc != PATH_OK) return rc;
+  return word == PATH_DEV_OK ? PATH_OK : PATH_ERR_TIMEOUT;
+}
+
+int path_attn_timing_enable(int enable) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_timing = enable != 0;
+  g_timing_used = 0;
+  return PATH_OK;
+}
+
+int path_attn_timing_read(double* prep_ms, double* attn_ms, long* calls) {
+  std::vector<TimingRec> recs;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    recs.assign(g_timing_recs.begin(), g_timing_recs.begin() + g_timing_used);
+  }
+  double p = 0, a = 0;
+  for (auto& r : recs) {
+    cudaError_t e = cudaEventSynchronize(r.e2);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    float x = 0, y = 0;
+    if ((e = cudaEventElapsedTime(&x, r.e0, r.e1)) != cudaSuccess ||
+        (e = cudaEventElapsedTime(&y, r.e1, r.e2)) != cudaSuccess)
+      return set_cuda_error(e);
+    p += x;
+    a += y;
+  }
+  if (prep_ms) *prep_ms = p;
+  if (attn_ms) *attn_ms = a;
+  if (calls) *calls = static_cast<long>(recs.size());
+  return PATH_OK;
+}
+
+int path_attn_debug_factors(const void* q, const void* k, const void* w, const float* beta,
+                            const float* logf, float scale, int B, int H, int T, int d,
+                            int dtype, void* kr, float* ql, void* ngt, float* sdt, float* lam2,
+                            void* stream) {
+  if (!q || !k || !w || !beta || !kr || !ql || !ngt || !sdt || (logf && !lam2))
+    return PATH_ERR_INVALID_ARG;
+  Geom g;
+  int rc = make_geom(B, H, T, d, dtype, logf != nullptr, &g);
+  if (rc != PATH_OK) return rc;
+  DeviceState* s = nullptr;
+  if ((rc = device_state(&s)) != PATH_OK) return rc;
+  if ((rc = check_device(s)) != PATH_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t bytes = workspace_layout(g, nullptr, nullptr);
+  void* base = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&base, bytes, s->pool, st);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  Workspace ws;
+  workspace_layout(g, static_cast<char*>(base), &ws);
+  Inputs in{q, k, nullptr, w, beta, logf, scale, nullptr, nullptr};
+  e = launch_prep(g, in, ws, st, nullptr);
+  const size_t es = g.bf16 ? 2 : 4, nch = g.nch, C = g.C;
+  if (e == cudaSuccess) e = cudaMemcpyAsync(kr, ws.kr, nch * C * d * es, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(ql, ws.ql, nch * C * d * 4, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(ngt, ws.ngt, nch * d * d * es, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(sdt, ws.sdt, nch * C * C * 4, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess && logf)
+    e = cudaMemcpyAsync(lam2, ws.lam2, static_cast<size_t>(g.BH) * g.Tp * 4,
+                        cudaMemcpyDeviceToDevice, st);
+  if (e != cudaSuccess) rc = set_cuda_error(e);
+  e = cudaFreeAsync(base, st);
+  if (rc == PATH_OK && e != cudaSuccess) rc = set_cuda_error(e);
+  return rc;
+}
+
+}  // extern "C"

@@ -1,0 +1,498 @@
+// attn_tc.cu -- PaTH forward scan on the sm_103a tensor cores (dtype bf16).
+//
+// One CTA per 128-row query tile (= one chunk b of one head).  The tile walks
+// the key chunks backwards from the diagonal ("PaTH Attention ..." slides,
+// frame "A right-to-left scan accumulates cross-block paths"):
+//
+//   diagonal   P_b = softmax-step(sdt_b)            (logits precomputed, fp32)
+//   for c = b-1 .. 0:
+//     S   = Qw . kr_c^T                            tcgen05, A = Qw from TMEM
+//     Qm += Qw . ngt_c^T   (only if c > 0)         crossing chunk c backwards
+//     P_c = softmax-step(S)                        online softmax, lazy rescale
+//     O  += P_{c+1} . V_{c+1}                      tcgen05, A = P from TMEM
+//   O += P_0 . V_0;  out = O / l,  lse = (m + log2 l) ln 2
+//
+// Qm is the fp32 master of the running query (q_i carried through every
+// transition crossed so far), held in TMEM and updated in place by the MMA;
+// Qw is its bf16 copy, the A operand of the next step.  The transition is the
+// dense d x d form of F_c^T = I - W^T U W from the chunk preparation.
+//
+// Warp roles (384 threads):
+//   warp 0      TMA producer: kr_c and ngt_c (one stage), V (own stage ring)
+//   warp 1      TMEM allocation and the single MMA-issuing thread
+//   warps 4-7   softmax: one query row per thread (TMEM lane = row)
+//   warps 8-11  running-query conversion Qm -> Qw (and its initial load)
+// TMEM columns: S [0,128), O, Qm (d each), Qw (d/2, packed bf16x2), P (64).
+// Every wait is bounded; on expiry the CTA records PATH_DEV_ERR_TIMEOUT in the
+// status word, drains its own copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace pathattn {
+namespace {
+
+constexpr int kC = 128;       // chunk length = query tile = key tile
+constexpr int kThreads = 384;
+constexpr int kRegsLow = 56, kRegsSoftmax = 240, kRegsQuery = 112;
+static_assert(128 * (kRegsLow + kRegsSoftmax + kRegsQuery) <= kThreads * 168, "register split");
+
+template <int D>
+struct TcCfg {
+  static constexpr int kHalves = D / 64;           // 64-column (128-byte) halves
+  static constexpr uint32_t kKrBytes = kC * D * 2;
+  static constexpr uint32_t kNgBytes = D * D * 2;
+  static constexpr uint32_t kVBytes = kC * D * 2;
+  static constexpr uint32_t kColS = 0;
+  static constexpr uint32_t kColO = 128;
+  static constexpr uint32_t kColQm = 128 + D;
+  static constexpr uint32_t kColQw = 128 + 2 * D;
+  static constexpr uint32_t kColP = 128 + 2 * D + D / 2;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr size_t kTileBytes = 2 * (kKrBytes + kNgBytes + kVBytes);
+  static constexpr size_t kSmemBytes = kTileBytes + 1024 /*align*/ + 256 /*barriers*/;
+  static_assert(kColP + 64 <= kTmemCols, "TMEM budget");
+};
+
+struct Bars {
+  uint64_t kg_full[2], kg_empty[2], v_full[2], v_empty[2];
+  uint64_t q_ready, s_free, p_full, qk_done, pv_done, final_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ void record_timeout(Bars* bars, int* status) {
+  bars->abort_flag = 1;
+  atomicExch(status, PATH_DEV_ERR_TIMEOUT);
+}
+
+// End of every role: all 384 threads meet on named barrier 1, then warp 1
+// (the allocating warp) frees TMEM.
+__device__ __forceinline__ void teardown(int warp, uint32_t tb, uint32_t ncols) {
+  tc_fence_before_sync();
+  asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tb, ncols);
+  }
+}
+
+template <int D, bool kGate>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap map_kr,
+                   const __grid_constant__ CUtensorMap map_ng,
+                   const __grid_constant__ CUtensorMap map_v, const float* __restrict__ ql,
+                   const float* __restrict__ sdt, const float* __restrict__ lam2,
+                   __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
+                   int* __restrict__ status, int T, int Np, int BH, float sl2) {
+  using Cfg = TcCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* s_kr = base;                                   // [2][kKrBytes]
+  uint8_t* s_ng = base + 2 * Cfg::kKrBytes;               // [2][kNgBytes]
+  uint8_t* s_v = s_ng + 2 * Cfg::kNgBytes;                // [2][kVBytes]
+  Bars* bars = reinterpret_cast<Bars*>(base + Cfg::kTileBytes);
+  volatile int* abort_flag = &bars->abort_flag;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int ord = blockIdx.x;           // longest tiles (largest b) first
+  const int b = Np - 1 - ord / BH;
+  const int bh = ord % BH;
+  const int Tp = Np * kC;
+  const uint64_t LIM = kWaitLimitNs;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->kg_full[s], 1);
+      mbar_init(&bars->kg_empty[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
+    }
+    mbar_init(&bars->q_ready, 128);
+    mbar_init(&bars->s_free, 128);
+    mbar_init(&bars->p_full, 128);
+    mbar_init(&bars->qk_done, 1);
+    mbar_init(&bars->pv_done, 1);
+    mbar_init(&bars->final_done, 1);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&map_kr);
+    tma_prefetch_map(&map_ng);
+    tma_prefetch_map(&map_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tb = bars->tmem_base;
+
+  // 384 threads launched at <= 168 registers each (64512); each warpgroup
+  // re-sizes itself: 128 x 56 (producer / MMA / idle) + 128 x 240 (softmax) +
+  // 128 x 112 (running query) = 52224.  The three warpgroups never rejoin:
+  // each ends with its own copy of the teardown.
+  if (warp < 4) {
+    regs_dec<kRegsLow>();
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int last_kg[2] = {-1, -1}, last_v[2] = {-1, -1};
+      bool ok = true;
+      for (int n = 0; n <= b && ok; ++n) {
+        const int s = n & 1;
+        if (n < b) {
+          const int c = b - 1 - n;
+          if (n >= 2) ok = mbar_wait(&bars->kg_empty[s], ((n >> 1) - 1) & 1, abort_flag, LIM);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&bars->kg_full[s], Cfg::kKrBytes + Cfg::kNgBytes);
+          for (int h = 0; h < Cfg::kHalves; ++h) {
+            tma_load_2d(s_kr + s * Cfg::kKrBytes + h * (kC * 128), &map_kr, h * 64,
+                        bh * Tp + c * kC, &bars->kg_full[s]);
+            tma_load_2d(s_ng + s * Cfg::kNgBytes + h * (D * 128), &map_ng, h * 64,
+                        (bh * Np + c) * D, &bars->kg_full[s]);
+          }
+          last_kg[s] = (n >> 1) & 1;
+        }
+        if (n >= 2) ok = mbar_wait(&bars->v_empty[s], ((n >> 1) - 1) & 1, abort_flag, LIM);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&bars->v_full[s], Cfg::kVBytes);
+        for (int h = 0; h < Cfg::kHalves; ++h)
+          tma_load_3d(s_v + s * Cfg::kVBytes + h * (kC * 128), &map_v, h * 64, (b - n) * kC, bh,
+                      &bars->v_full[s]);
+        last_v[s] = (n >> 1) & 1;
+      }
+      if (!ok) record_timeout(bars, status);
+      // every copy this thread started has landed before the CTA may exit
+      for (int s = 0; s < 2; ++s) {
+        if (last_kg[s] >= 0) mbar_wait(&bars->kg_full[s], last_kg[s], nullptr, LIM);
+        if (last_v[s] >= 0) mbar_wait(&bars->v_full[s], last_v[s], nullptr, LIM);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t tS = tb + Cfg::kColS, tO = tb + Cfg::kColO, tQm = tb + Cfg::kColQm,
+                     tQw = tb + Cfg::kColQw, tP = tb + Cfg::kColP;
+      constexpr uint32_t idS = idesc_bf16_f32(128, kC, false, false);
+      constexpr uint32_t idD = idesc_bf16_f32(128, D, false, false);
+      constexpr uint32_t idPV = idesc_bf16_f32(128, D, false, true);
+      bool ok = true;
+      for (int n = 0; n < b && ok; ++n) {
+        const int c = b - 1 - n, s = n & 1;
+        ok = mbar_wait(&bars->q_ready, n & 1, abort_flag, LIM);
+        if (ok && n >= 1) ok = mbar_wait(&bars->s_free, (n - 1) & 1, abort_flag, LIM);
+        if (ok) ok = mbar_wait(&bars->kg_full[s], (n >> 1) & 1, abort_flag, LIM);
+        if (!ok) break;
+        tc_fence_after_sync();
+        const uint32_t kr_a = smem_addr(s_kr + s * Cfg::kKrBytes);
+        const uint32_t ng_a = smem_addr(s_ng + s * Cfg::kNgBytes);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * (kC * 128) + (k & 3) * 32;
+          mma_bf16_ts(tS, tQw + k * 8, sdesc_sw128(kr_a + off, 16, 1024), idS, k > 0);
+        }
+        if (c > 0) {
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k >> 2) * (D * 128) + (k & 3) * 32;
+            mma_bf16_ts(tQm, tQw + k * 8, sdesc_sw128(ng_a + off, 16, 1024), idD, 1);
+          }
+        }
+        mma_commit(&bars->qk_done);
+        mma_commit(&bars->kg_empty[s]);
+        // O += P_{c+1} V_{c+1}
+        ok = mbar_wait(&bars->p_full, n & 1, abort_flag, LIM);
+        if (ok) ok = mbar_wait(&bars->v_full[s], (n >> 1) & 1, abort_flag, LIM);
+        if (!ok) break;
+        tc_fence_after_sync();
+        const uint32_t v_a = smem_addr(s_v + s * Cfg::kVBytes);
+#pragma unroll
+        for (int k = 0; k < kC / 16; ++k)
+          mma_bf16_ts(tO, tP + k * 8, sdesc_sw128(v_a + k * 2048, kC * 128, 1024), idPV,
+                      (n > 0 || k > 0));
+        mma_commit(&bars->pv_done);
+        mma_commit(&bars->v_empty[s]);
+      }
+      if (ok) {
+        const int s = b & 1;
+        ok = mbar_wait(&bars->p_full, b & 1, abort_flag, LIM);
+        if (ok) ok = mbar_wait(&bars->v_full[s], (b >> 1) & 1, abort_flag, LIM);
+        if (ok) {
+          tc_fence_after_sync();
+          const uint32_t v_a = smem_addr(s_v + s * Cfg::kVBytes);
+#pragma unroll
+          for (int k = 0; k < kC / 16; ++k)
+            mma_bf16_ts(tO, tP + k * 8, sdesc_sw128(v_a + k * 2048, kC * 128, 1024), idPV,
+                        (b > 0 || k > 0));
+          mma_commit(&bars->pv_done);
+        }
+      }
+      if (!ok) record_timeout(bars, status);
+      // all MMAs of this CTA complete before TMEM is released
+      mma_commit(&bars->final_done);
+      mbar_wait(&bars->final_done, 0, nullptr, LIM);
+    }
+  }
+    teardown(warp, tb, Cfg::kTmemCols);
+  } else if (warp < 8) {
+    regs_inc<kRegsSoftmax>();
+    // ------------------------------------------------------------ softmax
+    const int q4 = warp - 4;
+    const int r = q4 * 32 + lane;
+    const int t = b * kC + r;
+    const uint32_t lb = static_cast<uint32_t>(q4 * 32) << 16;
+    const uint32_t tS = tb + lb + Cfg::kColS, tO = tb + lb + Cfg::kColO,
+                   tP = tb + lb + Cfg::kColP;
+    uint32_t x[128];
+    float m_used, l = 0.f;
+    // diagonal chunk: precomputed log2-domain logits sdt[ch][j][i]
+    {
+      const float* sd = sdt + (static_cast<size_t>(bh) * Np + b) * kC * kC + r;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < kC; ++j) {
+        const float v = __ldg(sd + j * kC);
+        x[j] = __float_as_uint(v);
+        mx = fmaxf(mx, v);
+      }
+      m_used = mx;
+      uint32_t pk[64];
+#pragma unroll
+      for (int j = 0; j < kC; j += 2) {
+        const float p0 = ex2_approx(__uint_as_float(x[j]) - m_used);
+        const float p1 = ex2_approx(__uint_as_float(x[j + 1]) - m_used);
+        l += p0 + p1;
+        pk[j / 2] = pack_bf16x2(p0, p1);
+      }
+      tmem_st_x32(tP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      tmem_st_x32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&bars->p_full);
+    }
+    bool ok = true;
+    const float lrow = kGate ? lam2[static_cast<size_t>(bh) * Tp + t] : 0.f;
+    for (int n = 0; n < b; ++n) {
+      const int c = b - 1 - n;
+      ok = mbar_wait(&bars->qk_done, n & 1, abort_flag, LIM);
+      if (!ok) break;
+      tc_fence_after_sync();
+      tmem_ld_x64(tS, *reinterpret_cast<uint32_t(*)[64]>(&x[0]));
+      tmem_ld_x64(tS + 64, *reinterpret_cast<uint32_t(*)[64]>(&x[64]));
+      tc_fence_before_sync();
+      mbar_arrive(&bars->s_free);
+      float mx = -INFINITY;
+      if (kGate) {
+        const float4* lg = reinterpret_cast<const float4*>(lam2 + static_cast<size_t>(bh) * Tp + c * kC);
+#pragma unroll
+        for (int j4 = 0; j4 < kC / 4; ++j4) {
+          const float4 g4 = __ldg(lg + j4);
+          const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int j = j4 * 4 + u;
+            const float v = fmaf(__uint_as_float(x[j]), sl2, lrow - gv[u]);
+            x[j] = __float_as_uint(v);
+            mx = fmaxf(mx, v);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < kC; ++j) {
+          const float v = __uint_as_float(x[j]) * sl2;
+          x[j] = __float_as_uint(v);
+          mx = fmaxf(mx, v);
+        }
+      }
+      // lazy rescaling: move the reference max only when it grows by > 8 (log2)
+      const bool need = mx > m_used + 8.f;
+      float alpha = 1.f;
+      if (need) {
+        alpha = ex2_approx(m_used - mx);
+        m_used = mx;
+        l *= alpha;
+      }
+      uint32_t pk[64];
+#pragma unroll
+      for (int j = 0; j < kC; j += 2) {
+        const float p0 = ex2_approx(__uint_as_float(x[j]) - m_used);
+        const float p1 = ex2_approx(__uint_as_float(x[j + 1]) - m_used);
+        l += p0 + p1;
+        pk[j / 2] = pack_bf16x2(p0, p1);
+      }
+      // P buffer and O are free once O += P_{c+1} V_{c+1} has completed
+      ok = mbar_wait(&bars->pv_done, n & 1, abort_flag, LIM);
+      if (!ok) break;
+      tc_fence_after_sync();
+      if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+        for (int cc = 0; cc < D; cc += 32) {
+          uint32_t o[32];
+          tmem_ld_x32(tO + cc, o);
+#pragma unroll
+          for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
+          tmem_st_x32(tO + cc, o);
+        }
+      }
+      tmem_st_x32(tP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      tmem_st_x32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&bars->p_full);
+    }
+    // epilogue: out = O / l, lse = (m + log2 l) ln 2
+    if (ok) ok = mbar_wait(&bars->pv_done, b & 1, abort_flag, LIM);
+    if (ok) {
+      tc_fence_after_sync();
+      const float inv = 1.f / l;
+      __nv_bfloat16* orow = out + (static_cast<size_t>(bh) * T + t) * D;
+#pragma unroll
+      for (int cc = 0; cc < D; cc += 32) {
+        uint32_t o[32];
+        tmem_ld_x32(tO + cc, o);
+        uint32_t pk[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          pk[u] = pack_bf16x2(__uint_as_float(o[2 * u]) * inv, __uint_as_float(o[2 * u + 1]) * inv);
+        if (t < T) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + cc);
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+      }
+      if (lse && t < T) lse[static_cast<size_t>(bh) * T + t] = (m_used + log2f(l)) * kLn2;
+    } else {
+      record_timeout(bars, status);
+    }
+    teardown(warp, tb, Cfg::kTmemCols);
+  } else {
+    regs_dec<kRegsQuery>();
+    // ------------------------------------------------------------ running query
+    const int q4 = warp - 8;
+    const int r = q4 * 32 + lane;
+    const uint32_t lb = static_cast<uint32_t>(q4 * 32) << 16;
+    const uint32_t tQm = tb + lb + Cfg::kColQm, tQw = tb + lb + Cfg::kColQw;
+    if (b > 0) {
+      const float4* qrow = reinterpret_cast<const float4*>(
+          ql + ((static_cast<size_t>(bh) * Np + b) * kC + r) * D);
+      uint32_t qw[D / 2];
+#pragma unroll
+      for (int cc = 0; cc < D; cc += 32) {
+        uint32_t m32[32];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float4 f = __ldg(qrow + cc / 4 + u);
+          m32[4 * u] = __float_as_uint(f.x);
+          m32[4 * u + 1] = __float_as_uint(f.y);
+          m32[4 * u + 2] = __float_as_uint(f.z);
+          m32[4 * u + 3] = __float_as_uint(f.w);
+        }
+        tmem_st_x32(tQm + cc, m32);
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          qw[cc / 2 + u] = pack_bf16x2(__uint_as_float(m32[2 * u]), __uint_as_float(m32[2 * u + 1]));
+      }
+#pragma unroll
+      for (int cc = 0; cc < D / 2; cc += 32)
+        tmem_st_x32(tQw + cc, *reinterpret_cast<uint32_t(*)[32]>(&qw[cc]));
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&bars->q_ready);
+      bool ok = true;
+      for (int n = 0; n + 1 < b; ++n) {
+        ok = mbar_wait(&bars->qk_done, n & 1, abort_flag, LIM);
+        if (!ok) break;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int cc = 0; cc < D; cc += 32) {
+          uint32_t m32[32];
+          tmem_ld_x32(tQm + cc, m32);
+#pragma unroll
+          for (int u = 0; u < 16; ++u)
+            qw[cc / 2 + u] = pack_bf16x2(__uint_as_float(m32[2 * u]), __uint_as_float(m32[2 * u + 1]));
+        }
+#pragma unroll
+        for (int cc = 0; cc < D / 2; cc += 32)
+          tmem_st_x32(tQw + cc, *reinterpret_cast<uint32_t(*)[32]>(&qw[cc]));
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(&bars->q_ready);
+      }
+      if (!ok) record_timeout(bars, status);
+    }
+    teardown(warp, tb, Cfg::kTmemCols);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// Row-major bf16 matrix viewed as [rows][cols] (2D) or [z][rows][cols] (3D),
+// 128-byte swizzled boxes of 64 columns x box_rows rows.
+bool make_map(CUtensorMap* m, const void* ptr, int rank, uint64_t cols, uint64_t rows,
+              uint64_t zdim, uint32_t box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {cols, rows, zdim};
+  cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
+  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides,
+             box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+template <int D, bool kGate>
+cudaError_t launch_tc(const Geom& g, const Inputs& in, const Workspace& ws, int* status,
+                      cudaStream_t st) {
+  using Cfg = TcCfg<D>;
+  CUtensorMap mkr, mng, mv;
+  if (!make_map(&mkr, ws.kr, 2, D, static_cast<uint64_t>(g.BH) * g.Tp, 1, kC) ||
+      !make_map(&mng, ws.ngt, 2, D, static_cast<uint64_t>(g.nch) * D, 1, D) ||
+      !make_map(&mv, in.v, 3, D, g.T, g.BH, kC))
+    return cudaErrorInvalidValue;
+  auto kern = attn_tc_kernel<D, kGate>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(Cfg::kSmemBytes));
+  if (e != cudaSuccess) return e;
+  kern<<<g.nch, kThreads, Cfg::kSmemBytes, st>>>(
+      mkr, mng, mv, ws.ql, ws.sdt, kGate ? ws.lam2 : nullptr,
+      static_cast<__nv_bfloat16*>(in.out), in.lse, status, g.T, g.Np, g.BH, in.scale * kLog2e);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_tc(const Geom& g, const Inputs& in, const Workspace& ws, int* status,
+                           cudaStream_t st, int* launches) {
+  if (launches) *launches = 1;
+  if (g.C != kC) return cudaErrorInvalidValue;
+  if (g.d == 128) return g.gate ? launch_tc<128, true>(g, in, ws, status, st)
+                                : launch_tc<128, false>(g, in, ws, status, st);
+  if (g.d == 64) return g.gate ? launch_tc<64, true>(g, in, ws, status, st)
+                               : launch_tc<64, false>(g, in, ws, status, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pathattn

@@ -1,0 +1,103 @@
+// common.cuh -- definitions shared by the PaTH forward kernels and the C ABI:
+// problem geometry, the workspace layout, device status codes and the
+// host-side launchers of each kernel family.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace pathattn {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Device status word values (stored in a per-device int; 0 = fine).
+constexpr int PATH_DEV_OK = 0;
+constexpr int PATH_DEV_ERR_TIMEOUT = 1;
+
+// Time limit of every bounded wait inside the kernels.
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
+
+// Problem geometry.  Tokens are grouped into chunks of C; the last chunk is
+// padded with beta = 0 tokens (H = I), which leaves every real logit as is.
+struct Geom {
+  int B, H, T, d, C;
+  int BH;       // B * H
+  int Np;       // chunks per head, ceil(T / C)
+  int Tp;       // Np * C
+  int nch;      // BH * Np
+  bool bf16;    // element type of q, k, v, w, out (else fp32)
+  bool gate;    // PaTH-FoX gate present
+};
+
+// Workspace: every region 256-byte aligned.  Per chunk ch = bh * Np + n:
+//   kr   [ch][C][d]   elem  boundary-adjusted keys (k_j through H_{j+1}..H_last)
+//   ql   [ch][C][d]   f32   boundary-adjusted queries (q_i through H_i..H_first)
+//   ngt  [ch][d][d]   elem  -(W^T U W)^T, so q_next = q + q ngt^T
+//   sdt  [ch][C][C]   f32   intra-chunk log2-domain logits, [j][i], -inf for j > i
+//   lam2 [bh][Tp]     f32   log2(e) * inclusive cumsum of log f (gate only)
+// and the scratch of the preparation kernels:
+//   lmat [ch][C][C] f32   strictLower(diag(beta) W W^T), then U
+//   awk  [ch][C][C] f32   strictLower(W K^T)
+//   aqw  [ch][C][C] f32   lower(Q W^T)
+//   aqk  [ch][C][C] f32   lower(Q K^T)
+//   tk   [ch][C][C] f32   U strictLower(W K^T)
+//   uw   [ch][C][d] f32   U W
+struct Workspace {
+  void* kr;
+  float* ql;
+  void* ngt;
+  float* sdt;
+  float* lam2;
+  float *lmat, *awk, *aqw, *aqk, *tk, *uw;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Lays out the workspace over `base` (may be null to only count bytes).
+inline size_t workspace_layout(const Geom& g, char* base, Workspace* ws) {
+  const size_t es = g.bf16 ? 2 : 4;
+  const size_t nch = static_cast<size_t>(g.nch);
+  const size_t C = g.C, d = g.d;
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> char* {
+    char* p = base ? base + off : nullptr;
+    off = align_up(off + bytes, 256);
+    return p;
+  };
+  Workspace w{};
+  w.kr = take(nch * C * d * es);
+  w.ql = reinterpret_cast<float*>(take(nch * C * d * 4));
+  w.ngt = take(nch * d * d * es);
+  w.sdt = reinterpret_cast<float*>(take(nch * C * C * 4));
+  w.lam2 = g.gate ? reinterpret_cast<float*>(take(static_cast<size_t>(g.BH) * g.Tp * 4)) : nullptr;
+  w.lmat = reinterpret_cast<float*>(take(nch * C * C * 4));
+  w.awk = reinterpret_cast<float*>(take(nch * C * C * 4));
+  w.aqw = reinterpret_cast<float*>(take(nch * C * C * 4));
+  w.aqk = reinterpret_cast<float*>(take(nch * C * C * 4));
+  w.tk = reinterpret_cast<float*>(take(nch * C * C * 4));
+  w.uw = reinterpret_cast<float*>(take(nch * C * d * 4));
+  if (ws) *ws = w;
+  return off;
+}
+
+struct Inputs {
+  const void *q, *k, *v, *w;
+  const float *beta, *logf;
+  float scale;
+  void* out;
+  float* lse;
+};
+
+// Kernel-family launchers (each returns the first launch error, if any).
+// Chunk preparation: fills kr, ql, ngt, sdt (and lam2 when gated).
+cudaError_t launch_prep(const Geom& g, const Inputs& in, const Workspace& ws, cudaStream_t st,
+                        int* launches);
+// fp32 attention over the prepared chunks (SIMT, fp32 throughout).
+cudaError_t launch_attn_f32(const Geom& g, const Inputs& in, const Workspace& ws,
+                            cudaStream_t st, int* launches);
+// bf16 attention over the prepared chunks (tcgen05 / TMEM / TMA).
+cudaError_t launch_attn_tc(const Geom& g, const Inputs& in, const Workspace& ws,
+                           int* dev_status, cudaStream_t st, int* launches);
+
+}  // namespace pathattn

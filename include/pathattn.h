@@ -1,0 +1,161 @@
+/*
+ * pathattn.h -- C ABI of libpathattn.so, the PaTH attention forward pass on
+ * one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (from "PaTH Attention: Position Encoding via Accumulating
+ * Householder Transformations", discussion slides for arXiv:2505.16381v2,
+ * frame "PaTH inserts a learned transformation along every path"):
+ *
+ *   H_t   = I - beta_t w_t w_t^T            (||w_t|| = 1, beta_t in [0, 2])
+ *   s_ij  = scale * k_j^T H_{j+1} ... H_i q_i  [+ sum_{s=j+1}^{i} log f_s]
+ *   o_i   = sum_{j<=i} softmax_j(s_ij) v_j,   lse_i = log sum_{j<=i} exp(s_ij)
+ *
+ * The bracketed gate term is the PaTH-FoX forget gate (frame "FoX adds a
+ * separate mechanism for forgetting"); it is added outside the scale.
+ *
+ * Conventions shared by every entry point:
+ *   - Tensors are dense, contiguous, row-major: q, k, v, w, out are
+ *     [B, H, T, d]; beta, logf, lse are [B, H, T].
+ *   - Device pointers must be 16-byte aligned and live on the current device.
+ *   - dtype selects the element type of q, k, v, w and out: PATH_DTYPE_BF16
+ *     (fp32 accumulation, tensor cores) or PATH_DTYPE_F32 (fp32 throughout).
+ *     beta, logf and lse are always fp32.
+ *   - d must be 64 or 128; B, H, T >= 1; B*H*T*d must fit in 2^31 - 1 rows*cols
+ *     per operand index space (checked).
+ *   - stream is a cudaStream_t (NULL = the legacy default stream).  Launches are
+ *     asynchronous on that stream; nothing here synchronises the device except
+ *     where a function says so.
+ *   - Inputs are never written.  The caller owns every pointer it passes.
+ *   - Errors are returned as path_status_t values; no function throws or
+ *     aborts.  Argument checks happen before any CUDA call.
+ */
+#ifndef PATHATTN_H
+#define PATHATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PATH_OK = 0,
+  PATH_ERR_INVALID_ARG = -1, /* NULL or misaligned pointer, bad size, bad dtype */
+  PATH_ERR_UNSUPPORTED = -2, /* valid but not supported here (e.g. d not 64/128, not sm_103) */
+  PATH_ERR_CUDA = -3,        /* a CUDA runtime/driver call failed */
+  PATH_ERR_TIMEOUT = -4,     /* a kernel's bounded wait expired (device status word) */
+  PATH_ERR_OOM = -5          /* workspace allocation failed */
+} path_status_t;
+
+typedef enum { PATH_DTYPE_F32 = 0, PATH_DTYPE_BF16 = 1 } path_dtype_t;
+
+/*
+ * path_attn_fwd -- the PaTH / PaTH-FoX causal attention forward pass.
+ *
+ * Defined by the slides' frames "PaTH inserts a learned transformation along
+ * every path" (logits and softmax readout) and "FoX adds a separate mechanism
+ * for forgetting" (gate); computed blockwise as in frames "A triangular
+ * representation makes paths computable", "A right-to-left scan accumulates
+ * cross-block paths" and "Backup: fix orientation before implementing UT
+ * products".
+ *
+ *   q, k, v, w  device, [B,H,T,d], dtype      read only
+ *   beta        device, [B,H,T], fp32          read only; values in [0, 2]
+ *   logf        device, [B,H,T], fp32, or NULL (NULL = plain PaTH, no gate)
+ *   scale       multiplies k_j^T (...) q_i only (e.g. 1/sqrt(d))
+ *   out         device, [B,H,T,d], dtype       written
+ *   lse         device, [B,H,T], fp32, or NULL; natural-log normaliser
+ *
+ * The library takes a stream-ordered workspace on `stream` from its own
+ * memory pool (cached across calls) and returns it, stream-ordered, before
+ * returning.  Returns PATH_ERR_OOM if it cannot.  Device-side wait timeouts
+ * are reported by path_attn_device_status(), not by this call.
+ */
+int path_attn_fwd(const void* q, const void* k, const void* v, const void* w,
+                  const float* beta, const float* logf, float scale, void* out,
+                  float* lse, int B, int H, int T, int d, int dtype, void* stream);
+
+/*
+ * path_attn_fwd_host -- the same operation on HOST buffers (same shapes and
+ * dtypes as path_attn_fwd).  Copies the inputs to the current device, runs
+ * path_attn_fwd on `stream`, copies out (and lse if non-NULL) back and
+ * synchronises `stream` before returning.  Host buffers may be pageable;
+ * page-locked buffers make the copies faster.  Device buffers come from the
+ * library's pool and are returned before the call ends.
+ */
+int path_attn_fwd_host(const void* q, const void* k, const void* v, const void* w,
+                       const float* beta, const float* logf, float scale, void* out,
+                       float* lse, int B, int H, int T, int d, int dtype, void* stream);
+
+/* Human-readable name of a path_status_t value (static storage). */
+const char* path_attn_status_string(int status);
+
+/* Text of the last CUDA error seen by this thread inside the library (empty
+ * if none); valid until the next call on this thread. */
+const char* path_attn_last_error(void);
+
+/* Library version: major*10000 + minor*100 + patch. */
+int path_attn_version(void);
+
+/*
+ * Bytes of workspace path_attn_fwd takes for this problem (host arithmetic
+ * only; touches no device).  Returns PATH_OK and writes *bytes, or an error
+ * for invalid sizes.
+ */
+int path_attn_workspace_bytes(int B, int H, int T, int d, int dtype, int with_gate,
+                              size_t* bytes);
+
+/* Chunk length C used by the blockwise algorithm for (d, dtype): 128 for
+ * bf16, 64 for fp32.  Returns a negative status for unsupported input. */
+int path_attn_chunk_size(int d, int dtype);
+
+/*
+ * Device status word of `device` (0 = no error since the last clear; a
+ * negative path_status_t such as PATH_ERR_TIMEOUT if a kernel's bounded wait
+ * expired).  Synchronises that device first.  clear != 0 resets the word.
+ */
+int path_attn_device_status(int device, int clear);
+
+/*
+ * Per-kernel timing with CUDA events recorded on the launch stream around each
+ * kernel of path_attn_fwd.  path_attn_timing_enable(1) starts recording (and
+ * clears the totals); path_attn_timing_read() synchronises on the recorded
+ * events and returns the summed milliseconds of the chunk-preparation kernels
+ * and of the attention kernel, and the number of path_attn_fwd calls timed.
+ * Any output pointer may be NULL.  Timing off by default.
+ */
+int path_attn_timing_enable(int enable);
+int path_attn_timing_read(double* prep_ms, double* attn_ms, long* calls);
+
+/*
+ * Number of kernel launches one path_attn_fwd call makes for this problem
+ * (host arithmetic only).
+ */
+int path_attn_launches_per_call(int d, int dtype, int with_gate);
+
+/*
+ * path_attn_debug_factors -- diagnostics: run only the chunk preparation and
+ * copy its per-chunk factors (frame "Backup: fix orientation before
+ * implementing UT products") into caller buffers, for tests.  With C =
+ * path_attn_chunk_size(d, dtype), Np = ceil(T / C), Tp = Np * C, BH = B * H:
+ *   kr   [BH, Tp, d]    dtype  boundary-adjusted keys  k_j through H_{j+1}..H_last
+ *   ql   [BH, Tp, d]    fp32   boundary-adjusted queries q_i through H_i..H_first
+ *   ngt  [BH, Np, d, d] dtype  -(W^T U W)^T of each chunk (the transition is
+ *                              q <- q + q ngt^T ... i.e. q^T F^T = q^T + q^T ngt^T)
+ *   sdt  [BH, Np, C, C] fp32   intra-chunk log2-domain logits, transposed:
+ *                              sdt[.., j, i] = log2(e) * (scale * At_ij + gate_ij)
+ *                              for j <= i, -inf above the diagonal
+ *   lam2 [BH, Tp]       fp32   log2(e) * cumulative sum of logf (NULL when
+ *                              logf is NULL)
+ * Tokens past T are padding with beta = 0.  Asynchronous on `stream`.
+ */
+int path_attn_debug_factors(const void* q, const void* k, const void* w, const float* beta,
+                            const float* logf, float scale, int B, int H, int T, int d,
+                            int dtype, void* kr, float* ql, void* ngt, float* sdt,
+                            float* lam2, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PATHATTN_H */

@@ -1,0 +1,219 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle on
+the same seeded inputs.
+
+Tolerances: fp32 inputs -- max-abs 1e-4 on out and lse; bf16 inputs -- max-abs
+2e-2 on out and lse and mean-relative error sum|gpu - ref| / sum|ref| <= 5e-3
+on out.  The oracle sees the stored (rounded) input values.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import householder_softmax_attention_gb300 as pa
+from oracle import path_oracle_fwd
+from oracle.chunked import head_chunk_factors
+from seeded_inputs import WORKLOADS, Workload, make_inputs, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+TOL_F32 = 1e-4
+TOL_BF16_ABS = 2e-2
+TOL_BF16_REL = 5e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from householder_softmax_attention_gb300 import build
+    build.build()
+    pa.load_library()
+    assert pa.path_attn_device_status(0, True) == 0
+
+
+def _np(t):
+    return None if t is None else t.detach().float().cpu().numpy()
+
+
+def _run(x, dev="cuda"):
+    d = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in x.items()}
+    out, lse = pa.path_attn_fwd(d["q"], d["k"], d["v"], d["w"], d["beta"], d["logf"], d["scale"])
+    torch.cuda.synchronize()
+    assert pa.path_attn_device_status(0, True) == 0, "a kernel wait expired"
+    return out, lse
+
+
+def _check(go, gl, ro, rl, bf16, label=""):
+    go, gl = np.asarray(go, np.float64), np.asarray(gl, np.float64)
+    assert np.isfinite(go).all() and np.isfinite(gl).all(), label
+    err = np.abs(go - ro)
+    lerr = np.abs(gl - rl)
+    if bf16:
+        rel = err.sum() / np.abs(ro).sum()
+        assert err.max() <= TOL_BF16_ABS, f"{label} max_abs {err.max():.3e}"
+        assert rel <= TOL_BF16_REL, f"{label} mean_rel {rel:.3e}"
+        assert lerr.max() <= TOL_BF16_ABS, f"{label} lse max_abs {lerr.max():.3e}"
+    else:
+        assert err.max() <= TOL_F32, f"{label} max_abs {err.max():.3e}"
+        assert lerr.max() <= TOL_F32, f"{label} lse max_abs {lerr.max():.3e}"
+    return float(err.max())
+
+
+def _full_case(wl: Workload):
+    x = make_inputs(wl)
+    out, lse = _run(x)
+    ro, rl = path_oracle_fwd(_np(x["q"]), _np(x["k"]), _np(x["v"]), _np(x["w"]),
+                             _np(x["beta"]), _np(x["logf"]), x["scale"])
+    return _check(_np(out), _np(lse), ro, rl, wl.dtype == "bf16", wl.name)
+
+
+# ------------------------------------------------------------ small, full oracle
+def test_tiny_f32_workload_full():
+    """B=1, H=2, T=256, d=64, fp32: every output against the oracle."""
+    _full_case(WORKLOADS["tiny_f32"])
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 200])
+def test_f32_lengths(d, T):
+    _full_case(Workload("f32_len", 1, 2, T, d, "f32", seed=T + d))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("T", [1, 127, 128, 129, 1000])
+def test_bf16_lengths_several_tiles_and_ragged(d, T):
+    _full_case(Workload("bf16_len", 1, 2, T, d, "bf16", seed=T * 3 + d))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_fox_gate_small(dtype, d):
+    _full_case(Workload("fox_small", 1, 2, 600, d, dtype, fox=True, seed=11 + d))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("rng", [(1.98, 2.0), (0.0, 0.05), (2.0, 2.0)])
+def test_beta_extremes_keep_long_paths(dtype, rng):
+    """beta near 2 (reflections) or near 0 (near-identity) keeps distant
+    logits large, so errors in far transitions are not hidden by decay."""
+    _full_case(Workload("beta_ext", 1, 2, 700, 128, dtype, beta_range=rng, seed=5))
+
+
+def test_near_reflection_mix_and_batches():
+    _full_case(Workload("refl_mix", 2, 3, 520, 64, "bf16", near_reflection=True, seed=3))
+
+
+def test_beta_zero_matches_sdpa_on_device():
+    """beta = 0: PaTH is plain causal softmax attention."""
+    wl = Workload("beta0", 1, 4, 777, 128, "bf16", beta_range=(0.0, 0.0), seed=9)
+    x = make_inputs(wl)
+    out, _ = _run(x)
+    q, k, v = (x[n].cuda().float() for n in ("q", "k", "v"))
+    ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True,
+                                                           scale=x["scale"])
+    err = (out.float() - ref).abs()
+    assert err.max().item() <= TOL_BF16_ABS
+    assert (err.sum() / ref.abs().sum()).item() <= TOL_BF16_REL
+
+
+# ------------------------------------------------------------ chunk factors
+@pytest.mark.parametrize("dtype,d,fox", [("f32", 64, False), ("f32", 128, True),
+                                         ("bf16", 128, False), ("bf16", 64, True)])
+def test_chunk_factors_match_blockwise_oracle(dtype, d, fox):
+    wl = Workload("factors", 1, 2, 300, d, dtype, fox=fox, seed=21)
+    x = make_inputs(wl)
+    dev = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in x.items()}
+    f = pa.path_attn_debug_factors(dev["q"], dev["k"], dev["w"], dev["beta"], dev["logf"],
+                                   x["scale"])
+    torch.cuda.synchronize()
+    C = f["C"]
+    log2e = 1.0 / math.log(2.0)
+    bf = dtype == "bf16"
+    for h in range(2):
+        q, k, w = (_np(x[n])[0, h] for n in ("q", "k", "w"))
+        beta = _np(x["beta"])[0, h]
+        fac = head_chunk_factors(q, k, w, beta, C)
+        lam = None
+        if fox:
+            lf = np.concatenate([_np(x["logf"])[0, h], np.zeros(len(fac) * C - wl.T)])
+            lam = np.cumsum(lf)
+            np.testing.assert_allclose(_np(f["lam2"])[h], lam * log2e, atol=1e-4, rtol=1e-6)
+        for n, fc in enumerate(fac):
+            sl = slice(n * C, (n + 1) * C)
+            kr = _np(f["kr"])[h, sl]
+            ql = _np(f["ql"])[h, sl]
+            ngt = _np(f["ngt"])[h, n]
+            sdt = _np(f["sdt"])[h, n]
+            tol_in = (2 ** -8) if bf else 2e-6
+            np.testing.assert_allclose(kr, fc["Kr"], atol=2e-4 + tol_in * np.abs(fc["Kr"]).max())
+            np.testing.assert_allclose(ngt, -fc["G"].T, atol=2e-4 + tol_in * np.abs(fc["G"]).max())
+            np.testing.assert_allclose(ql, fc["Ql"], atol=5e-4 if bf else 2e-4)
+            S = log2e * x["scale"] * fc["Adiag"]
+            if fox:
+                lg = lam[sl]
+                S = S + log2e * (lg[:, None] - lg[None, :])
+            mask = np.tril(np.ones((C, C), dtype=bool))
+            got = sdt.T
+            assert np.all(np.isneginf(got[~mask]))
+            np.testing.assert_allclose(got[mask], S[mask], atol=5e-4 if bf else 2e-4)
+
+
+# ------------------------------------------------------------ full-size workloads
+def _heads_for(B, H, n_random, seed):
+    g = np.random.default_rng(seed)
+    picks = {(0, 0), (B - 1, H - 1)}
+    while len(picks) < min(B * H, 2 + n_random):
+        picks.add((int(g.integers(B)), int(g.integers(H))))
+    return sorted(picks)
+
+
+def _sampled_case(wl: Workload, n_heads=2, n_rows=24):
+    """Full-size forward on the GPU; the oracle evaluates a seeded sample of
+    rows in a few (b, h) problems, each row exactly."""
+    x = make_inputs(wl, device="cuda")
+    out, lse = _run(x)
+    heads = _heads_for(wl.B, wl.H, n_heads, wl.seed)
+    rows = sample_rows(wl.T, 128, n_rows, seed=wl.seed)
+    sel = lambda t: None if t is None else torch.stack([t[b, h] for b, h in heads]).float().cpu().numpy()
+    qs, ks, vs, ws_, bs = (sel(x[n]) for n in ("q", "k", "v", "w", "beta"))
+    ls = sel(x["logf"])
+    flat = [i * wl.T + r for i in range(len(heads)) for r in rows]
+    ro, rl = path_oracle_fwd(qs, ks, vs, ws_, bs, ls, x["scale"], rows=flat)
+    go = torch.stack([out[b, h] for b, h in heads]).float().cpu().numpy().reshape(-1, wl.d)[flat]
+    gl = torch.stack([lse[b, h] for b, h in heads]).float().cpu().numpy().reshape(-1)[flat]
+    return _check(go, gl, ro, rl, True, wl.name)
+
+
+@pytest.mark.parametrize("name", ["t2k_d128", "t2k_d64", "t4k_d128_refl", "t4k_d64_refl",
+                                  "fox_t8k_d128", "t16k_d128", "t16k_d64"])
+def test_full_size_workloads_sampled(name):
+    _sampled_case(WORKLOADS[name])
+
+
+def test_repeat_calls_are_deterministic():
+    wl = Workload("det", 1, 2, 1000, 128, "bf16", seed=4)
+    x = make_inputs(wl)
+    o1, l1 = _run(x)
+    o2, l2 = _run(x)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_host_buffer_entry_matches_device_entry():
+    wl = Workload("host", 1, 2, 390, 64, "bf16", fox=True, seed=8)
+    x = make_inputs(wl)
+    o1, l1 = _run(x)
+    o2, l2 = pa.path_attn_fwd_host(x["q"], x["k"], x["v"], x["w"], x["beta"], x["logf"],
+                                   x["scale"])
+    assert torch.equal(o1.cpu(), o2) and torch.equal(l1.cpu(), l2)
+
+
+def test_lse_optional_and_no_status_error():
+    wl = Workload("nolse", 1, 1, 256, 128, "bf16", seed=2)
+    x = make_inputs(wl)
+    d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in x.items()}
+    o1, l1 = pa.path_attn_fwd(d["q"], d["k"], d["v"], d["w"], d["beta"], None, d["scale"])
+    o2, l2 = pa.path_attn_fwd(d["q"], d["k"], d["v"], d["w"], d["beta"], None, d["scale"],
+                              want_lse=False)
+    torch.cuda.synchronize()
+    assert l2 is None and torch.equal(o1, o2)
+    assert pa.path_attn_device_status(0) == 0
