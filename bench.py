@@ -1,0 +1,348 @@
+"""Benchmark of the PaTH attention forward pass on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl reference]
+
+One step is one full forward (chunk preparation + attention scan) over one
+batch of seeded synthetic inputs of the named workload, inputs resident in
+HBM.  The JSON line reports issued TFLOP/s (formulas in ``step_flops``),
+ms per step, the roofline of the attention kernel, an end-to-end number
+through the host-buffer C-ABI entry, sampled SM clocks and a CPU-oracle
+baseline.  ``--impl reference`` times the fp64 CPU oracle instead, on a
+bounded sample of the same workload.  Under torchrun (N > 1) every rank runs
+the full workload on its own GPU (independent replicas; weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "PaTH-attn fwd ms & TFLOP/s at B=2,T=16384,H=16,d=128 bf16; % of BF16 peak"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "t16k_d128"
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ------------------------------------------------------------------ FLOP model
+def step_flops(B, H, T, d, C=128):
+    """Issued FLOPs of one forward, by kernel.
+
+    Per (b, h) with N = ceil(T / C) chunks:
+      attention kernel (tensor cores):
+        S = Qw kr^T     2 C^2 d * N(N-1)/2     (every off-diagonal chunk pair)
+        O += P V        2 C^2 d * N(N+1)/2     (diagonal chunk included)
+        Qm += Qw ngt^T  2 C d^2 * (N-1)(N-2)/2 (crossings of chunks 1 .. b-1)
+      chunk preparation, per chunk:
+        4 Gram blocks 8 C^2 d, U W / kr / ql 6 C^2 d, ngt 2 C d^2,
+        U strictLower(W K^T) and the diagonal correction 4 C^3,
+        triangular solve C^3 / 3
+    """
+    N = -(-T // C)
+    BH = B * H
+    qk = 2 * C * C * d * N * (N - 1) // 2
+    pv = 2 * C * C * d * N * (N + 1) // 2
+    tr = 2 * C * d * d * (N - 1) * (N - 2) // 2 if N >= 2 else 0
+    prep = N * (14 * C * C * d + 2 * C * d * d + 4 * C ** 3 + C ** 3 // 3)
+    return {"attn": BH * (qk + pv + tr), "prep": BH * prep,
+            "flash_equiv": 2 * BH * T * T * d}
+
+
+# ------------------------------------------------------------------ helpers
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p.get("bf16_tflops"), p.get("hbm_gbs"), "measured"
+    except Exception:
+        return 1900.0, 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def dist_setup():
+    """(rank, world, local_rank); initialises torch.distributed under torchrun."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(x: float, world: int) -> float:
+    """Max of a host float over ranks (identity for one rank)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" \
+        else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_sample(wl, budget_s, threads, seed=0):
+    """Time the fp64 oracle on a seeded row sample of one (b, h) problem of the
+    workload; returns (seconds per unit of row work, description, threads).
+    Row i costs i + 1 path steps, so the full workload is sum over rows."""
+    import numpy as np
+    import torch
+
+    from oracle import path_oracle_fwd
+    from seeded_inputs import make_inputs
+
+    one = wl.with_(B=1, H=1)
+    x = make_inputs(one)
+    f = lambda t: None if t is None else t.float().numpy()
+    q, k, v, w, b, lf = (f(x[n]) for n in ("q", "k", "v", "w", "beta", "logf"))
+    g = np.random.default_rng(seed)
+    rows, units, spent = [], 0, 0.0
+    # grow the sample until the time budget is used
+    batch = max(threads, 8)
+    while spent < budget_s:
+        r = g.integers(0, wl.T, size=batch).tolist()
+        t0 = time.perf_counter()
+        path_oracle_fwd(q, k, v, w, b, lf, x["scale"], rows=r, threads=threads)
+        spent += time.perf_counter() - t0
+        rows += r
+        units += sum(i + 1 for i in r)
+    desc = (f"{len(rows)} random query rows of one (b,h) problem of {wl.name}, "
+            f"{spent:.1f} s; extrapolated by row cost (i+1) to all B*H*T rows")
+    return spent / units, desc
+
+
+def full_units(wl):
+    return wl.B * wl.H * wl.T * (wl.T + 1) // 2
+
+
+# ------------------------------------------------------------------ arms
+def run_reference(args, wl, flops):
+    rank, world, _ = dist_setup()
+    if rank != 0:
+        return 0
+    threads = os.cpu_count() or 1
+    per_step = []
+    for s in range(args.warmup + args.steps):
+        sec_per_unit, desc = oracle_sample(wl, args.ref_step_s, threads, seed=s)
+        if s >= args.warmup:
+            per_step.append(sec_per_unit * full_units(wl))
+    est = statistics.median(per_step)
+    value = (flops["attn"] + flops["prep"]) / est / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": est * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "T": wl.T, "d": wl.d},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gpu(args, wl, flops):
+    import torch
+
+    import householder_softmax_attention_gb300 as pa
+    from seeded_inputs import make_inputs
+
+    rank, world, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pa.load_library()
+    x = make_inputs(wl, device=dev)
+    q, k, v, w, beta, logf, scale = (x[n] for n in ("q", "k", "v", "w", "beta", "logf", "scale"))
+    out = torch.empty_like(q)
+    lse = torch.empty(beta.shape, device=dev, dtype=torch.float32)
+    st = torch.cuda.current_stream(dev)
+
+    def step():
+        pa.path_attn_fwd(q, k, v, w, beta, logf, scale, out=out, lse=lse, stream=st)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    assert pa.path_attn_device_status(local, True) == 0, "a kernel wait expired"
+
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, w, beta) if t is not None)
+    ws_bytes = pa.path_attn_workspace_bytes(wl.B, wl.H, wl.T, wl.d, 1, logf is not None)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pa.path_attn_timing_enable(True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        e0.record(st)
+        for _ in range(args.steps):
+            step()
+        e1.record(st)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    ms = e0.elapsed_time(e1) / args.steps
+    prep_ms, attn_ms, calls = pa.path_attn_timing_read()
+    pa.path_attn_timing_enable(False)
+    assert calls == args.steps
+    assert pa.path_attn_device_status(local, True) == 0, "a kernel wait expired"
+    ms_max = reduce_max(ms, world)
+    total = flops["attn"] + flops["prep"]
+    value = world * total / (ms_max * 1e-3) / 1e12
+
+    # roofline of the dominant kernel (the attention scan)
+    attn_avg_ms = attn_ms / calls
+    peak, _, peak_src = _peaks()
+    achieved = flops["attn"] / (attn_avg_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": args.traffic,
+                "kernel": "attn_tc_kernel", "peak_source": f"{peak_src} bf16 burst",
+                "avg_launch_ms": attn_avg_ms, "prep_avg_ms": prep_ms / calls}
+
+    # end to end through the host-buffer entry: H2D of the inputs from pinned
+    # memory, the forward, D2H of out and lse, every step
+    hx = {n: (t.cpu().pin_memory() if torch.is_tensor(t) else t) for n, t in x.items()}
+    hout = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    hlse = torch.empty(beta.shape, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        pa.path_attn_fwd_host(hx["q"], hx["k"], hx["v"], hx["w"], hx["beta"], hx["logf"],
+                              scale, out=hout, lse=hlse, stream=st)
+
+    for _ in range(max(1, min(args.warmup, 3))):
+        e2e_step()
+    n_e2e = max(1, min(args.steps, 10))
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        e2e_step()
+    e2e_ms = reduce_max((time.perf_counter() - t0) * 1e3 / n_e2e, world)
+    d2h = hout.numel() * hout.element_size() + hlse.numel() * 4
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "T": wl.T, "d": wl.d,
+                   "fox": wl.fox, "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2: {in_bytes / 2**20:.0f} MiB inputs + "
+                         f"{ws_bytes / 2**20:.0f} MiB workspace per step"},
+        "flops_per_step": {"attn": flops["attn"], "prep": flops["prep"]},
+        "flash_equiv_tflops": world * flops["flash_equiv"] / (ms_max * 1e-3) / 1e12,
+        "roofline": roofline,
+        "e2e": {"value": world * total / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": in_bytes,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * pa.path_attn_launches_per_call(
+            wl.d, 1 if wl.dtype == "bf16" else 0, logf is not None),
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        sec_per_unit, desc = oracle_sample(wl, args.cpu_budget_s, threads)
+        est = sec_per_unit * full_units(wl)
+        line["cpu_baseline"] = {"value": total / est / 1e12, "unit": UNIT, "cores": threads,
+                                "kind": "oracle", "sample": desc,
+                                "est_full_workload_s": est}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--ref-step-s", type=float, default=2.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per attention launch from an ncu capture, if current")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    from seeded_inputs import WORKLOADS
+    wl = WORKLOADS[args.workload]
+    f = step_flops(wl.B, wl.H, wl.T, wl.d)
+    if args.impl == "reference":
+        return run_reference(args, wl, f)
+    return run_gpu(args, wl, f)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
