@@ -21,6 +21,7 @@ import threading
 
 __all__ = [
     "PathAttnError", "load_library", "path_attn_fwd", "path_attn_fwd_host",
+    "path_attn_fwd_noalloc",
     "path_attn_debug_factors", "path_attn_device_status", "path_attn_workspace_bytes",
     "path_attn_chunk_size", "path_attn_launches_per_call", "path_attn_timing_enable",
     "path_attn_timing_read", "path_attn_version", "path_attn_status_string",
@@ -91,6 +92,9 @@ def load_library(path: str | None = None):
         lib.path_attn_debug_factors.argtypes = [vp, vp, vp, fp, fp, f, i, i, i, i, i,
                                                 vp, vp, vp, vp, vp, vp]
         lib.path_attn_debug_factors.restype = i
+        lib.path_attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, fp, fp, f, vp, fp, vp,
+                                              i, i, i, i, i, vp]
+        lib.path_attn_fwd_noalloc.restype = i
         _lib = lib
         return lib
 
@@ -185,6 +189,32 @@ def path_attn_fwd_host(q, k, v, w, beta, logf=None, scale=None, out=None, lse=No
                                 float(scale), _ptr(out), _ptr(lse), B, H, T, d,
                                 _dtype_code(q), ctypes.c_void_p(st.cuda_stream))
     _check(rc, "path_attn_fwd_host")
+    return out, lse
+
+
+def path_attn_fwd_noalloc(q, k, v, w, beta, logf=None, scale=None, out=None, lse=None,
+                          status=None, want_lse=True, stream=None):
+    """The forward through the allocation-free C entry, whose workspace is a
+    static 64 MiB device array inside the library (for callers that may not
+    allocate device memory).  Arguments as ``path_attn_fwd``; ``status`` is an
+    optional device int32 tensor that receives the kernels' wait status.
+    Output tensors are allocated here only when not passed in."""
+    import torch
+    lib = load_library()
+    _check_inputs(q, k, v, w, beta, logf, True)
+    B, H, T, d = q.shape
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, T), device=q.device, dtype=torch.float32)
+    st = stream if stream is not None else torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        rc = lib.path_attn_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(beta), _ptr(logf),
+                                       float(scale), _ptr(out), _ptr(lse), _ptr(status),
+                                       B, H, T, d, _dtype_code(q), ctypes.c_void_p(st.cuda_stream))
+    _check(rc, "path_attn_fwd_noalloc")
     return out, lse
 
 

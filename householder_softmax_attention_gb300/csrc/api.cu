@@ -345,3 +345,88 @@ int path_attn_debug_factors(const void* q, const void* k, const void* w, const f
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry: the workspace lives in a static device array.
+namespace {
+
+__device__ __align__(256) unsigned char g_noalloc_scratch[PATH_NOALLOC_SCRATCH_BYTES];
+__device__ __align__(256) int g_noalloc_status;
+
+struct NoAllocState {
+  bool ready = false;
+  char* scratch = nullptr;  // device address of g_noalloc_scratch
+  int* status = nullptr;    // device address of g_noalloc_status
+  int cc_major = 0, cc_minor = 0;
+};
+NoAllocState g_noalloc[kMaxDevices];
+
+// Once per device, with that device current: look up the arrays' device
+// addresses (host code may not use the symbols themselves as pointers).
+int noalloc_setup(NoAllocState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  if (dev < 0 || dev >= kMaxDevices) return PATH_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  NoAllocState& s = g_noalloc[dev];
+  if (!s.ready) {
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, g_noalloc_scratch)) != cudaSuccess) return set_cuda_error(e);
+    s.scratch = static_cast<char*>(p);
+    if ((e = cudaGetSymbolAddress(&p, g_noalloc_status)) != cudaSuccess) return set_cuda_error(e);
+    s.status = static_cast<int*>(p);
+    if ((e = cudaDeviceGetAttribute(&s.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) !=
+            cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&s.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) !=
+            cudaSuccess)
+      return set_cuda_error(e);
+    s.ready = true;
+  }
+  *out = &s;
+  return PATH_OK;
+}
+
+}  // namespace
+
+extern "C" int path_attn_fwd_noalloc(const void* q, const void* k, const void* v, const void* w,
+                                     const float* beta, const float* logf, float scale,
+                                     void* out, float* lse, int* status, int B, int H, int T,
+                                     int d, int dtype, void* stream) {
+  if (!q || !k || !v || !w || !beta || !out) return PATH_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(w) || !aligned16(beta) ||
+      !aligned16(out) || (logf && !aligned16(logf)) || (lse && !aligned16(lse)) ||
+      (status && (reinterpret_cast<uintptr_t>(status) & 3u)))
+    return PATH_ERR_INVALID_ARG;
+  if (!(scale == scale)) return PATH_ERR_INVALID_ARG;
+  Geom g;
+  int rc = make_geom(B, H, T, d, dtype, logf != nullptr, &g);
+  if (rc != PATH_OK) return rc;
+  const size_t bytes = workspace_layout(g, nullptr, nullptr);
+  if (bytes > PATH_NOALLOC_SCRATCH_BYTES) {
+    std::snprintf(g_last_error, sizeof(g_last_error),
+                  "path_attn_fwd_noalloc: this problem needs %zu bytes of workspace; the static "
+                  "scratch holds %zu",
+                  bytes, static_cast<size_t>(PATH_NOALLOC_SCRATCH_BYTES));
+    return PATH_ERR_UNSUPPORTED;
+  }
+  NoAllocState* s = nullptr;
+  if ((rc = noalloc_setup(&s)) != PATH_OK) return rc;
+  if (s->cc_major != 10 || s->cc_minor != 3) {
+    std::snprintf(g_last_error, sizeof(g_last_error),
+                  "libpathattn is built for sm_103a; this device is sm_%d%d", s->cc_major,
+                  s->cc_minor);
+    return PATH_ERR_UNSUPPORTED;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* word = status ? status : s->status;
+  cudaError_t e = cudaMemsetAsync(word, 0, sizeof(int), st);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  Workspace ws;
+  workspace_layout(g, s->scratch, &ws);
+  Inputs in{q, k, v, w, beta, logf, scale, out, lse};
+  if ((e = launch_prep(g, in, ws, st, nullptr)) != cudaSuccess) return set_cuda_error(e);
+  e = g.bf16 ? launch_attn_tc(g, in, ws, word, st, nullptr) : launch_attn_f32(g, in, ws, st, nullptr);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  return PATH_OK;
+}

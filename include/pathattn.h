@@ -154,6 +154,39 @@ int path_attn_debug_factors(const void* q, const void* k, const void* w, const f
                             int dtype, void* kr, float* ql, void* ngt, float* sdt,
                             float* lam2, void* stream);
 
+/*
+ * path_attn_fwd_noalloc -- path_attn_fwd for callers that cannot allocate
+ * device memory.  The paper has no counterpart; this is a library interface.
+ *
+ * Some callers must not call cudaMalloc (or any allocating routine): a host
+ * framework that has already reserved the device's memory for its own
+ * allocator, where an extra allocation would fail or fragment that pool, or
+ * a steady-state serving loop with a fixed memory budget.  This entry runs
+ * the same kernels as path_attn_fwd but takes its workspace from a static
+ * device array of PATH_NOALLOC_SCRATCH_BYTES (64 MiB) inside the library, so
+ * it allocates nothing.  Every GPU on which this entry has been called holds
+ * that array until the process exits.
+ *
+ *   Arguments as path_attn_fwd, plus
+ *   status  device int, or NULL: set to 0 at the start of the call, and to a
+ *           non-zero value by a kernel whose bounded wait expired (NULL = a
+ *           second static word in the library).
+ *
+ * Problems whose workspace (path_attn_workspace_bytes) exceeds the array are
+ * rejected with PATH_ERR_UNSUPPORTED before any launch; the message says how
+ * many bytes were needed.  The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current; make that
+ * first call before any stream capture.  All calls share the one array, which
+ * keeps the last call's contents: calls that may overlap on the GPU (other
+ * streams, other host threads) race on it and must be serialised by the
+ * caller.  Asynchronous on `stream`.
+ */
+#define PATH_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+int path_attn_fwd_noalloc(const void* q, const void* k, const void* v, const void* w,
+                          const float* beta, const float* logf, float scale, void* out,
+                          float* lse, int* status, int B, int H, int T, int d, int dtype,
+                          void* stream);
+
 #ifdef __cplusplus
 }
 #endif
