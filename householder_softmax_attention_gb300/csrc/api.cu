@@ -183,7 +183,8 @@ int path_attn_workspace_bytes(int B, int H, int T, int d, int dtype, int with_ga
 int path_attn_launches_per_call(int d, int dtype, int with_gate) {
   const int C = chunk_size(d, dtype);
   if (C < 0) return C;
-  return 11 + (with_gate ? 1 : 0) + 1;
+  const int prep = dtype == PATH_DTYPE_BF16 ? 1 : 11;
+  return prep + (with_gate ? 1 : 0) + 1;
 }
 
 int path_attn_fwd(const void* q, const void* k, const void* v, const void* w,

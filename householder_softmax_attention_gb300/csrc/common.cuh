@@ -36,7 +36,7 @@ struct Geom {
 //   ngt  [ch][d][d]   elem  -(W^T U W)^T, so q_next = q + q ngt^T
 //   sdt  [ch][C][C]   f32   intra-chunk log2-domain logits, [j][i], -inf for j > i
 //   lam2 [bh][Tp]     f32   log2(e) * inclusive cumsum of log f (gate only)
-// and the scratch of the preparation kernels:
+// and, for fp32 inputs only, the scratch of the SIMT preparation kernels:
 //   lmat [ch][C][C] f32   strictLower(diag(beta) W W^T), then U
 //   awk  [ch][C][C] f32   strictLower(W K^T)
 //   aqw  [ch][C][C] f32   lower(Q W^T)
@@ -71,6 +71,11 @@ inline size_t workspace_layout(const Geom& g, char* base, Workspace* ws) {
   w.ngt = take(nch * d * d * es);
   w.sdt = reinterpret_cast<float*>(take(nch * C * C * 4));
   w.lam2 = g.gate ? reinterpret_cast<float*>(take(static_cast<size_t>(g.BH) * g.Tp * 4)) : nullptr;
+  if (g.bf16) {  // the fused tensor-core preparation keeps its intermediates on chip
+    w.lmat = w.awk = w.aqw = w.aqk = w.tk = w.uw = nullptr;
+    if (ws) *ws = w;
+    return off;
+  }
   w.lmat = reinterpret_cast<float*>(take(nch * C * C * 4));
   w.awk = reinterpret_cast<float*>(take(nch * C * C * 4));
   w.aqw = reinterpret_cast<float*>(take(nch * C * C * 4));
@@ -90,9 +95,12 @@ struct Inputs {
 };
 
 // Kernel-family launchers (each returns the first launch error, if any).
-// Chunk preparation: fills kr, ql, ngt, sdt (and lam2 when gated).
+// Chunk preparation: fills kr, ql, ngt, sdt (and lam2 when gated); bf16 runs
+// the fused tensor-core kernel (launch_prep_mma), fp32 the SIMT kernels.
 cudaError_t launch_prep(const Geom& g, const Inputs& in, const Workspace& ws, cudaStream_t st,
                         int* launches);
+cudaError_t launch_prep_mma(const Geom& g, const Inputs& in, const Workspace& ws,
+                            cudaStream_t st);
 // fp32 attention over the prepared chunks (SIMT, fp32 throughout).
 cudaError_t launch_attn_f32(const Geom& g, const Inputs& in, const Workspace& ws,
                             cudaStream_t st, int* launches);

@@ -16,8 +16,8 @@
 // and, for PaTH-FoX (frame "FoX adds a separate mechanism for forgetting"),
 //   lam2 = log2(e) * inclusive cumsum of log f  (gate_ij = lam_i - lam_j).
 //
-// All arithmetic is fp32 (inputs widened exactly); bf16 outputs are rounded
-// to nearest.  This version runs on the CUDA cores.
+// All arithmetic is fp32 (inputs widened exactly).  These SIMT kernels serve
+// fp32 inputs; bf16 inputs go to the fused tensor-core kernel in prep_mma.cu.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -302,6 +302,11 @@ cudaError_t launch_prep(const Geom& g, const Inputs& in, const Workspace& ws, cu
     gate_cumsum_kernel<<<g.BH, 1024, 0, st>>>(in.logf, ws.lam2, g.T, g.Tp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     ++n;
+  }
+  if (g.bf16) {
+    if ((e = launch_prep_mma(g, in, ws, st)) != cudaSuccess) return e;
+    if (launches) *launches = n + 1;
+    return cudaSuccess;
   }
   const InTensor Q{in.q, g.T, d, C, g.Np, g.bf16}, K{in.k, g.T, d, C, g.Np, g.bf16},
       W{in.w, g.T, d, C, g.Np, g.bf16};

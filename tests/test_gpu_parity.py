@@ -147,7 +147,10 @@ def test_chunk_factors_match_blockwise_oracle(dtype, d, fox):
             tol_in = (2 ** -8) if bf else 2e-6
             np.testing.assert_allclose(kr, fc["Kr"], atol=2e-4 + tol_in * np.abs(fc["Kr"]).max())
             np.testing.assert_allclose(ngt, -fc["G"].T, atol=2e-4 + tol_in * np.abs(fc["G"]).max())
-            np.testing.assert_allclose(ql, fc["Ql"], atol=5e-4 if bf else 2e-4)
+            # bf16 inputs: the fused preparation rounds computed operands to tf32
+            # (2^-11) before its tensor-core products; sums of up to C such terms
+            tol_tf32 = 5e-3 if bf else 2e-4
+            np.testing.assert_allclose(ql, fc["Ql"], atol=tol_tf32)
             S = log2e * x["scale"] * fc["Adiag"]
             if fox:
                 lg = lam[sl]
@@ -155,7 +158,7 @@ def test_chunk_factors_match_blockwise_oracle(dtype, d, fox):
             mask = np.tril(np.ones((C, C), dtype=bool))
             got = sdt.T
             assert np.all(np.isneginf(got[~mask]))
-            np.testing.assert_allclose(got[mask], S[mask], atol=5e-4 if bf else 2e-4)
+            np.testing.assert_allclose(got[mask], S[mask], atol=tol_tf32)
 
 
 # ------------------------------------------------------------ full-size workloads

@@ -78,7 +78,7 @@ def test_noalloc_matches_allocating_entry_two_calls_in_a_row(lib):
 
 @pytest.mark.gpu
 def test_noalloc_rejects_problems_beyond_the_static_scratch(lib):
-    wl = Workload("noalloc_big", 1, 8, 4096, 128, "bf16", seed=34)
+    wl = Workload("noalloc_big", 2, 16, 4096, 128, "bf16", seed=34)
     need = pa.path_attn_workspace_bytes(wl.B, wl.H, wl.T, wl.d, pa.PATH_DTYPE_BF16)
     assert need > 64 << 20
     x = {n: (t.cuda() if torch.is_tensor(t) else t) for n, t in make_inputs(wl).items()}
