@@ -331,6 +331,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--ref-step-s", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--B", type=int, default=None, help="override the workload's batch")
+    ap.add_argument("--H", type=int, default=None, help="override the workload's heads")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per attention launch from an ncu capture, if current")
     args = ap.parse_args(argv)
@@ -338,6 +340,8 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     from seeded_inputs import WORKLOADS
     wl = WORKLOADS[args.workload]
+    if args.B or args.H:
+        wl = wl.with_(B=args.B or wl.B, H=args.H or wl.H, name=f"{wl.name}_B{args.B or wl.B}H{args.H or wl.H}")
     f = step_flops(wl.B, wl.H, wl.T, wl.d)
     if args.impl == "reference":
         return run_reference(args, wl, f)

@@ -6,8 +6,8 @@
 //
 //   diagonal   P_b = softmax-step(sdt_b)            (logits precomputed, fp32)
 //   for c = b-1 .. 0:
-//     S   = Qw . kr_c^T                            tcgen05, A = Qw from TMEM
 //     Qm += Qw . ngt_c^T   (only if c > 0)         crossing chunk c backwards
+//     S   = Qw . kr_c^T                            tcgen05, A = Qw from TMEM
 //     P_c = softmax-step(S)                        online softmax, lazy rescale
 //     O  += P_{c+1} . V_{c+1}                      tcgen05, A = P from TMEM
 //   O += P_0 . V_0;  out = O / l,  lse = (m + log2 l) ln 2
@@ -38,6 +38,7 @@ namespace {
 
 constexpr int kC = 128;       // chunk length = query tile = key tile
 constexpr int kThreads = 384;
+constexpr int kHeadGroup = 8;
 constexpr int kRegsLow = 56, kRegsSoftmax = 240, kRegsQuery = 112;
 static_assert(128 * (kRegsLow + kRegsSoftmax + kRegsQuery) <= kThreads * 168, "register split");
 
@@ -60,7 +61,7 @@ struct TcCfg {
 
 struct Bars {
   uint64_t kg_full[2], kg_empty[2], v_full[2], v_empty[2];
-  uint64_t q_ready, s_free, p_full, qk_done, pv_done, final_done;
+  uint64_t q_ready, s_free, p_full, qk_done, delta_done, pv_done, final_done;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -100,9 +101,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int ord = blockIdx.x;           // longest tiles (largest b) first
-  const int b = Np - 1 - ord / BH;
-  const int bh = ord % BH;
+  // Tile order: heads in groups of kHeadGroup; inside a group, longest tiles
+  // (largest b) first, interleaved over the group's heads.  Tiles of one head
+  // that run together walk the same kr / ngt / V chunks, which then come
+  // from L2; longest-first keeps the tail short.
+  int b, bh;
+  {
+    const int ord = blockIdx.x;
+    const int per_group = kHeadGroup * Np;
+    const int grp = ord / per_group, r = ord - grp * per_group;
+    const int heads = min(kHeadGroup, BH - grp * kHeadGroup);
+    b = Np - 1 - r / heads;
+    bh = grp * kHeadGroup + r % heads;
+  }
   const int Tp = Np * kC;
   const uint64_t LIM = kWaitLimitNs;
 
@@ -117,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->s_free, 128);
     mbar_init(&bars->p_full, 128);
     mbar_init(&bars->qk_done, 1);
+    mbar_init(&bars->delta_done, 1);
     mbar_init(&bars->pv_done, 1);
     mbar_init(&bars->final_done, 1);
     bars->abort_flag = 0;
@@ -195,17 +207,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         const uint32_t kr_a = smem_addr(s_kr + s * Cfg::kKrBytes);
         const uint32_t ng_a = smem_addr(s_ng + s * Cfg::kNgBytes);
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * (kC * 128) + (k & 3) * 32;
-          mma_bf16_ts(tS, tQw + k * 8, sdesc_sw128(kr_a + off, 16, 1024), idS, k > 0);
-        }
+        // the transition first: the running-query warps convert its result
+        // while S is being computed
         if (c > 0) {
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const uint32_t off = (k >> 2) * (D * 128) + (k & 3) * 32;
             mma_bf16_ts(tQm, tQw + k * 8, sdesc_sw128(ng_a + off, 16, 1024), idD, 1);
           }
+          mma_commit(&bars->delta_done);
+        }
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * (kC * 128) + (k & 3) * 32;
+          mma_bf16_ts(tS, tQw + k * 8, sdesc_sw128(kr_a + off, 16, 1024), idS, k > 0);
         }
         mma_commit(&bars->qk_done);
         mma_commit(&bars->kg_empty[s]);
@@ -306,11 +321,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
+        // logits stay raw; the scale enters through the FFMA inside the exp
+        if (sl2 >= 0.f) {
+          float hi = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < kC; ++j) {
-          const float v = __uint_as_float(x[j]) * sl2;
-          x[j] = __float_as_uint(v);
-          mx = fmaxf(mx, v);
+          for (int j = 0; j < kC; ++j) hi = fmaxf(hi, __uint_as_float(x[j]));
+          mx = hi * sl2;
+        } else {
+          float lo = INFINITY;
+#pragma unroll
+          for (int j = 0; j < kC; ++j) lo = fminf(lo, __uint_as_float(x[j]));
+          mx = lo * sl2;
         }
       }
       // lazy rescaling: move the reference max only when it grows by > 8 (log2)
@@ -322,10 +343,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         l *= alpha;
       }
       uint32_t pk[64];
+      // gated logits are already in the log2 domain; plain ones get the scale here
+      const float mul = kGate ? 1.f : sl2;
 #pragma unroll
       for (int j = 0; j < kC; j += 2) {
-        const float p0 = ex2_approx(__uint_as_float(x[j]) - m_used);
-        const float p1 = ex2_approx(__uint_as_float(x[j + 1]) - m_used);
+        const float p0 = ex2_approx(fmaf(__uint_as_float(x[j]), mul, -m_used));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(x[j + 1]), mul, -m_used));
         l += p0 + p1;
         pk[j / 2] = pack_bf16x2(p0, p1);
       }
@@ -410,17 +433,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&bars->q_ready);
       bool ok = true;
       for (int n = 0; n + 1 < b; ++n) {
-        ok = mbar_wait(&bars->qk_done, n & 1, abort_flag, LIM);
+        // Qm is final for this step once the transition MMA is done ...
+        ok = mbar_wait(&bars->delta_done, n & 1, abort_flag, LIM);
         if (!ok) break;
         tc_fence_after_sync();
 #pragma unroll
-        for (int cc = 0; cc < D; cc += 32) {
-          uint32_t m32[32];
-          tmem_ld_x32(tQm + cc, m32);
+        for (int cc = 0; cc < D; cc += 64) {
+          uint32_t m64[64];
+          tmem_ld_x64(tQm + cc, m64);
 #pragma unroll
-          for (int u = 0; u < 16; ++u)
-            qw[cc / 2 + u] = pack_bf16x2(__uint_as_float(m32[2 * u]), __uint_as_float(m32[2 * u + 1]));
+          for (int u = 0; u < 32; ++u)
+            qw[cc / 2 + u] = pack_bf16x2(__uint_as_float(m64[2 * u]), __uint_as_float(m64[2 * u + 1]));
         }
+        // ... and Qw may be overwritten once S = Qw kr^T has read it
+        ok = mbar_wait(&bars->qk_done, n & 1, abort_flag, LIM);
+        if (!ok) break;
+        tc_fence_after_sync();
 #pragma unroll
         for (int cc = 0; cc < D / 2; cc += 32)
           tmem_st_x32(tQw + cc, *reinterpret_cast<uint32_t(*)[32]>(&qw[cc]));
