@@ -6,8 +6,8 @@
 //
 //   diagonal   P_b = softmax-step(sdt_b)            (logits precomputed, fp32)
 //   for c = b-1 .. 0:
-//     Qm += Qw . ngt_c^T   (only if c > 0)         crossing chunk c backwards
-//     S   = Qw . kr_c^T                            tcgen05, A = Qw from TMEM
+//     [S | Qm] += Qw . [kr_c ; ngt_c]^T            one tcgen05 MMA (S zeroed
+//                                                  first; no ngt for c = 0)
 //     P_c = softmax-step(S)                        online softmax, lazy rescale
 //     O  += P_{c+1} . V_{c+1}                      tcgen05, A = P from TMEM
 //   O += P_0 . V_0;  out = O / l,  lse = (m + log2 l) ln 2
@@ -18,11 +18,11 @@
 // dense d x d form of F_c^T = I - W^T U W from the chunk preparation.
 //
 // Warp roles (384 threads):
-//   warp 0      TMA producer: kr_c and ngt_c (one stage), V (own stage ring)
+//   warp 0      TMA producer: kr_c over ngt_c (one B tile), V (own ring)
 //   warp 1      TMEM allocation and the single MMA-issuing thread
 //   warps 4-7   softmax: one query row per thread (TMEM lane = row)
 //   warps 8-11  running-query conversion Qm -> Qw (and its initial load)
-// TMEM columns: S [0,128), O, Qm (d each), Qw (d/2, packed bf16x2), P (64).
+// TMEM columns: S [0,128), Qm (d), O (d), Qw (d/2, packed bf16x2), P (64).
 // Every wait is bounded; on expiry the CTA records PATH_DEV_ERR_TIMEOUT in the
 // status word, drains its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -45,30 +45,60 @@ static_assert(128 * (kRegsLow + kRegsSoftmax + kRegsQuery) <= kThreads * 168, "r
 template <int D>
 struct TcCfg {
   static constexpr int kHalves = D / 64;           // 64-column (128-byte) halves
-  static constexpr uint32_t kKrBytes = kC * D * 2;
-  static constexpr uint32_t kNgBytes = D * D * 2;
+  // One B tile per step stacks kr_c (kC rows) over ngt_c (D rows), so that
+  // S = Qw kr^T and the transition Qm += Qw ngt^T are a single MMA of width
+  // N = kC + D; tcgen05.mma pays a fixed cost per instruction below N = 256.
+  static constexpr int kKgRows = kC + D;
+  static constexpr uint32_t kKgHalf = kKgRows * 128;  // one 64-column half
+  static constexpr uint32_t kKgBytes = kHalves * kKgHalf;
   static constexpr uint32_t kVBytes = kC * D * 2;
-  static constexpr uint32_t kColS = 0;
-  static constexpr uint32_t kColO = 128;
-  static constexpr uint32_t kColQm = 128 + D;
+  static constexpr uint32_t kColS = 0;             // S and Qm are adjacent: one
+  static constexpr uint32_t kColQm = 128;          // accumulator of width kC + D
+  static constexpr uint32_t kColO = 128 + D;
   static constexpr uint32_t kColQw = 128 + 2 * D;
   static constexpr uint32_t kColP = 128 + 2 * D + D / 2;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr size_t kTileBytes = 2 * (kKrBytes + kNgBytes + kVBytes);
+  static constexpr size_t kTileBytes = 2 * (kKgBytes + kVBytes);
   static constexpr size_t kSmemBytes = kTileBytes + 1024 /*align*/ + 256 /*barriers*/;
   static_assert(kColP + 64 <= kTmemCols, "TMEM budget");
 };
 
 struct Bars {
   uint64_t kg_full[2], kg_empty[2], v_full[2], v_empty[2];
-  uint64_t q_ready, s_free, p_full, qk_done, delta_done, pv_done, final_done;
+  uint64_t q_ready, s_free, p_full, qk_done, pv_done, final_done;
   uint32_t tmem_base;
   int abort_flag;
 };
 
+// The warp's tcgen05 stores / loads are fenced by each thread before this;
+// the warp then arrives once.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 __device__ __forceinline__ void record_timeout(Bars* bars, int* status) {
   bars->abort_flag = 1;
   atomicExch(status, PATH_DEV_ERR_TIMEOUT);
+}
+
+// Row max / min of 128 values held as bit patterns, as eight independent
+// chains (a single chain would put 128 dependent operations on the path).
+__device__ __forceinline__ float row_max(const uint32_t (&x)[128]) {
+  float m[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) m[u] = __uint_as_float(x[u]);
+#pragma unroll
+  for (int j = 8; j < 128; ++j) m[j & 7] = fmaxf(m[j & 7], __uint_as_float(x[j]));
+  return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
+}
+__device__ __forceinline__ float row_min(const uint32_t (&x)[128]) {
+  float m[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) m[u] = __uint_as_float(x[u]);
+#pragma unroll
+  for (int j = 8; j < 128; ++j) m[j & 7] = fminf(m[j & 7], __uint_as_float(x[j]));
+  return fminf(fminf(fminf(m[0], m[1]), fminf(m[2], m[3])), fminf(fminf(m[4], m[5]), fminf(m[6], m[7])));
 }
 
 // End of every role: all 384 threads meet on named barrier 1, then warp 1
@@ -94,9 +124,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* s_kr = base;                                   // [2][kKrBytes]
-  uint8_t* s_ng = base + 2 * Cfg::kKrBytes;               // [2][kNgBytes]
-  uint8_t* s_v = s_ng + 2 * Cfg::kNgBytes;                // [2][kVBytes]
+  uint8_t* s_kg = base;                                   // [2][kKgBytes]
+  uint8_t* s_v = base + 2 * Cfg::kKgBytes;                // [2][kVBytes]
   Bars* bars = reinterpret_cast<Bars*>(base + Cfg::kTileBytes);
   volatile int* abort_flag = &bars->abort_flag;
 
@@ -124,11 +153,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
     }
-    mbar_init(&bars->q_ready, 128);
-    mbar_init(&bars->s_free, 128);
-    mbar_init(&bars->p_full, 128);
+    mbar_init(&bars->q_ready, 4);  // one arrival per warp
+    mbar_init(&bars->s_free, 4);  // one arrival per warp
+    mbar_init(&bars->p_full, 4);  // one arrival per warp
     mbar_init(&bars->qk_done, 1);
-    mbar_init(&bars->delta_done, 1);
     mbar_init(&bars->pv_done, 1);
     mbar_init(&bars->final_done, 1);
     bars->abort_flag = 0;
@@ -165,12 +193,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int c = b - 1 - n;
           if (n >= 2) ok = mbar_wait(&bars->kg_empty[s], ((n >> 1) - 1) & 1, abort_flag, LIM);
           if (!ok) break;
-          mbar_arrive_expect_tx(&bars->kg_full[s], Cfg::kKrBytes + Cfg::kNgBytes);
+          mbar_arrive_expect_tx(&bars->kg_full[s], Cfg::kKgBytes);
           for (int h = 0; h < Cfg::kHalves; ++h) {
-            tma_load_2d(s_kr + s * Cfg::kKrBytes + h * (kC * 128), &map_kr, h * 64,
-                        bh * Tp + c * kC, &bars->kg_full[s]);
-            tma_load_2d(s_ng + s * Cfg::kNgBytes + h * (D * 128), &map_ng, h * 64,
-                        (bh * Np + c) * D, &bars->kg_full[s]);
+            uint8_t* dst = s_kg + s * Cfg::kKgBytes + h * Cfg::kKgHalf;
+            tma_load_2d(dst, &map_kr, h * 64, bh * Tp + c * kC, &bars->kg_full[s]);
+            tma_load_2d(dst + kC * 128, &map_ng, h * 64, (bh * Np + c) * D, &bars->kg_full[s]);
           }
           last_kg[s] = (n >> 1) & 1;
         }
@@ -194,33 +221,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t tS = tb + Cfg::kColS, tO = tb + Cfg::kColO, tQm = tb + Cfg::kColQm,
                      tQw = tb + Cfg::kColQw, tP = tb + Cfg::kColP;
-      constexpr uint32_t idS = idesc_bf16_f32(128, kC, false, false);
-      constexpr uint32_t idD = idesc_bf16_f32(128, D, false, false);
+      constexpr uint32_t idS = idesc_bf16_f32(128, kC, false, false);       // S only
+      constexpr uint32_t idSQ = idesc_bf16_f32(128, kC + D, false, false);  // [S | Qm]
       constexpr uint32_t idPV = idesc_bf16_f32(128, D, false, true);
       bool ok = true;
       for (int n = 0; n < b && ok; ++n) {
         const int c = b - 1 - n, s = n & 1;
         ok = mbar_wait(&bars->q_ready, n & 1, abort_flag, LIM);
-        if (ok && n >= 1) ok = mbar_wait(&bars->s_free, (n - 1) & 1, abort_flag, LIM);
+        // S has been read and zeroed by the softmax warps
+        if (ok) ok = mbar_wait(&bars->s_free, n & 1, abort_flag, LIM);
         if (ok) ok = mbar_wait(&bars->kg_full[s], (n >> 1) & 1, abort_flag, LIM);
         if (!ok) break;
         tc_fence_after_sync();
-        const uint32_t kr_a = smem_addr(s_kr + s * Cfg::kKrBytes);
-        const uint32_t ng_a = smem_addr(s_ng + s * Cfg::kNgBytes);
-        // the transition first: the running-query warps convert its result
-        // while S is being computed
-        if (c > 0) {
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = (k >> 2) * (D * 128) + (k & 3) * 32;
-            mma_bf16_ts(tQm, tQw + k * 8, sdesc_sw128(ng_a + off, 16, 1024), idD, 1);
-          }
-          mma_commit(&bars->delta_done);
-        }
+        const uint32_t kg_a = smem_addr(s_kg + s * Cfg::kKgBytes);
+        // [S | Qm] += Qw [kr_c ; ngt_c]^T: the logits and the backward crossing
+        // of chunk c in one MMA of width kC + D (S starts from zero); the last
+        // chunk needs no crossing
+        const uint32_t id = c > 0 ? idSQ : idS;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * (kC * 128) + (k & 3) * 32;
-          mma_bf16_ts(tS, tQw + k * 8, sdesc_sw128(kr_a + off, 16, 1024), idS, k > 0);
+          const uint32_t off = (k >> 2) * Cfg::kKgHalf + (k & 3) * 32;
+          mma_bf16_ts(tS, tQw + k * 8, sdesc_sw128(kg_a + off, 16, 1024), id, 1);
         }
         mma_commit(&bars->qk_done);
         mma_commit(&bars->kg_empty[s]);
@@ -269,30 +290,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                    tP = tb + lb + Cfg::kColP;
     uint32_t x[128];
     float m_used, l = 0.f;
+    // S accumulates from zero every step: clear it before the first MMA
+    {
+      uint32_t z[32];
+#pragma unroll
+      for (int u = 0; u < 32; ++u) z[u] = 0u;
+#pragma unroll
+      for (int cc = 0; cc < kC; cc += 32) tmem_st_x32(tS + cc, z);
+      tmem_st_wait();
+      tc_fence_before_sync();
+      warp_arrive(&bars->s_free);
+    }
     // diagonal chunk: precomputed log2-domain logits sdt[ch][j][i]
     {
       const float* sd = sdt + (static_cast<size_t>(bh) * Np + b) * kC * kC + r;
-      float mx = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < kC; ++j) {
-        const float v = __ldg(sd + j * kC);
-        x[j] = __float_as_uint(v);
-        mx = fmaxf(mx, v);
-      }
-      m_used = mx;
+      for (int j = 0; j < kC; ++j) x[j] = __float_as_uint(__ldg(sd + j * kC));
+      m_used = row_max(x);
       uint32_t pk[64];
+      float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < kC; j += 2) {
         const float p0 = ex2_approx(__uint_as_float(x[j]) - m_used);
         const float p1 = ex2_approx(__uint_as_float(x[j + 1]) - m_used);
-        l += p0 + p1;
+        part[(j / 2) & 7] += p0 + p1;
         pk[j / 2] = pack_bf16x2(p0, p1);
       }
+      l = ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
       tmem_st_x32(tP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
       tmem_st_x32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
       tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(&bars->p_full);
+      warp_arrive(&bars->p_full);
     }
     bool ok = true;
     const float lrow = kGate ? lam2[static_cast<size_t>(bh) * Tp + t] : 0.f;
@@ -301,10 +330,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = mbar_wait(&bars->qk_done, n & 1, abort_flag, LIM);
       if (!ok) break;
       tc_fence_after_sync();
-      tmem_ld_x64(tS, *reinterpret_cast<uint32_t(*)[64]>(&x[0]));
-      tmem_ld_x64(tS + 64, *reinterpret_cast<uint32_t(*)[64]>(&x[64]));
+      tmem_ld_x128(tS, x);
+      {
+        uint32_t z[32];
+#pragma unroll
+        for (int u = 0; u < 32; ++u) z[u] = 0u;
+#pragma unroll
+        for (int cc = 0; cc < kC; cc += 32) tmem_st_x32(tS + cc, z);
+        tmem_st_wait();
+      }
       tc_fence_before_sync();
-      mbar_arrive(&bars->s_free);
+      warp_arrive(&bars->s_free);
       float mx = -INFINITY;
       if (kGate) {
         const float4* lg = reinterpret_cast<const float4*>(lam2 + static_cast<size_t>(bh) * Tp + c * kC);
@@ -315,23 +351,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int j = j4 * 4 + u;
-            const float v = fmaf(__uint_as_float(x[j]), sl2, lrow - gv[u]);
-            x[j] = __float_as_uint(v);
-            mx = fmaxf(mx, v);
+            x[j] = __float_as_uint(fmaf(__uint_as_float(x[j]), sl2, lrow - gv[u]));
           }
         }
+        mx = row_max(x);
       } else {
         // logits stay raw; the scale enters through the FFMA inside the exp
         if (sl2 >= 0.f) {
-          float hi = -INFINITY;
-#pragma unroll
-          for (int j = 0; j < kC; ++j) hi = fmaxf(hi, __uint_as_float(x[j]));
-          mx = hi * sl2;
+          mx = row_max(x) * sl2;
         } else {
-          float lo = INFINITY;
-#pragma unroll
-          for (int j = 0; j < kC; ++j) lo = fminf(lo, __uint_as_float(x[j]));
-          mx = lo * sl2;
+          mx = row_min(x) * sl2;
         }
       }
       // lazy rescaling: move the reference max only when it grows by > 8 (log2)
@@ -345,13 +374,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t pk[64];
       // gated logits are already in the log2 domain; plain ones get the scale here
       const float mul = kGate ? 1.f : sl2;
+      float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < kC; j += 2) {
         const float p0 = ex2_approx(fmaf(__uint_as_float(x[j]), mul, -m_used));
         const float p1 = ex2_approx(fmaf(__uint_as_float(x[j + 1]), mul, -m_used));
-        l += p0 + p1;
+        part[(j / 2) & 7] += p0 + p1;
         pk[j / 2] = pack_bf16x2(p0, p1);
       }
+      l += ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
       // P buffer and O are free once O += P_{c+1} V_{c+1} has completed
       ok = mbar_wait(&bars->pv_done, n & 1, abort_flag, LIM);
       if (!ok) break;
@@ -370,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_x32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
       tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(&bars->p_full);
+      warp_arrive(&bars->p_full);
     }
     // epilogue: out = O / l, lse = (m + log2 l) ln 2
     if (ok) ok = mbar_wait(&bars->pv_done, b & 1, abort_flag, LIM);
@@ -430,11 +461,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_x32(tQw + cc, *reinterpret_cast<uint32_t(*)[32]>(&qw[cc]));
       tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(&bars->q_ready);
+      warp_arrive(&bars->q_ready);
       bool ok = true;
       for (int n = 0; n + 1 < b; ++n) {
-        // Qm is final for this step once the transition MMA is done ...
-        ok = mbar_wait(&bars->delta_done, n & 1, abort_flag, LIM);
+        // Qm (and S) are final for this step once the fused MMA is done
+        ok = mbar_wait(&bars->qk_done, n & 1, abort_flag, LIM);
         if (!ok) break;
         tc_fence_after_sync();
 #pragma unroll
@@ -445,16 +476,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int u = 0; u < 32; ++u)
             qw[cc / 2 + u] = pack_bf16x2(__uint_as_float(m64[2 * u]), __uint_as_float(m64[2 * u + 1]));
         }
-        // ... and Qw may be overwritten once S = Qw kr^T has read it
-        ok = mbar_wait(&bars->qk_done, n & 1, abort_flag, LIM);
-        if (!ok) break;
-        tc_fence_after_sync();
 #pragma unroll
         for (int cc = 0; cc < D / 2; cc += 32)
           tmem_st_x32(tQw + cc, *reinterpret_cast<uint32_t(*)[32]>(&qw[cc]));
         tmem_st_wait();
         tc_fence_before_sync();
-        mbar_arrive(&bars->q_ready);
+        warp_arrive(&bars->q_ready);
       }
       if (!ok) record_timeout(bars, status);
     }

@@ -45,6 +45,9 @@ struct PCfg {
   static constexpr size_t kSmem = 2 * kWBytes + kUBytes + kBBytes + 2 * kPC * 4;
 };
 
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
 __device__ __forceinline__ uint32_t tf32r(float x) {
   uint32_t r;
   asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
@@ -140,10 +143,58 @@ __device__ __forceinline__ void acc_to_a(uint32_t (&a)[4], const float (&c)[4], 
   a[3] = tf32r(odd ? v1 : v0);
 }
 
+// One doubling level of the unit-lower-triangular inverse: for every pair of
+// s x s diagonal blocks [[A, 0], [Cb, Dm]] whose inverses Ainv, Dinv are in
+// place, overwrite Cb with -Dinv (Cb Ainv).  Thread t owns column t % s of one
+// pair and rows i0, i0 + 4, ... of it, so the operand shared by its outputs is
+// loaded once per k and the row operands come in as float4 broadcasts.
+template <int S, int s>
+__device__ __forceinline__ void invert_level(float* sU, int tid) {
+  constexpr int kPer = s / 4;                  // outputs per thread
+  constexpr int kPairs = kPC / (2 * s);
+  const int jj = tid % s, rest = tid / s;
+  const int p = rest % kPairs, i0 = rest / kPairs;
+  const int r0 = p * 2 * s + s, c0 = p * 2 * s;
+  float e[kPer];
+#pragma unroll
+  for (int r = 0; r < kPer; ++r) e[r] = 0.f;
+  // E = Cb Ainv   (Ainv's upper part is zero, so every k can be summed)
+#pragma unroll 4
+  for (int kk = 0; kk < s; kk += 4) {
+    const float a0 = sU[(c0 + kk) * S + c0 + jj], a1 = sU[(c0 + kk + 1) * S + c0 + jj];
+    const float a2 = sU[(c0 + kk + 2) * S + c0 + jj], a3 = sU[(c0 + kk + 3) * S + c0 + jj];
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) {
+      const float4 cv = *reinterpret_cast<const float4*>(sU + (r0 + i0 + 4 * r) * S + c0 + kk);
+      e[r] = fmaf(cv.x, a0, fmaf(cv.y, a1, fmaf(cv.z, a2, fmaf(cv.w, a3, e[r]))));
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < kPer; ++r) sU[(r0 + i0 + 4 * r) * S + c0 + jj] = e[r];
+  __syncthreads();
+  // F = -Dinv E   (Dinv's upper part is zero)
+#pragma unroll
+  for (int r = 0; r < kPer; ++r) e[r] = 0.f;
+#pragma unroll 4
+  for (int kk = 0; kk < s; kk += 4) {
+    const float b0 = sU[(r0 + kk) * S + c0 + jj], b1 = sU[(r0 + kk + 1) * S + c0 + jj];
+    const float b2 = sU[(r0 + kk + 2) * S + c0 + jj], b3 = sU[(r0 + kk + 3) * S + c0 + jj];
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) {
+      const float4 dv = *reinterpret_cast<const float4*>(sU + (r0 + i0 + 4 * r) * S + r0 + kk);
+      e[r] = fmaf(dv.x, b0, fmaf(dv.y, b1, fmaf(dv.z, b2, fmaf(dv.w, b3, e[r]))));
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < kPer; ++r) sU[(r0 + i0 + 4 * r) * S + c0 + jj] = -e[r];
+  __syncthreads();
+}
+
 // X = (I + L)^{-1} in place (L strictly lower on entry, stride S), by
 // recursive doubling: invert the 16 x 16 diagonal blocks by substitution, then
-// for block sizes s = 16, 32, 64 fill each bottom-left block with
-// -Dinv (Cblk Ainv).  Ends with a block-wide barrier.
+// combine blocks of 16, 32 and 64.  Ends with a block-wide barrier.
 template <int S>
 __device__ __forceinline__ void invert_unit_lower(float* sU, int tid) {
   {
@@ -165,54 +216,9 @@ __device__ __forceinline__ void invert_unit_lower(float* sU, int tid) {
     }
     __syncthreads();
   }
-#pragma unroll
-  for (int lvl = 0; lvl < 3; ++lvl) {
-    const int s = 16 << lvl;                 // block size being combined
-    const int per = (kPC / (2 * s)) * s * s / kPThreads;  // 4, 8, 16
-    float e[16];
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      if (r < per) {
-        const int o = threadIdx.x + kPThreads * r;
-        const int p = o / (s * s), rem = o % (s * s), i = rem / s, jj = rem % s;
-        const int r0 = p * 2 * s + s, c0 = p * 2 * s;
-        float acc = 0.f;
-        for (int kk = jj; kk < s; ++kk) acc = fmaf(sU[(r0 + i) * S + c0 + kk], sU[(c0 + kk) * S + c0 + jj], acc);
-        e[r] = acc;
-      }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      if (r < per) {
-        const int o = threadIdx.x + kPThreads * r;
-        const int p = o / (s * s), rem = o % (s * s), i = rem / s, jj = rem % s;
-        sU[(p * 2 * s + s + i) * S + p * 2 * s + jj] = e[r];
-      }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      if (r < per) {
-        const int o = threadIdx.x + kPThreads * r;
-        const int p = o / (s * s), rem = o % (s * s), i = rem / s, jj = rem % s;
-        const int r0 = p * 2 * s + s, c0 = p * 2 * s;
-        float acc = 0.f;
-        for (int kk = 0; kk <= i; ++kk) acc = fmaf(sU[(r0 + i) * S + r0 + kk], sU[(r0 + kk) * S + c0 + jj], acc);
-        e[r] = -acc;
-      }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      if (r < per) {
-        const int o = threadIdx.x + kPThreads * r;
-        const int p = o / (s * s), rem = o % (s * s), i = rem / s, jj = rem % s;
-        sU[(p * 2 * s + s + i) * S + p * 2 * s + jj] = e[r];
-      }
-    }
-    __syncthreads();
-  }
+  invert_level<S, 16>(sU, tid);
+  invert_level<S, 32>(sU, tid);
+  invert_level<S, 64>(sU, tid);
 }
 
 template <int D, bool kGate>
@@ -243,17 +249,23 @@ __global__ void __launch_bounds__(kPThreads, 1)
   const __nv_bfloat16* Kg = k + row0 * D;
   const __nv_bfloat16* Qg = q + row0 * D;
 
-  // ---- stage W, K, beta (and the gate prefix) in shared memory
+  // ---- stage W, K, beta (and the gate prefix) in shared memory; all 16-byte
+  // copies in flight at once (cp.async), padding rows zero-filled
   for (int e = tid; e < kPC * D / 8; e += kPThreads) {
     const int r = e / (D / 8), c8 = e % (D / 8);
-    uint4 wv = make_uint4(0, 0, 0, 0), kv = make_uint4(0, 0, 0, 0);
+    __nv_bfloat16* dw = sW + r * SW + c8 * 8;
+    __nv_bfloat16* dk = sK + r * SW + c8 * 8;
     if (r < nrows) {
-      wv = __ldg(reinterpret_cast<const uint4*>(Wg + r * D) + c8);
-      kv = __ldg(reinterpret_cast<const uint4*>(Kg + r * D) + c8);
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dw)),
+                   "l"(Wg + r * D + c8 * 8) : "memory");
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dk)),
+                   "l"(Kg + r * D + c8 * 8) : "memory");
+    } else {
+      *reinterpret_cast<uint4*>(dw) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(dk) = make_uint4(0, 0, 0, 0);
     }
-    *reinterpret_cast<uint4*>(sW + r * SW + c8 * 8) = wv;
-    *reinterpret_cast<uint4*>(sK + r * SW + c8 * 8) = kv;
   }
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
   if (tid < kPC) {
     sBeta[tid] = tid < nrows ? beta[row0 + tid] : 0.f;
     if (kGate) sLam[tid] = lam2[static_cast<size_t>(bh) * Np * kPC + t0 + tid];
