@@ -192,9 +192,84 @@ __device__ __forceinline__ void invert_level(float* sU, int tid) {
   __syncthreads();
 }
 
+// acc[nt] += A[m0:m0+16, k0:k1] * B[k0:k1, n0:n0+8 nt] on fp32 shared-memory
+// matrices (row-major, strides SA / SB) with three tf32 products per term
+// (hi*hi + hi*lo + lo*hi), which keeps about fp32 accuracy.
+template <int NT, int SA, int SB>
+__device__ __forceinline__ void mma_3xtf32(float (&acc)[NT][4], const float* A, int m0,
+                                           const float* B, int n0, int k0, int k1, int g,
+                                           int t, float sign) {
+  for (int k = k0; k < k1; k += 8) {
+    uint32_t ah[4], al[4];
+    const float av[4] = {A[(m0 + g) * SA + k + t], A[(m0 + g + 8) * SA + k + t],
+                         A[(m0 + g) * SA + k + t + 4], A[(m0 + g + 8) * SA + k + t + 4]};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float x = sign * av[u];
+      ah[u] = tf32r(x);
+      al[u] = tf32r(x - __uint_as_float(ah[u]));
+    }
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const float b0 = B[(k + t) * SB + n0 + 8 * j + g], b1 = B[(k + t + 4) * SB + n0 + 8 * j + g];
+      uint32_t bh[2] = {tf32r(b0), tf32r(b1)};
+      uint32_t bl[2] = {tf32r(b0 - __uint_as_float(bh[0])), tf32r(b1 - __uint_as_float(bh[1]))};
+      mma_tf32(acc[j], al, bh);
+      mma_tf32(acc[j], ah, bl);
+      mma_tf32(acc[j], ah, bh);
+    }
+  }
+}
+
+// Doubling level on the tensor cores for s = 32 or 64: the same update as
+// invert_level, E = Cb Ainv then Cb <- -Dinv E, with 16 x 8 output tiles
+// spread over the 8 warps.
+template <int S, int s>
+__device__ __forceinline__ void invert_level_mma(float* sU, int warp, int g, int t) {
+  constexpr int kPairs = kPC / (2 * s);
+  constexpr int kMTiles = s / 16, kNTiles = s / 8;
+  constexpr int kTilesPerPair = kMTiles * kNTiles;           // 16-row x 8-col tiles
+  constexpr int kNT = kPairs * kTilesPerPair / 8;             // n-tiles per warp
+  static_assert(kNT >= 1 && kNTiles % kNT == 0, "tile split");
+  // warp -> (pair, m-tile, first n-tile)
+  const int tile0 = warp * kNT;
+  const int p = tile0 / kTilesPerPair, rem = tile0 % kTilesPerPair;
+  const int mt = rem / kNTiles, nt0 = rem % kNTiles;
+  const int r0 = p * 2 * s + s, c0 = p * 2 * s;
+  float acc[kNT][4];
+#pragma unroll
+  for (int j = 0; j < kNT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+  // E = Cb Ainv: A = rows r0 + 16 mt of Cb (columns c0..), B = Ainv (rows c0.., cols c0..)
+  mma_3xtf32<kNT, S, S>(acc, sU + c0, r0 + 16 * mt, sU + c0 * S + c0, 8 * nt0, 0, s, g, t, 1.f);
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < kNT; ++j) {
+    const int c = c0 + 8 * (nt0 + j) + 2 * t, ra = r0 + 16 * mt + g;
+    sU[ra * S + c] = acc[j][0];
+    sU[ra * S + c + 1] = acc[j][1];
+    sU[(ra + 8) * S + c] = acc[j][2];
+    sU[(ra + 8) * S + c + 1] = acc[j][3];
+    acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+  }
+  __syncthreads();
+  // -Dinv E: A = Dinv (rows r0.., cols r0..), B = E (rows r0.., cols c0..)
+  mma_3xtf32<kNT, S, S>(acc, sU + r0, r0 + 16 * mt, sU + r0 * S + c0, 8 * nt0, 0, s, g, t, -1.f);
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < kNT; ++j) {
+    const int c = c0 + 8 * (nt0 + j) + 2 * t, ra = r0 + 16 * mt + g;
+    sU[ra * S + c] = acc[j][0];
+    sU[ra * S + c + 1] = acc[j][1];
+    sU[(ra + 8) * S + c] = acc[j][2];
+    sU[(ra + 8) * S + c + 1] = acc[j][3];
+  }
+  __syncthreads();
+}
+
 // X = (I + L)^{-1} in place (L strictly lower on entry, stride S), by
 // recursive doubling: invert the 16 x 16 diagonal blocks by substitution, then
-// combine blocks of 16, 32 and 64.  Ends with a block-wide barrier.
+// combine blocks of 16 (CUDA cores), 32 and 64 (tensor cores).  Ends with a
+// block-wide barrier.
 template <int S>
 __device__ __forceinline__ void invert_unit_lower(float* sU, int tid) {
   {
@@ -217,8 +292,9 @@ __device__ __forceinline__ void invert_unit_lower(float* sU, int tid) {
     __syncthreads();
   }
   invert_level<S, 16>(sU, tid);
-  invert_level<S, 32>(sU, tid);
-  invert_level<S, 64>(sU, tid);
+  const int warp = tid >> 5, g = (tid & 31) >> 2, t = tid & 3;
+  invert_level_mma<S, 32>(sU, warp, g, t);
+  invert_level_mma<S, 64>(sU, warp, g, t);
 }
 
 template <int D, bool kGate>
