@@ -85,8 +85,12 @@ class ClockSampler:
             os.close(fd)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            # the timed region starts only once sampling is running
+            t0 = time.time()
+            while time.time() - t0 < 5.0 and os.path.getsize(self.path) == 0:
+                time.sleep(0.01)
         except Exception:
             self.proc = None
         return self
@@ -119,6 +123,24 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
                 "samples": len(rows)}
+
+
+def traffic_record():
+    """DRAM bytes per attention launch from the committed ncu record, or None
+    when the kernel sources have changed since that capture."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "attn_tc_traffic.json")) as f:
+            rec = json.load(f)["attn_tc_kernel"]
+        h = hashlib.sha256()
+        for src in rec["sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != rec["sources_sha256"]:
+            return None
+        return rec["dram_bytes_per_launch"]
+    except Exception:
+        return None
 
 
 def dist_setup():
@@ -266,7 +288,9 @@ def run_gpu(args, wl, flops):
     peak, _, peak_src = _peaks()
     achieved = flops["attn"] / (attn_avg_ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": args.traffic,
+                "frac": achieved / peak,
+                "traffic": args.traffic if args.traffic is not None else (
+                    traffic_record() if wl.name == DEFAULT_WORKLOAD else None),
                 "kernel": "attn_tc_kernel", "peak_source": f"{peak_src} bf16 burst",
                 "avg_launch_ms": attn_avg_ms, "prep_avg_ms": prep_ms / calls}
 
@@ -324,7 +348,7 @@ def run_gpu(args, wl, flops):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
