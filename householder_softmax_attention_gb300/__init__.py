@@ -21,7 +21,7 @@ import threading
 
 __all__ = [
     "PathAttnError", "load_library", "path_attn_fwd", "path_attn_fwd_host",
-    "path_attn_fwd_noalloc",
+    "path_attn_fwd_noalloc", "path_attn_debug_wait_timeout",
     "path_attn_debug_factors", "path_attn_device_status", "path_attn_workspace_bytes",
     "path_attn_chunk_size", "path_attn_launches_per_call", "path_attn_timing_enable",
     "path_attn_timing_read", "path_attn_version", "path_attn_status_string",
@@ -92,6 +92,8 @@ def load_library(path: str | None = None):
         lib.path_attn_debug_factors.argtypes = [vp, vp, vp, fp, fp, f, i, i, i, i, i,
                                                 vp, vp, vp, vp, vp, vp]
         lib.path_attn_debug_factors.restype = i
+        lib.path_attn_debug_wait_timeout.argtypes = [ctypes.c_ulonglong, vp]
+        lib.path_attn_debug_wait_timeout.restype = i
         lib.path_attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, fp, fp, f, vp, fp, vp,
                                               i, i, i, i, i, vp]
         lib.path_attn_fwd_noalloc.restype = i
@@ -251,6 +253,15 @@ def path_attn_debug_factors(q, k, w, beta, logf=None, scale=None, stream=None):
                                          ctypes.c_void_p(st.cuda_stream))
     _check(rc, "path_attn_debug_factors")
     return dict(C=C, kr=kr, ql=ql, ngt=ngt, sdt=sdt, lam2=lam2)
+
+
+def path_attn_debug_wait_timeout(limit_ns: int, stream=None):
+    """Launch the diagnostics kernel whose bounded wait expires after
+    ``limit_ns``; the device status word then reads PATH_ERR_TIMEOUT."""
+    import torch
+    st = stream if stream is not None else torch.cuda.current_stream()
+    _check(load_library().path_attn_debug_wait_timeout(int(limit_ns), ctypes.c_void_p(st.cuda_stream)),
+           "path_attn_debug_wait_timeout")
 
 
 def path_attn_device_status(device: int = 0, clear: bool = True) -> int:

@@ -345,6 +345,16 @@ int path_attn_debug_factors(const void* q, const void* k, const void* w, const f
   return rc;
 }
 
+int path_attn_debug_wait_timeout(unsigned long long limit_ns, void* stream) {
+  if (limit_ns == 0 || limit_ns > 2000000000ull) return PATH_ERR_INVALID_ARG;
+  DeviceState* s = nullptr;
+  int rc = device_state(&s);
+  if (rc != PATH_OK) return rc;
+  if ((rc = check_device(s)) != PATH_OK) return rc;
+  cudaError_t e = launch_debug_wait(s->status, limit_ns, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PATH_OK : set_cuda_error(e);
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------------

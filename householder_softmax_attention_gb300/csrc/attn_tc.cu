@@ -537,7 +537,24 @@ cudaError_t launch_tc(const Geom& g, const Inputs& in, const Workspace& ws, int*
   return cudaGetLastError();
 }
 
+// Diagnostics: one thread waits, with the library's bounded wait, on an
+// mbarrier that nothing arrives at, and records the expiry like the kernels
+// above do.  Used to check the timeout path without faulting the device.
+__global__ void debug_wait_kernel(int* status, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    if (!mbar_wait(&bar, 0, nullptr, limit_ns)) atomicExch(status, PATH_DEV_ERR_TIMEOUT);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_debug_wait(int* status, unsigned long long limit_ns, cudaStream_t st) {
+  debug_wait_kernel<<<1, 32, 0, st>>>(status, limit_ns);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_attn_tc(const Geom& g, const Inputs& in, const Workspace& ws, int* status,
                            cudaStream_t st, int* launches) {

@@ -107,5 +107,7 @@ cudaError_t launch_attn_f32(const Geom& g, const Inputs& in, const Workspace& ws
 // bf16 attention over the prepared chunks (tcgen05 / TMEM / TMA).
 cudaError_t launch_attn_tc(const Geom& g, const Inputs& in, const Workspace& ws,
                            int* dev_status, cudaStream_t st, int* launches);
+// Diagnostics: a kernel whose bounded wait can only expire (sets *status).
+cudaError_t launch_debug_wait(int* status, unsigned long long limit_ns, cudaStream_t st);
 
 }  // namespace pathattn

@@ -155,6 +155,17 @@ int path_attn_debug_factors(const void* q, const void* k, const void* w, const f
                             float* lam2, void* stream);
 
 /*
+ * path_attn_debug_wait_timeout -- diagnostics for the failure path: launches
+ * on `stream` a one-thread kernel that waits, with the same bounded wait the
+ * attention kernel uses, on a barrier nothing arrives at, for limit_ns
+ * nanoseconds (1 .. 2e9).  The wait expires and the kernel records the
+ * timeout in the device status word, which path_attn_device_status() then
+ * reports as PATH_ERR_TIMEOUT (and clears).  Nothing faults; the context
+ * stays usable.
+ */
+int path_attn_debug_wait_timeout(unsigned long long limit_ns, void* stream);
+
+/*
  * path_attn_fwd_noalloc -- path_attn_fwd for callers that cannot allocate
  * device memory.  The paper has no counterpart; this is a library interface.
  *
