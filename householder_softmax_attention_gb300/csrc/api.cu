@@ -137,7 +137,7 @@ int run_forward(const Geom& g, const Inputs& in, char* ws_base, DeviceState* s,
   }
   cudaError_t e;
   if (rec) cudaEventRecord(rec->e0, st);
-  if ((e = launch_prep(g, in, ws, st, nullptr)) != cudaSuccess) return set_cuda_error(e);
+  if ((e = launch_prep(g, in, ws, s->status, st, nullptr)) != cudaSuccess) return set_cuda_error(e);
   if (rec) cudaEventRecord(rec->e1, st);
   if (g.bf16)
     e = launch_attn_tc(g, in, ws, s->status, st, nullptr);
@@ -330,7 +330,7 @@ int path_attn_debug_factors(const void* q, const void* k, const void* w, const f
   Workspace ws;
   workspace_layout(g, static_cast<char*>(base), &ws);
   Inputs in{q, k, nullptr, w, beta, logf, scale, nullptr, nullptr};
-  e = launch_prep(g, in, ws, st, nullptr);
+  e = launch_prep(g, in, ws, s->status, st, nullptr);
   const size_t es = g.bf16 ? 2 : 4, nch = g.nch, C = g.C;
   if (e == cudaSuccess) e = cudaMemcpyAsync(kr, ws.kr, nch * C * d * es, cudaMemcpyDeviceToDevice, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(ql, ws.ql, nch * C * d * 4, cudaMemcpyDeviceToDevice, st);
@@ -436,7 +436,7 @@ extern "C" int path_attn_fwd_noalloc(const void* q, const void* k, const void* v
   Workspace ws;
   workspace_layout(g, s->scratch, &ws);
   Inputs in{q, k, v, w, beta, logf, scale, out, lse};
-  if ((e = launch_prep(g, in, ws, st, nullptr)) != cudaSuccess) return set_cuda_error(e);
+  if ((e = launch_prep(g, in, ws, word, st, nullptr)) != cudaSuccess) return set_cuda_error(e);
   e = g.bf16 ? launch_attn_tc(g, in, ws, word, st, nullptr) : launch_attn_f32(g, in, ws, st, nullptr);
   if (e != cudaSuccess) return set_cuda_error(e);
   return PATH_OK;

@@ -17,7 +17,8 @@
 //   lam2 = log2(e) * inclusive cumsum of log f  (gate_ij = lam_i - lam_j).
 //
 // All arithmetic is fp32 (inputs widened exactly).  These SIMT kernels serve
-// fp32 inputs; bf16 inputs go to the fused tensor-core kernel in prep_mma.cu.
+// fp32 inputs; bf16 inputs go to the fused tensor-core kernels (prep_tc.cu,
+// prep_mma.cu).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -293,8 +294,8 @@ __global__ void gate_cumsum_kernel(const float* logf, float* lam2, int T, int Tp
 
 }  // namespace
 
-cudaError_t launch_prep(const Geom& g, const Inputs& in, const Workspace& ws, cudaStream_t st,
-                        int* launches) {
+cudaError_t launch_prep(const Geom& g, const Inputs& in, const Workspace& ws, int* dev_status,
+                        cudaStream_t st, int* launches) {
   const int C = g.C, d = g.d, nch = g.nch;
   cudaError_t e;
   int n = 0;
@@ -304,7 +305,8 @@ cudaError_t launch_prep(const Geom& g, const Inputs& in, const Workspace& ws, cu
     ++n;
   }
   if (g.bf16) {
-    if ((e = launch_prep_mma(g, in, ws, st)) != cudaSuccess) return e;
+    e = g.d == 128 ? launch_prep_tc(g, in, ws, dev_status, st) : launch_prep_mma(g, in, ws, st);
+    if (e != cudaSuccess) return e;
     if (launches) *launches = n + 1;
     return cudaSuccess;
   }
