@@ -125,8 +125,10 @@ __device__ __forceinline__ void invert_level_mma(float* sU, int warp, int g, int
   float acc[kNT][4];
 #pragma unroll
   for (int j = 0; j < kNT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-  // E = Cb Ainv: A = rows r0 + 16 mt of Cb (columns c0..), B = Ainv (rows c0.., cols c0..)
-  mma_3xtf32<kNT, S, S>(acc, sU + c0, r0 + 16 * mt, sU + c0 * S + c0, 8 * nt0, 0, s, g, t, 1.f);
+  // E = Cb Ainv: A = rows r0 + 16 mt of Cb (columns c0..), B = Ainv (rows c0.., cols c0..);
+  // Ainv is lower triangular, so rows k < 8 nt0 of it are zero in these columns
+  mma_3xtf32<kNT, S, S>(acc, sU + c0, r0 + 16 * mt, sU + c0 * S + c0, 8 * nt0, 8 * nt0, s, g, t,
+                        1.f);
   __syncthreads();
 #pragma unroll
   for (int j = 0; j < kNT; ++j) {
@@ -138,8 +140,10 @@ __device__ __forceinline__ void invert_level_mma(float* sU, int warp, int g, int
     acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
   }
   __syncthreads();
-  // -Dinv E: A = Dinv (rows r0.., cols r0..), B = E (rows r0.., cols c0..)
-  mma_3xtf32<kNT, S, S>(acc, sU + r0, r0 + 16 * mt, sU + r0 * S + c0, 8 * nt0, 0, s, g, t, -1.f);
+  // -Dinv E: A = Dinv (rows r0.., cols r0..), B = E (rows r0.., cols c0..); Dinv is
+  // lower triangular, so columns k > 16 mt + 15 of these rows are zero
+  mma_3xtf32<kNT, S, S>(acc, sU + r0, r0 + 16 * mt, sU + r0 * S + c0, 8 * nt0, 0, 16 * mt + 16, g,
+                        t, -1.f);
   __syncthreads();
 #pragma unroll
   for (int j = 0; j < kNT; ++j) {

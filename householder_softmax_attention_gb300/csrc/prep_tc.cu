@@ -196,11 +196,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int gi = 0; gi < 8; ++gi) {
       const int grp = tid + gi * kThreads, i = grp >> 4, c8 = grp & 15;
+      const float4 x0 = *reinterpret_cast<const float4*>(sL + i * kSL + c8 * 8);
+      const float4 x1 = *reinterpret_cast<const float4*>(sL + i * kSL + c8 * 8 + 4);
+      const float4 b0 = *reinterpret_cast<const float4*>(sBeta + c8 * 8);
+      const float4 b1 = *reinterpret_cast<const float4*>(sBeta + c8 * 8 + 4);
+      const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      const float bs[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int c = c8 * 8 + u;
-        v[gi][u] = c <= i ? sL[i * kSL + c] * sBeta[c] : 0.f;
-      }
+      for (int u = 0; u < 8; ++u) v[gi][u] = c8 * 8 + u <= i ? xs[u] * bs[u] : 0.f;
     }
     __syncthreads();
     uint8_t* u_hi = base + kRL;
@@ -391,22 +394,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before_sync();
   __syncthreads();
-  // ql = Q + ql', one row per warp instruction: coalesced loads and stores
+  // ql = Q + ql', one row per warp instruction: coalesced loads and stores;
+  // all Q loads of a thread are issued before they are used
   {
     const float* sq = sL;
     float* out = ql + static_cast<size_t>(ch) * kC * kD;
-    for (int e = tid; e < kC * kD / 4; e += kThreads) {
-      const int i = e / (kD / 4), n4 = (e % (kD / 4)) * 4;
+    constexpr int kIter = kC * kD / 4 / kThreads;  // 16
+    uint2 qv[kIter];
+#pragma unroll
+    for (int r = 0; r < kIter; ++r) {
+      const int e = tid + r * kThreads, i = e / (kD / 4), n4 = (e % (kD / 4)) * 4;
+      qv[r] = i < nrows ? __ldg(reinterpret_cast<const uint2*>(q + (row0 + i) * kD + n4))
+                        : make_uint2(0u, 0u);
+    }
+#pragma unroll
+    for (int r = 0; r < kIter; ++r) {
+      const int e = tid + r * kThreads, i = e / (kD / 4), n4 = (e % (kD / 4)) * 4;
       float4 o = *reinterpret_cast<const float4*>(sq + i * kSL + n4);
-      if (i < nrows) {
-        const uint2 qv = __ldg(reinterpret_cast<const uint2*>(q + (row0 + i) * kD + n4));
-        const __nv_bfloat162 q01 = *reinterpret_cast<const __nv_bfloat162*>(&qv.x);
-        const __nv_bfloat162 q23 = *reinterpret_cast<const __nv_bfloat162*>(&qv.y);
-        o.x += __low2float(q01);
-        o.y += __high2float(q01);
-        o.z += __low2float(q23);
-        o.w += __high2float(q23);
-      }
+      const __nv_bfloat162 q01 = *reinterpret_cast<const __nv_bfloat162*>(&qv[r].x);
+      const __nv_bfloat162 q23 = *reinterpret_cast<const __nv_bfloat162*>(&qv[r].y);
+      o.x += __low2float(q01);
+      o.y += __high2float(q01);
+      o.z += __low2float(q23);
+      o.w += __high2float(q23);
       *reinterpret_cast<float4*>(out + i * kD + n4) = o;
     }
   }
