@@ -59,7 +59,7 @@ struct TcCfg {
   static constexpr uint32_t kColP = 128 + 2 * D + D / 2;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr size_t kTileBytes = 2 * (kKgBytes + kVBytes);
-  static constexpr size_t kSmemBytes = kTileBytes + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr size_t kSmemBytes = kTileBytes + 1024 /*align*/ + 1280 /*barriers, gate*/;
   static_assert(kColP + 64 <= kTmemCols, "TMEM budget");
 };
 
@@ -68,7 +68,23 @@ struct Bars {
   uint64_t q_ready, s_free, p_full, qk_done, pv_done, final_done;
   uint32_t tmem_base;
   int abort_flag;
+  alignas(16) float gate[2][kC];  // FoX: log2-domain gate prefix, read as float4
 };
+
+static_assert(sizeof(Bars) <= 1280, "barrier block size");
+
+// Barrier of the softmax warpgroup (named barrier 2, 128 threads) that also
+// returns whether every thread passed `v` as true.
+__device__ __forceinline__ bool softmax_bar_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 2, 128, p;\n\tselp.b32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
 
 // The warp's tcgen05 stores / loads are fenced by each thread before this;
 // the warp then arrives once.
@@ -325,10 +341,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     bool ok = true;
     const float lrow = kGate ? lam2[static_cast<size_t>(bh) * Tp + t] : 0.f;
+    // FoX: each thread stages one gate value of the next key chunk a step ahead
+    const float* lamh = kGate ? lam2 + static_cast<size_t>(bh) * Tp : nullptr;
+    if (kGate && b > 0) {
+      bars->gate[0][r] = lamh[(b - 1) * kC + r];
+      softmax_bar_and(true);
+    }
     for (int n = 0; n < b; ++n) {
       const int c = b - 1 - n;
+      const float gnext = (kGate && c >= 1) ? __ldg(lamh + (c - 1) * kC + r) : 0.f;
       ok = mbar_wait(&bars->qk_done, n & 1, abort_flag, LIM);
-      if (!ok) break;
+      if (!ok && !kGate) break;
+      if (ok) {
       tc_fence_after_sync();
       tmem_ld_x128(tS, x);
       {
@@ -343,10 +367,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       warp_arrive(&bars->s_free);
       float mx = -INFINITY;
       if (kGate) {
-        const float4* lg = reinterpret_cast<const float4*>(lam2 + static_cast<size_t>(bh) * Tp + c * kC);
+        const float4* lg = reinterpret_cast<const float4*>(&bars->gate[n & 1][0]);
 #pragma unroll
         for (int j4 = 0; j4 < kC / 4; ++j4) {
-          const float4 g4 = __ldg(lg + j4);
+          const float4 g4 = lg[j4];
           const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -385,7 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       l += ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
       // P buffer and O are free once O += P_{c+1} V_{c+1} has completed
       ok = mbar_wait(&bars->pv_done, n & 1, abort_flag, LIM);
-      if (!ok) break;
+      if (!ok && !kGate) break;
+      if (ok) {
       tc_fence_after_sync();
       if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
@@ -402,6 +427,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_wait();
       tc_fence_before_sync();
       warp_arrive(&bars->p_full);
+      }  // pv_done
+      }  // qk_done
+      if (kGate) {
+        // all softmax threads are past this step: the other buffer is free
+        bars->gate[(n + 1) & 1][r] = gnext;
+        ok = softmax_bar_and(ok);
+      }
+      if (!ok) break;
     }
     // epilogue: out = O / l, lse = (m + log2 l) ln 2
     if (ok) ok = mbar_wait(&bars->pv_done, b & 1, abort_flag, LIM);
