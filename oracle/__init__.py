@@ -12,6 +12,9 @@ Two independent formulations live here, both in fp64:
   Source: "PaTH Attention: Position Encoding via Accumulating Householder
   Transformations" (slides), frames "PaTH inserts a learned transformation
   along every path" and "FoX adds a separate mechanism for forgetting".
+* ``path_oracle_decoded_keys`` / ``path_oracle_decode_step`` -- decoding with
+  keys rewritten in place (frame "Decoding updates historical keys in place"),
+  also in C.
 * ``chunked`` -- the blockwise UT-transform algebra in numpy (frames "A
   triangular representation makes paths computable", "A right-to-left scan
   accumulates cross-block paths" and "Backup: fix orientation before
@@ -63,6 +66,13 @@ def _load():
                 ctypes.c_int, ctypes.c_int, dp, dp, dp, dp, dp, ctypes.c_double,
                 ctypes.c_int, dp]
             lib.path_oracle_logits.restype = ctypes.c_int
+            lib.path_oracle_decoded_keys.argtypes = [
+                ctypes.c_int, ctypes.c_int, dp, dp, dp, ctypes.c_int, dp]
+            lib.path_oracle_decoded_keys.restype = ctypes.c_int
+            lib.path_oracle_decode_step.argtypes = [
+                ctypes.c_int, ctypes.c_int, dp, dp, dp, dp, dp, dp, dp, ctypes.c_double,
+                dp, ctypes.c_double, dp, dp]
+            lib.path_oracle_decode_step.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -138,3 +148,41 @@ def path_oracle_logits(q, k, w, beta, i, logf=None, scale=None):
     if rc != 0:
         raise RuntimeError(f"path_oracle_logits failed with status {rc}")
     return s
+
+
+def path_oracle_decoded_keys(k, w, beta, t):
+    """Keys of one head (``k, w: [T, d]``, ``beta: [T]``) as a decoder holds
+    them after token ``t``: ``k_j^(t) = H_t ... H_{j+1} k_j`` for j < t and
+    ``k_t``; returns ``[t + 1, d]``."""
+    k, w, beta = (_f64(x) for x in (k, w, beta))
+    T, d = k.shape
+    out = np.zeros((t + 1, d), dtype=np.float64)
+    rc = _load().path_oracle_decoded_keys(T, d, _ptr(k), _ptr(w), _ptr(beta), int(t), _ptr(out))
+    if rc != 0:
+        raise RuntimeError(f"path_oracle_decoded_keys failed with status {rc}")
+    return out
+
+
+def path_oracle_decode_step(kc, vc, lam, q, k, v, w, beta, logf, t, scale=None):
+    """One decoding step of one head at position ``t``.
+
+    ``kc, vc``: ``[>= t + 1, d]`` fp64 arrays, rows ``< t`` hold the cache and
+    are rewritten in place, row ``t`` receives ``k`` / ``v``; ``lam``:
+    ``[>= t + 1]`` gate prefixes (natural log) or None with ``logf`` None.
+    Returns ``(out [d], lse)``.
+    """
+    for a in (kc, vc) + (() if lam is None else (lam,)):
+        assert a.dtype == np.float64 and a.flags.c_contiguous
+    q, k, v, w = (_f64(x) for x in (q, k, v, w))
+    d = q.shape[0]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    lf = None if logf is None else np.array([float(logf)], dtype=np.float64)
+    out = np.zeros(d)
+    lse = np.zeros(1)
+    rc = _load().path_oracle_decode_step(int(t), d, _ptr(kc), _ptr(vc), _ptr(lam), _ptr(q),
+                                         _ptr(k), _ptr(v), _ptr(w), float(beta), _ptr(lf),
+                                         float(scale), _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise RuntimeError(f"path_oracle_decode_step failed with status {rc}")
+    return out, float(lse[0])

@@ -167,3 +167,70 @@ int path_oracle_logits(int T, int d, const double *q, const double *k,
   free(z);
   return 0;
 }
+
+/*
+ * Keys of one head as a decoder holds them after token t ("PaTH Attention
+ * ..." slides, frame "Decoding updates historical keys in place"): every new
+ * token t' rewrites each earlier key k_j <- k_j - beta_t' w_t' (w_t'^T k_j),
+ * so after token t the cache holds k_j^(t) = H_t ... H_{j+1} k_j for j < t and
+ * k_t itself.  Written literally: H_{j+1} is applied first, H_t last.
+ * k, w: [T, d]; beta: [T]; out: [t + 1, d].  Requires 0 <= t < T.
+ */
+int path_oracle_decoded_keys(int T, int d, const double *k, const double *w,
+                             const double *beta, int t, double *out) {
+  if (T < 1 || d < 1 || t < 0 || t >= T || !k || !w || !beta || !out) return -1;
+  for (int j = 0; j <= t; ++j) {
+    double *z = out + (size_t)j * d;
+    memcpy(z, k + (size_t)j * d, sizeof(double) * (size_t)d);
+    for (int s = j + 1; s <= t; ++s) {
+      const double *ws = w + (size_t)s * d;
+      double wz = 0.0;
+      for (int m = 0; m < d; ++m) wz += ws[m] * z[m];
+      const double c = beta[s] * wz;
+      for (int m = 0; m < d; ++m) z[m] -= c * ws[m];
+    }
+  }
+  return 0;
+}
+
+/*
+ * One decoding step of one head, literally as the slides' frame "Decoding
+ * updates historical keys in place" describes it, with the FoX gate of frame
+ * "FoX adds a separate mechanism for forgetting":
+ *   1. every cached key j < t is rewritten k_j <- k_j - beta w (w^T k_j) with
+ *      the new token's (w, beta);
+ *   2. the new key, value and gate prefix are appended at row t:
+ *      lam[t] = lam[t-1] + logf (lam[0] = logf), lam[j] = sum_{s<=j} log f_s;
+ *   3. standard causal softmax readout over rows 0..t:
+ *      s_j = scale * k_j^T q + (lam[t] - lam[j]).
+ * kc, vc: [t + 1, d] (rows < t hold the cache, row t is written); lam: [t + 1]
+ * or NULL together with logf.  out: [d]; *lse: natural log.
+ */
+int path_oracle_decode_step(int t, int d, double *kc, double *vc, double *lam,
+                            const double *q, const double *k, const double *v,
+                            const double *w, double beta, const double *logf,
+                            double scale, double *out, double *lse) {
+  if (t < 0 || d < 1 || !kc || !vc || !q || !k || !v || !w || !out || !lse) return -1;
+  if ((lam == NULL) != (logf == NULL)) return -1;
+  for (int j = 0; j < t; ++j) {
+    double *kj = kc + (size_t)j * d;
+    double wk = 0.0;
+    for (int m = 0; m < d; ++m) wk += w[m] * kj[m];
+    const double c = beta * wk;
+    for (int m = 0; m < d; ++m) kj[m] -= c * w[m];
+  }
+  memcpy(kc + (size_t)t * d, k, sizeof(double) * (size_t)d);
+  memcpy(vc + (size_t)t * d, v, sizeof(double) * (size_t)d);
+  if (lam) lam[t] = (t > 0 ? lam[t - 1] : 0.0) + *logf;
+  double *s = (double *)malloc(sizeof(double) * (size_t)(t + 1));
+  if (!s) return -2;
+  for (int j = 0; j <= t; ++j) {
+    const double *kj = kc + (size_t)j * d;
+    double dot = 0.0;
+    for (int m = 0; m < d; ++m) dot += kj[m] * q[m];
+    s[j] = scale * dot + (lam ? lam[t] - lam[j] : 0.0);
+  }
+  path_row_readout(d, vc, t, s, out, lse);
+  free(s);
+  return 0;
+}

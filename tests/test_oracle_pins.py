@@ -19,7 +19,8 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import path_oracle_fwd, path_oracle_logits
+from oracle import (path_oracle_decode_step, path_oracle_decoded_keys, path_oracle_fwd,
+                    path_oracle_logits)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -346,3 +347,69 @@ def test_oracle_rejects_bad_rows():
     q, k, v, w, b = _rand_inputs(rng, 5, 3)
     with pytest.raises(RuntimeError):
         path_oracle_fwd(q, k, v, w, b, rows=[5])
+
+
+# ------------------------------------------- decoding: keys rewritten in place
+def test_decoded_keys_give_the_path_logits():
+    """(k_j^(t))^T q_t = k_j^T H_{j+1} .. H_t q_t (frame "Decoding updates
+    historical keys in place"), checked against the pinned logits."""
+    rng = np.random.default_rng(21)
+    T, d = 26, 7
+    q, k, _, w, b = _rand_inputs(rng, T, d)
+    for t in (0, 1, 12, T - 1):
+        kt = path_oracle_decoded_keys(k, w, b, t)
+        s = path_oracle_logits(q, k, w, b, t, scale=1.0)
+        np.testing.assert_allclose(kt @ q[t], s, atol=1e-12, rtol=0)
+        np.testing.assert_array_equal(kt[t], k[t])  # the newest key is untouched
+
+
+def test_decoded_keys_match_explicit_products_and_one_step_update():
+    rng = np.random.default_rng(22)
+    T, d = 12, 5
+    _, k, _, w, b = _rand_inputs(rng, T, d)
+    H = [np.eye(d) - b[t] * np.outer(w[t], w[t]) for t in range(T)]
+    t = T - 1
+    kt = path_oracle_decoded_keys(k, w, b, t)
+    for j in range(t + 1):
+        P = np.eye(d)
+        for s_ in range(j + 1, t + 1):  # H_t ... H_{j+1}
+            P = H[s_] @ P
+        np.testing.assert_allclose(kt[j], P @ k[j], atol=1e-12)
+    # one decoding step is the rank-one rewrite of every earlier key
+    prev = path_oracle_decoded_keys(k, w, b, t - 1)
+    step = prev - b[t] * np.outer(prev @ w[t], w[t])
+    np.testing.assert_allclose(kt[:t], step, atol=1e-12)
+
+
+@pytest.mark.parametrize("fox", [False, True])
+def test_decoding_token_by_token_reproduces_the_forward(fox):
+    """Decoding from an empty cache gives every row of the (pinned) forward,
+    and leaves the cache holding the keys aligned to the last token."""
+    rng = np.random.default_rng(23)
+    T, d = 33, 6
+    q, k, v, w, b = _rand_inputs(rng, T, d)
+    logf = np.log(rng.uniform(0.6, 1.0, T)) if fox else None
+    scale = 0.41
+    ref_out, ref_lse = path_oracle_fwd(q, k, v, w, b, logf=logf, scale=scale)
+    kc, vc = np.zeros((T, d)), np.zeros((T, d))
+    lam = np.zeros(T) if fox else None
+    for t in range(T):
+        o, l = path_oracle_decode_step(kc, vc, lam, q[t], k[t], v[t], w[t], b[t],
+                                       None if logf is None else logf[t], t, scale=scale)
+        np.testing.assert_allclose(o, ref_out[t], atol=1e-12, rtol=0)
+        assert abs(l - ref_lse[t]) < 1e-12
+    np.testing.assert_allclose(kc, path_oracle_decoded_keys(k, w, b, T - 1), atol=1e-12)
+    np.testing.assert_array_equal(vc, v)
+    if fox:
+        np.testing.assert_allclose(lam, np.cumsum(logf), atol=1e-13)
+
+
+def test_decoding_first_token_attends_to_itself():
+    rng = np.random.default_rng(24)
+    d = 5
+    q, k, v, w, b = _rand_inputs(rng, 1, d)
+    kc, vc = np.zeros((1, d)), np.zeros((1, d))
+    o, l = path_oracle_decode_step(kc, vc, None, q[0], k[0], v[0], w[0], b[0], None, 0,
+                                   scale=0.3)
+    np.testing.assert_array_equal(o, v[0])
+    assert abs(l - 0.3 * (k[0] @ q[0])) < 1e-15
