@@ -5,7 +5,10 @@
 
 One step is one full forward (chunk preparation + attention scan) over one
 batch of seeded synthetic inputs of the named workload, inputs resident in
-HBM.  The JSON line reports issued TFLOP/s (formulas in ``step_flops``),
+HBM.  With a decoding workload (``--workload decode_t16k_d128``) one step is
+one decoding step of every (b, h) at the last position of a full key/value
+cache (keys rewritten in place); that line reports GB/s of algorithmic HBM
+traffic against the measured copy bandwidth.  The JSON line reports issued TFLOP/s (formulas in ``step_flops``),
 ms per step, the roofline of the attention kernel, an end-to-end number
 through the host-buffer C-ABI entry, sampled SM clocks and a CPU-oracle
 baseline.  ``--impl reference`` times the fp64 CPU oracle instead, on a
@@ -210,6 +213,173 @@ def full_units(wl):
     return wl.B * wl.H * wl.T * (wl.T + 1) // 2
 
 
+# ------------------------------------------------------------------ decoding
+DECODE_METRIC = "PaTH decode step (keys rewritten in place) GB/s at B=2,T=16384,H=16,d=128 bf16"
+
+
+def decode_bytes(wl):
+    """Algorithmic HBM bytes of one decoding step at position T - 1: every
+    cached key read and written back (fp32), every cached value read, the
+    gate prefixes read (gated only), plus the new token in and out."""
+    es = 2 if wl.dtype == "bf16" else 4
+    t = wl.T - 1
+    per_head = t * wl.d * (4 + 4 + es) + (t * 4 if wl.fox else 0)
+    per_head += 5 * wl.d * es + wl.d * (4 + es) + 16  # q k v w in, out, cache row, scalars
+    return wl.B * wl.H * per_head
+
+
+def oracle_decode_sample(wl, budget_s):
+    """Seconds per (b, h) decoding step of the fp64 oracle, timed on a sample
+    of heads of the workload; returns (seconds per head, description)."""
+    import numpy as np
+
+    from oracle import path_oracle_decode_step
+    from seeded_inputs import make_decode_inputs
+
+    x = make_decode_inputs(wl.with_(B=1, H=1))
+    f = lambda t: None if t is None else t.double().numpy()[0, 0]
+    kc0, vc0, lam0 = f(x["kcache"]), f(x["vcache"]), f(x["lamcache"])
+    one = {n: f(x[n]) for n in ("q", "k", "v", "w", "beta", "logf")}
+    n, spent = 0, 0.0
+    while spent < budget_s or n == 0:
+        kc, vc = kc0.copy(), vc0.copy()
+        lam = None if lam0 is None else lam0.copy()
+        t0 = time.perf_counter()
+        path_oracle_decode_step(kc, vc, lam, one["q"], one["k"], one["v"], one["w"],
+                                float(one["beta"]), None if one["logf"] is None else float(one["logf"]),
+                                wl.T - 1, scale=x["scale"])
+        spent += time.perf_counter() - t0
+        n += 1
+    return spent / n, (f"{n} single-head decoding steps at position {wl.T - 1} of {wl.name}, "
+                       f"{spent:.1f} s on one core; extrapolated to all B*H heads")
+
+
+def run_decode(args, wl):
+    import torch
+
+    import householder_softmax_attention_gb300 as pa
+    from seeded_inputs import make_decode_inputs
+
+    rank, world, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pa.load_library()
+    x = make_decode_inputs(wl, device=dev)
+    cache = pa.DecodeCache.wrap(x["kcache"], x["vcache"], x["lamcache"])
+    q, k, v, w, beta, logf, scale = (x[n] for n in ("q", "k", "v", "w", "beta", "logf", "scale"))
+    pos = torch.full((wl.B,), wl.T - 1, dtype=torch.int32, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty(beta.shape, device=dev, dtype=torch.float32)
+    st = torch.cuda.current_stream(dev)
+
+    def step():
+        pa.path_attn_decode_step(q, k, v, w, beta, logf, cache, pos, wl.T, scale, out=out,
+                                 lse=lse, stream=st)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    assert pa.path_attn_device_status(local, True) == 0, "a decoding kernel reported an error"
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        e0.record(st)
+        for _ in range(args.steps):
+            step()
+        e1.record(st)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    ms = reduce_max(e0.elapsed_time(e1) / args.steps, world)
+    assert pa.path_attn_device_status(local, True) == 0, "a decoding kernel reported an error"
+    nbytes = decode_bytes(wl)
+    value = world * nbytes / (ms * 1e-3) / 1e9
+    _, hbm, peak_src = _peaks()
+    roofline = {"bound": "hbm", "achieved": nbytes / (ms * 1e-3) / 1e9, "peak": hbm,
+                "unit": "GB/s", "frac": nbytes / (ms * 1e-3) / 1e9 / hbm,
+                "traffic": args.traffic, "kernel": "decode_split_kernel + decode_combine_kernel",
+                "peak_source": f"{peak_src} copy bandwidth",
+                "avg_launch_ms": ms, "algorithmic_bytes": nbytes}
+
+    # end to end through the Python API: the new token from pinned host memory,
+    # the step, out and lse back to the host, every step
+    hx = {n: x[n].cpu().pin_memory() for n in ("q", "k", "v", "w", "beta") }
+    if logf is not None:
+        hx["logf"] = logf.cpu().pin_memory()
+    dx = {n: torch.empty_like(t, device=dev) for n, t in hx.items()}
+    hout = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    hlse = torch.empty(beta.shape, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        for n, t in hx.items():
+            dx[n].copy_(t, non_blocking=True)
+        pa.path_attn_decode_step(dx["q"], dx["k"], dx["v"], dx["w"], dx["beta"], dx.get("logf"),
+                                 cache, pos, wl.T, scale, out=out, lse=lse, stream=st)
+        hout.copy_(out, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+        st.synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    barrier(world)
+    t0 = time.perf_counter()
+    n_e2e = max(1, args.steps)
+    for _ in range(n_e2e):
+        e2e_step()
+    e2e_ms = reduce_max((time.perf_counter() - t0) * 1e3 / n_e2e, world)
+    h2d = sum(t.numel() * t.element_size() for t in hx.values())
+    line = {
+        "metric": DECODE_METRIC if wl.name == "decode_t16k_d128" else f"PaTH decode step GB/s, {wl.name}",
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "cache_rows": wl.T, "d": wl.d,
+                   "fox": wl.fox, "position": wl.T - 1, "parallelism": f"replicas x{world}",
+                   "l2": f"cache larger than L2: {nbytes / 2**20:.0f} MiB moved per step"},
+        "roofline": roofline,
+        "e2e": {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": hout.numel() * hout.element_size() + hlse.numel() * 4},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        sec, desc = oracle_decode_sample(wl, min(args.cpu_budget_s, 10.0))
+        est = sec * wl.B * wl.H
+        line["cpu_baseline"] = {"value": nbytes / est / 1e9, "unit": "GB/s", "cores": 1,
+                                "kind": "oracle", "sample": desc, "est_full_step_s": est}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_decode_reference(args, wl):
+    rank, world, _ = dist_setup()
+    if rank != 0:
+        return 0
+    per_step = []
+    for s in range(args.warmup + args.steps):
+        sec, desc = oracle_decode_sample(wl, min(args.ref_step_s, 2.0))
+        if s >= args.warmup:
+            per_step.append(sec * wl.B * wl.H)
+    est = statistics.median(per_step)
+    value = decode_bytes(wl) / est / 1e9
+    line = {
+        "impl": "reference", "metric": DECODE_METRIC if wl.name == "decode_t16k_d128"
+        else f"PaTH decode step GB/s, {wl.name}", "value": value, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": est * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "cache_rows": wl.T, "d": wl.d},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 # ------------------------------------------------------------------ arms
 def run_reference(args, wl, flops):
     rank, world, _ = dist_setup()
@@ -362,7 +532,12 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
-    from seeded_inputs import WORKLOADS
+    from seeded_inputs import DECODE_WORKLOADS, WORKLOADS
+    if args.workload in DECODE_WORKLOADS:
+        wl = DECODE_WORKLOADS[args.workload]
+        if args.B or args.H:
+            wl = wl.with_(B=args.B or wl.B, H=args.H or wl.H)
+        return run_decode_reference(args, wl) if args.impl == "reference" else run_decode(args, wl)
     wl = WORKLOADS[args.workload]
     if args.B or args.H:
         wl = wl.with_(B=args.B or wl.B, H=args.H or wl.H, name=f"{wl.name}_B{args.B or wl.B}H{args.H or wl.H}")

@@ -21,7 +21,8 @@ import threading
 
 __all__ = [
     "PathAttnError", "load_library", "path_attn_fwd", "path_attn_fwd_host",
-    "path_attn_fwd_noalloc", "path_attn_debug_wait_timeout",
+    "path_attn_fwd_noalloc", "path_attn_debug_wait_timeout", "path_attn_prefill",
+    "path_attn_decode_step", "DecodeCache",
     "path_attn_debug_factors", "path_attn_device_status", "path_attn_workspace_bytes",
     "path_attn_chunk_size", "path_attn_launches_per_call", "path_attn_timing_enable",
     "path_attn_timing_read", "path_attn_version", "path_attn_status_string",
@@ -97,6 +98,12 @@ def load_library(path: str | None = None):
         lib.path_attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, fp, fp, f, vp, fp, vp,
                                               i, i, i, i, i, vp]
         lib.path_attn_fwd_noalloc.restype = i
+        lib.path_attn_prefill.argtypes = [vp, vp, vp, vp, fp, fp, f, vp, fp, fp, vp, fp, i,
+                                          i, i, i, i, i, vp]
+        lib.path_attn_prefill.restype = i
+        lib.path_attn_decode_step.argtypes = [vp, vp, vp, vp, fp, fp, f, fp, vp, fp, vp, i,
+                                              vp, fp, i, i, i, i, i, vp]
+        lib.path_attn_decode_step.restype = i
         _lib = lib
         return lib
 
@@ -220,6 +227,109 @@ def path_attn_fwd_noalloc(q, k, v, w, beta, logf=None, scale=None, out=None, lse
     return out, lse
 
 
+class DecodeCache:
+    """Device caches of one decoder (layout of ``include/pathattn.h``):
+    ``kcache [B, H, Tmax, d]`` float32 (keys carried to the latest token),
+    ``vcache [B, H, Tmax, d]`` in the model dtype, ``lamcache [B, H, Tmax]``
+    float32 (gate prefixes; None without a gate)."""
+
+    def __init__(self, B, H, Tmax, d, dtype, device, gated=False):
+        import torch
+        self.B, self.H, self.Tmax, self.d = B, H, Tmax, d
+        self.kcache = torch.zeros((B, H, Tmax, d), device=device, dtype=torch.float32)
+        self.vcache = torch.zeros((B, H, Tmax, d), device=device, dtype=dtype)
+        self.lamcache = (torch.zeros((B, H, Tmax), device=device, dtype=torch.float32)
+                         if gated else None)
+
+    @classmethod
+    def wrap(cls, kcache, vcache, lamcache=None):
+        """A cache over existing tensors (kept, not copied)."""
+        self = cls.__new__(cls)
+        self.B, self.H, self.Tmax, self.d = kcache.shape
+        import torch
+        if kcache.dtype != torch.float32 or vcache.shape != kcache.shape:
+            raise ValueError("kcache must be float32 and share [B, H, Tmax, d] with vcache")
+        for t in (kcache, vcache, lamcache):
+            if t is not None and not t.is_contiguous():
+                raise ValueError("cache tensors must be contiguous")
+        if lamcache is not None and lamcache.shape != kcache.shape[:-1]:
+            raise ValueError("lamcache must be [B, H, Tmax]")
+        self.kcache, self.vcache, self.lamcache = kcache, vcache, lamcache
+        return self
+
+    def rows(self, b0, b1):
+        """The caches of batch rows b0..b1-1 (views of the same memory)."""
+        return DecodeCache.wrap(self.kcache[b0:b1], self.vcache[b0:b1],
+                                None if self.lamcache is None else self.lamcache[b0:b1])
+
+
+def path_attn_prefill(q, k, v, w, beta, logf, cache: DecodeCache, scale=None, out=None,
+                      lse=None, want_lse=True, stream=None):
+    """``path_attn_fwd`` over a prompt that also fills rows ``0..T-1`` of
+    ``cache`` (keys carried to the prompt end, values, gate prefixes)."""
+    import torch
+    lib = load_library()
+    _check_inputs(q, k, v, w, beta, logf, True)
+    B, H, T, d = q.shape
+    if (B, H, d) != (cache.B, cache.H, cache.d) or cache.vcache.dtype != q.dtype:
+        raise ValueError("cache does not match the inputs")
+    if (logf is None) != (cache.lamcache is None):
+        raise ValueError("a gated prompt needs a gated cache and the reverse")
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, T), device=q.device, dtype=torch.float32)
+    st = stream if stream is not None else torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        rc = lib.path_attn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(beta), _ptr(logf),
+                                   float(scale), _ptr(out), _ptr(lse), _ptr(cache.kcache),
+                                   _ptr(cache.vcache), _ptr(cache.lamcache), cache.Tmax,
+                                   B, H, T, d, _dtype_code(q), ctypes.c_void_p(st.cuda_stream))
+    _check(rc, "path_attn_prefill")
+    return out, lse
+
+
+def path_attn_decode_step(q, k, v, w, beta, logf, cache: DecodeCache, pos, max_len,
+                          scale=None, out=None, lse=None, want_lse=True, stream=None):
+    """One decoding step: ``q, k, v, w [B, H, d]``, ``beta`` (and ``logf``)
+    ``[B, H]`` float32, ``pos`` a device int32 ``[B]`` tensor with each batch
+    row's position, ``max_len`` a host bound above every ``pos[b]``.  Rewrites
+    the cached keys in place, appends the new token, returns ``(out, lse)``."""
+    import torch
+    lib = load_library()
+    for name, t in (("q", q), ("k", k), ("v", v), ("w", w)):
+        if t.dim() != 3 or t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [B, H, d] tensor like q")
+    B, H, d = q.shape
+    for name, t in (("beta", beta), ("logf", logf)):
+        if t is not None and (t.shape != (B, H) or t.dtype != torch.float32
+                              or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous float32 [B, H] tensor")
+    if pos.dtype != torch.int32 or pos.shape != (B,) or not pos.is_cuda:
+        raise ValueError("pos must be a device int32 [B] tensor")
+    if (B, H, d) != (cache.B, cache.H, cache.d) or cache.vcache.dtype != q.dtype:
+        raise ValueError("cache does not match the inputs")
+    if (logf is None) != (cache.lamcache is None):
+        raise ValueError("a gated step needs a gated cache and the reverse")
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H), device=q.device, dtype=torch.float32)
+    st = stream if stream is not None else torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        rc = lib.path_attn_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(beta), _ptr(logf),
+                                       float(scale), _ptr(cache.kcache), _ptr(cache.vcache),
+                                       _ptr(cache.lamcache), _ptr(pos), int(max_len), _ptr(out),
+                                       _ptr(lse), B, H, cache.Tmax, d, _dtype_code(q),
+                                       ctypes.c_void_p(st.cuda_stream))
+    _check(rc, "path_attn_decode_step")
+    return out, lse
+
+
 def path_attn_chunk_size(d: int, dtype_code: int) -> int:
     c = load_library().path_attn_chunk_size(d, dtype_code)
     if c < 0:
@@ -265,8 +375,10 @@ def path_attn_debug_wait_timeout(limit_ns: int, stream=None):
 
 
 def path_attn_device_status(device: int = 0, clear: bool = True) -> int:
-    """0 if no kernel wait expired on ``device`` since the last clear, else a
-    negative status (PATH_ERR_TIMEOUT).  Synchronises the device."""
+    """0 if no kernel reported an error on ``device`` since the last clear,
+    else a negative status: PATH_ERR_TIMEOUT (a bounded wait expired) or
+    PATH_ERR_INVALID_ARG (a decoding position out of bounds).  Synchronises
+    the device."""
     return load_library().path_attn_device_status(device, 1 if clear else 0)
 
 

@@ -5,6 +5,7 @@
 // calls).  Kernels report bounded-wait expiry through a per-device status word.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <climits>
 #include <cstdio>
 #include <cstdint>
@@ -27,6 +28,7 @@ struct DeviceState {
   cudaMemPool_t pool = nullptr;
   int* status = nullptr;  // device int, 0 = fine
   int cc_major = 0, cc_minor = 0;
+  int num_sms = 0;
 };
 
 std::mutex g_mu;
@@ -59,6 +61,7 @@ int device_state(DeviceState** out) {
     if ((e = cudaGetDeviceProperties(&prop, dev)) != cudaSuccess) return set_cuda_error(e);
     s.cc_major = prop.major;
     s.cc_minor = prop.minor;
+    s.num_sms = prop.multiProcessorCount;
     cudaMemPoolProps props;
     std::memset(&props, 0, sizeof(props));
     props.allocType = cudaMemAllocationTypePinned;
@@ -261,6 +264,90 @@ int path_attn_fwd_host(const void* q, const void* k, const void* v, const void* 
   return rc;
 }
 
+int path_attn_prefill(const void* q, const void* k, const void* v, const void* w,
+                      const float* beta, const float* logf, float scale, void* out,
+                      float* lse, float* kcache, void* vcache, float* lamcache, int Tmax,
+                      int B, int H, int T, int d, int dtype, void* stream) {
+  if (!q || !k || !v || !w || !beta || !out || !kcache || !vcache) return PATH_ERR_INVALID_ARG;
+  if ((logf != nullptr) != (lamcache != nullptr)) return PATH_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(w) || !aligned16(beta) ||
+      !aligned16(out) || (logf && !aligned16(logf)) || (lse && !aligned16(lse)) ||
+      !aligned16(kcache) || !aligned16(vcache) || (lamcache && !aligned16(lamcache)))
+    return PATH_ERR_INVALID_ARG;
+  if (!(scale == scale) || Tmax < T) return PATH_ERR_INVALID_ARG;
+  Geom g;
+  int rc = make_geom(B, H, T, d, dtype, logf != nullptr, &g);
+  if (rc != PATH_OK) return rc;
+  DeviceState* s = nullptr;
+  if ((rc = device_state(&s)) != PATH_OK) return rc;
+  if ((rc = check_device(s)) != PATH_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t bytes = workspace_layout(g, nullptr, nullptr);
+  void* ws = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&ws, bytes, s->pool, st);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  Inputs in{q, k, v, w, beta, logf, scale, out, lse};
+  rc = run_forward(g, in, static_cast<char*>(ws), s, st);
+  if (rc == PATH_OK) {
+    Workspace wsp;
+    workspace_layout(g, static_cast<char*>(ws), &wsp);
+    const size_t es = g.bf16 ? 2 : 4;
+    const size_t row = static_cast<size_t>(d) * es;
+    if ((e = launch_align_keys(g, wsp, kcache, Tmax, st)) != cudaSuccess ||
+        (e = cudaMemcpy2DAsync(vcache, row * Tmax, v, row * T, row * T, g.BH,
+                               cudaMemcpyDeviceToDevice, st)) != cudaSuccess ||
+        (logf && (e = launch_gate_prefix(logf, lamcache, g.BH, T, T, static_cast<size_t>(Tmax),
+                                         1.0, st)) != cudaSuccess))
+      rc = set_cuda_error(e);
+  }
+  e = cudaFreeAsync(ws, st);
+  if (rc == PATH_OK && e != cudaSuccess) rc = set_cuda_error(e);
+  return rc;
+}
+
+int path_attn_decode_step(const void* q, const void* k, const void* v, const void* w,
+                          const float* beta, const float* logf, float scale, float* kcache,
+                          void* vcache, float* lamcache, const int* pos, int max_len,
+                          void* out, float* lse, int B, int H, int Tmax, int d, int dtype,
+                          void* stream) {
+  if (!q || !k || !v || !w || !beta || !out || !kcache || !vcache || !pos)
+    return PATH_ERR_INVALID_ARG;
+  if ((logf != nullptr) != (lamcache != nullptr)) return PATH_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(w) || !aligned16(beta) ||
+      !aligned16(out) || (logf && !aligned16(logf)) || (lse && !aligned16(lse)) ||
+      !aligned16(kcache) || !aligned16(vcache) || (lamcache && !aligned16(lamcache)))
+    return PATH_ERR_INVALID_ARG;
+  if (!(scale == scale) || B < 1 || H < 1 || Tmax < 1 || max_len < 1 || max_len > Tmax)
+    return PATH_ERR_INVALID_ARG;
+  if (chunk_size(d, dtype) < 0) return chunk_size(d, dtype);
+  const long long BH = static_cast<long long>(B) * H;
+  if (BH > 65535) return PATH_ERR_UNSUPPORTED;  // grid.y of the span kernel
+  DeviceState* s = nullptr;
+  int rc = device_state(&s);
+  if (rc != PATH_OK) return rc;
+  if ((rc = check_device(s)) != PATH_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // spans of whole tiles, about two CTAs per SM when there are few heads
+  const int tile = decode_tile_keys(d);
+  const long long tiles = std::max<long long>(1, (max_len - 1 + tile - 1) / tile);
+  long long nsplit = std::max<long long>(1, 2LL * s->num_sms / BH);
+  nsplit = std::min(nsplit, tiles);
+  const long long per = (tiles + nsplit - 1) / nsplit;
+  nsplit = (tiles + per - 1) / per;
+  float* part = nullptr;
+  const size_t part_bytes = static_cast<size_t>(BH) * nsplit * (d + 2) * sizeof(float);
+  cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&part), part_bytes, s->pool, st);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  DecodeParams p{q, k, v, w, beta, logf, scale, kcache, vcache, lamcache, pos, H, Tmax, max_len,
+                 static_cast<int>(nsplit), static_cast<int>(per * tile), part, out, lse,
+                 s->status};
+  if ((e = launch_decode(p, static_cast<int>(BH), d, dtype == PATH_DTYPE_BF16, st)) != cudaSuccess)
+    rc = set_cuda_error(e);
+  e = cudaFreeAsync(part, st);
+  if (rc == PATH_OK && e != cudaSuccess) rc = set_cuda_error(e);
+  return rc;
+}
+
 int path_attn_device_status(int device, int clear) {
   int prev = 0;
   cudaError_t e = cudaGetDevice(&prev);
@@ -277,7 +364,8 @@ int path_attn_device_status(int device, int clear) {
   }
   cudaSetDevice(prev);
   if (rc != PATH_OK) return rc;
-  return word == PATH_DEV_OK ? PATH_OK : PATH_ERR_TIMEOUT;
+  if (word == PATH_DEV_OK) return PATH_OK;
+  return word == PATH_DEV_ERR_BAD_POS ? PATH_ERR_INVALID_ARG : PATH_ERR_TIMEOUT;
 }
 
 int path_attn_timing_enable(int enable) {

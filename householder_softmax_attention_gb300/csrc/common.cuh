@@ -14,6 +14,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 // Device status word values (stored in a per-device int; 0 = fine).
 constexpr int PATH_DEV_OK = 0;
 constexpr int PATH_DEV_ERR_TIMEOUT = 1;
+constexpr int PATH_DEV_ERR_BAD_POS = 2;  // a decoding position outside its bounds
 
 // Time limit of every bounded wait inside the kernels.
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
@@ -111,6 +112,38 @@ cudaError_t launch_attn_f32(const Geom& g, const Inputs& in, const Workspace& ws
 // bf16 attention over the prepared chunks (tcgen05 / TMEM / TMA).
 cudaError_t launch_attn_tc(const Geom& g, const Inputs& in, const Workspace& ws,
                            int* dev_status, cudaStream_t st, int* launches);
+// Decoding over a key cache rewritten in place (decode.cu).  Per head bh:
+//   q, k, v, w [bh][d] elem; beta, logf [bh] f32 (logf may be null)
+//   kcache [bh][Tmax][d] f32; vcache [bh][Tmax][d] elem; lamcache [bh][Tmax] f32
+//   pos [B] int32: position of the new token of each batch row
+//   part [bh][nsplit][d + 2] f32 scratch: (max, sum, o) of each key span
+struct DecodeParams {
+  const void *q, *k, *v, *w;
+  const float *beta, *logf;
+  float scale;
+  float* kcache;
+  void* vcache;
+  float* lamcache;
+  const int* pos;
+  int H, Tmax, max_len;
+  int nsplit, span;  // spans of `span` cached keys (a multiple of the tile)
+  float* part;
+  void* out;
+  float* lse;
+  int* status;
+};
+// Key rows per pipeline stage of the decoding kernel (spans are multiples).
+int decode_tile_keys(int d);
+// Two launches: the span kernel, then the per-head merge + append.
+cudaError_t launch_decode(const DecodeParams& p, int BH, int d, bool bf16, cudaStream_t st);
+// Prefill: kcache rows j < T of each head <- key j carried to token T - 1,
+// from the chunk factors kr and ngt of a prepared workspace.
+cudaError_t launch_align_keys(const Geom& g, const Workspace& ws, float* kcache, int Tmax,
+                              cudaStream_t st);
+// Gate prefix: out[bh * out_stride + t] = mult * sum_{s<=t} logf[bh][s] for
+// t < n_out (tokens at or past T add 0).
+cudaError_t launch_gate_prefix(const float* logf, float* out, int BH, int T, int n_out,
+                               size_t out_stride, double mult, cudaStream_t st);
 // Diagnostics: a kernel whose bounded wait can only expire (sets *status).
 cudaError_t launch_debug_wait(int* status, unsigned long long limit_ns, cudaStream_t st);
 

@@ -257,8 +257,10 @@ __global__ void tri_solve_kernel(float* lmat, const float* beta, int C, int T, i
 }
 
 // ------------------------------------------------------------ gate prefix sum
-// lam2[bh][t] = log2(e) * sum_{s<=t} logf[bh][s], padding tokens add 0.
-__global__ void gate_cumsum_kernel(const float* logf, float* lam2, int T, int Tp) {
+// out[bh * out_stride + t] = mult * sum_{s<=t} logf[bh][s] for t < n_out;
+// tokens at or past T (chunk padding) add 0.  Accumulated in fp64.
+__global__ void gate_cumsum_kernel(const float* logf, float* out_base, int T, int Tp,
+                                   size_t out_stride, double mult) {
   __shared__ double warp_tot[32];
   const int bh = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
   const int seg = (Tp + nt - 1) / nt;
@@ -285,14 +287,20 @@ __global__ void gate_cumsum_kernel(const float* logf, float* lam2, int T, int Tp
   }
   __syncthreads();
   double run = (inc - local) + (wid > 0 ? warp_tot[wid - 1] : 0.0);
-  float* out = lam2 + static_cast<size_t>(bh) * Tp;
+  float* out = out_base + static_cast<size_t>(bh) * out_stride;
   for (int t = t0; t < t0 + seg && t < Tp; ++t) {
     run += t < T ? static_cast<double>(lf[t]) : 0.0;
-    out[t] = static_cast<float>(run * 1.4426950408889634);
+    out[t] = static_cast<float>(run * mult);
   }
 }
 
 }  // namespace
+
+cudaError_t launch_gate_prefix(const float* logf, float* out, int BH, int T, int n_out,
+                               size_t out_stride, double mult, cudaStream_t st) {
+  gate_cumsum_kernel<<<BH, 1024, 0, st>>>(logf, out, T, n_out, out_stride, mult);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_prep(const Geom& g, const Inputs& in, const Workspace& ws, int* dev_status,
                         cudaStream_t st, int* launches) {
@@ -300,8 +308,9 @@ cudaError_t launch_prep(const Geom& g, const Inputs& in, const Workspace& ws, in
   cudaError_t e;
   int n = 0;
   if (g.gate) {
-    gate_cumsum_kernel<<<g.BH, 1024, 0, st>>>(in.logf, ws.lam2, g.T, g.Tp);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_gate_prefix(in.logf, ws.lam2, g.BH, g.T, g.Tp, static_cast<size_t>(g.Tp),
+                                1.4426950408889634, st)) != cudaSuccess)
+      return e;
     ++n;
   }
   if (g.bf16) {

@@ -87,6 +87,64 @@ int path_attn_fwd_host(const void* q, const void* k, const void* v, const void* 
                        const float* beta, const float* logf, float scale, void* out,
                        float* lse, int B, int H, int T, int d, int dtype, void* stream);
 
+/*
+ * Decoding with keys rewritten in place (slides' frame "Decoding updates
+ * historical keys in place").  A decoder keeps, per (b, h), a key cache in
+ * which row j < t holds k_j carried to the latest token t - 1,
+ * H_{t-1} ... H_{j+1} k_j, a value cache, and (PaTH-FoX) the gate prefix
+ * lam_j = sum_{s<=j} log f_s.  Token t rewrites every cached key
+ * k_j <- k_j - beta_t w_t (w_t^T k_j), appends k_t, v_t, lam_t, and reads out
+ *   o_t = sum_{j<=t} softmax_j(scale * k_j^T q_t + lam_t - lam_j) v_j,
+ * which equals row t of path_attn_fwd over tokens 0..t.
+ *
+ * Cache layout (caller-owned device memory, 16-byte aligned):
+ *   kcache    [B,H,Tmax,d] fp32  (fp32 whatever dtype is: each key is rewritten
+ *             once per later token, and rounding would compound)
+ *   vcache    [B,H,Tmax,d] dtype
+ *   lamcache  [B,H,Tmax]   fp32, natural log; used only with a gate (else NULL)
+ *
+ * path_attn_prefill -- path_attn_fwd over a prompt of T tokens (same
+ * arguments and results) that also fills rows 0..T-1 of the caches: kcache
+ * with every key carried to token T - 1, vcache with v, lamcache (iff logf is
+ * not NULL) with the prefix sums.  Rows >= T are not touched.  Requires
+ * T <= Tmax.  The cached keys come from the forward's chunk factors: the keys
+ * of chunk c carried to the chunk end, times the product of the transitions of
+ * the later chunks (frames "Backup: fix orientation before implementing UT
+ * products" and "A right-to-left scan accumulates cross-block paths").
+ */
+int path_attn_prefill(const void* q, const void* k, const void* v, const void* w,
+                      const float* beta, const float* logf, float scale, void* out,
+                      float* lse, float* kcache, void* vcache, float* lamcache, int Tmax,
+                      int B, int H, int T, int d, int dtype, void* stream);
+
+/*
+ * path_attn_decode_step -- one decoding step for every (b, h).
+ *
+ *   q, k, v, w  device, [B,H,d], dtype     the new token of each (b, h)
+ *   beta        device, [B,H], fp32;  logf: device, [B,H], fp32, or NULL
+ *   kcache, vcache, lamcache   as above; for batch row b, rows < pos[b] are
+ *               the cache (rewritten in place), row pos[b] receives the new
+ *               key, value and gate prefix.  lamcache is required iff logf is
+ *               not NULL.
+ *   pos         device, [B], int32: position t of the new token of batch row
+ *               b (= its number of cached tokens); rows may differ
+ *   max_len     host int, 1 <= max_len <= Tmax; every pos[b] must be below
+ *               it.  It sizes the launch: the key cache is cut into spans
+ *               covering rows [0, max_len - 1).
+ *   out         device, [B,H,d], dtype;  lse: device, [B,H], fp32, or NULL
+ *
+ * Two kernel launches on `stream` and a small stream-ordered scratch
+ * ([B*H][spans][d+2] fp32) from the library's pool.  A pos[b] outside
+ * [0, max_len) is only visible on the device: that batch row's out and lse
+ * become NaN, its cache rows are left as they were, and
+ * path_attn_device_status() then returns PATH_ERR_INVALID_ARG.
+ */
+int path_attn_decode_step(const void* q, const void* k, const void* v, const void* w,
+                          const float* beta, const float* logf, float scale, float* kcache,
+                          void* vcache, float* lamcache, const int* pos, int max_len,
+                          void* out, float* lse, int B, int H, int Tmax, int d, int dtype,
+                          void* stream);
+
 /* Human-readable name of a path_status_t value (static storage). */
 const char* path_attn_status_string(int status);
 
@@ -111,8 +169,10 @@ int path_attn_chunk_size(int d, int dtype);
 
 /*
  * Device status word of `device` (0 = no error since the last clear; a
- * negative path_status_t such as PATH_ERR_TIMEOUT if a kernel's bounded wait
- * expired).  Synchronises that device first.  clear != 0 resets the word.
+ * negative path_status_t otherwise: PATH_ERR_TIMEOUT if a kernel's bounded
+ * wait expired, PATH_ERR_INVALID_ARG if path_attn_decode_step met a position
+ * outside its bounds).  Synchronises that device first.  clear != 0 resets
+ * the word.
  */
 int path_attn_device_status(int device, int clear);
 

@@ -103,6 +103,44 @@ def make_inputs(wl: Workload, device="cpu"):
                 beta=beta, logf=logf, scale=1.0 / math.sqrt(wl.d))
 
 
+# Decoding: one new token per (b, h) against a cache of Tmax rows.
+DECODE_WORKLOADS = {
+    "decode_t16k_d128": Workload("decode_t16k_d128", 2, 16, 16384, 128,
+                                 note="one decoding step at position T - 1 of a 16K cache"),
+    "decode_t16k_d64": Workload("decode_t16k_d64", 2, 32, 16384, 64),
+}
+
+
+def make_decode_inputs(wl: Workload, device="cpu"):
+    """Draw one decoding step of ``wl`` (T = cache rows): the new token's q, k,
+    v, w ([B,H,d], workload dtype), beta and logf ([B,H] fp32; logf only with
+    ``wl.fox``), and a synthetic cache state: kcache ~ N(0, 1) fp32 and vcache
+    ~ N(0, 1) ([B,H,T,d]); with ``wl.fox`` a decreasing lamcache ([B,H,T] fp32,
+    steps ~ U[0, 0.1)).  Returns a dict (also ``scale``)."""
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(wl.seed + 104729)
+    B, H, T, d = wl.B, wl.H, wl.T, wl.d
+    dt = wl.torch_dtype
+
+    def normal(shp):
+        return torch.randn(shp, generator=g, device=dev, dtype=torch.float32)
+
+    q, k, v, w = (normal((B, H, d)) for _ in range(4))
+    w = w / w.norm(dim=-1, keepdim=True).clamp_min(1e-30)
+    beta = (2.0 * torch.sigmoid(normal((B, H)))).clamp(0.0, 2.0).contiguous()
+    kcache = normal((B, H, T, d)).contiguous()
+    vcache = normal((B, H, T, d)).to(dt).contiguous()
+    logf = lamcache = None
+    if wl.fox:
+        logf = torch.log(torch.sigmoid(normal((B, H)) + 2.0)).contiguous()
+        steps = 0.1 * torch.rand((B, H, T), generator=g, device=dev)
+        lamcache = (-torch.cumsum(steps, dim=-1)).contiguous()
+    return dict(q=q.to(dt).contiguous(), k=k.to(dt).contiguous(), v=v.to(dt).contiguous(),
+                w=w.to(dt).contiguous(), beta=beta, logf=logf, kcache=kcache, vcache=vcache,
+                lamcache=lamcache, scale=1.0 / math.sqrt(d))
+
+
 def sample_rows(T: int, C: int, n_extra: int, seed: int = 0):
     """A fixed, seeded set of query rows of one head for sampled parity checks:
     the first and last rows, chunk boundaries around the first and last four

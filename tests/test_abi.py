@@ -94,3 +94,29 @@ def test_validation_happens_before_any_cuda_call(lib):
                                   None) == INVALID
     assert lib.path_attn_debug_factors(q, k, w, beta, None, 0.1, 1, 1, 8, 64, 1, None, None,
                                        None, None, None, None) == INVALID
+
+
+def test_decode_and_prefill_validate_before_any_cuda_call(lib):
+    g = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(12)]
+    q, k, v, w, beta, out, kc, vc, pos = g[:9]
+    lam, logf = g[9], g[10]
+    dec = lambda **kw: lib.path_attn_decode_step(
+        kw.get("q", q), k, v, w, beta, kw.get("logf"), kw.get("scale", 0.1), kw.get("kc", kc), vc,
+        kw.get("lam"), kw.get("pos", pos), kw.get("max_len", 8), out, None, 1, 1,
+        kw.get("Tmax", 8), kw.get("d", 64), 1, None)
+    assert dec(q=None) == INVALID
+    assert dec(pos=None) == INVALID
+    assert dec(kc=ctypes.c_void_p(0x70008)) == INVALID      # misaligned cache
+    assert dec(logf=logf) == INVALID                        # gate without its prefix cache
+    assert dec(lam=lam) == INVALID                          # prefix cache without a gate
+    assert dec(max_len=9) == INVALID                        # above Tmax
+    assert dec(max_len=0) == INVALID
+    assert dec(d=96) == UNSUPPORTED
+    assert dec(scale=float("nan")) == INVALID
+    pre = lambda **kw: lib.path_attn_prefill(
+        q, k, v, w, beta, kw.get("logf"), 0.1, out, None, kw.get("kc", kc), vc, kw.get("lam"),
+        kw.get("Tmax", 16), 1, 1, kw.get("T", 16), 64, 1, None)
+    assert pre(kc=None) == INVALID
+    assert pre(Tmax=15) == INVALID                          # cache shorter than the prompt
+    assert pre(logf=logf) == INVALID
+    assert pre(T=0) == INVALID
