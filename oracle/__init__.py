@@ -15,6 +15,8 @@ Two independent formulations live here, both in fp64:
 * ``path_oracle_decoded_keys`` / ``path_oracle_decode_step`` -- decoding with
   keys rewritten in place (frame "Decoding updates historical keys in place"),
   also in C.
+* ``path_oracle_partial_fwd`` -- partial PaTH (PaTH on the first r head
+  dimensions, no position encoding on the rest), in C.
 * ``chunked`` -- the blockwise UT-transform algebra in numpy (frames "A
   triangular representation makes paths computable", "A right-to-left scan
   accumulates cross-block paths" and "Backup: fix orientation before
@@ -73,6 +75,10 @@ def _load():
                 ctypes.c_int, ctypes.c_int, dp, dp, dp, dp, dp, dp, dp, ctypes.c_double,
                 dp, ctypes.c_double, dp, dp]
             lib.path_oracle_decode_step.restype = ctypes.c_int
+            lib.path_oracle_partial_fwd.argtypes = [
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, dp, dp, dp, dp, dp, dp,
+                ctypes.c_double, dp, dp]
+            lib.path_oracle_partial_fwd.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -186,3 +192,26 @@ def path_oracle_decode_step(kc, vc, lam, q, k, v, w, beta, logf, t, scale=None):
     if rc != 0:
         raise RuntimeError(f"path_oracle_decode_step failed with status {rc}")
     return out, float(lse[0])
+
+
+def path_oracle_partial_fwd(q, k, v, u, beta, logf=None, scale=None):
+    """Partial PaTH forward in fp64: PaTH with ``u [..., T, r]`` on the first
+    ``r`` head dimensions, plain dot products on the other ``d - r``.  Shapes
+    as ``path_oracle_fwd`` (``u`` has its own last dimension r, 0 <= r <= d).
+    Returns ``(out, lse)``."""
+    q, k, v, beta = (_f64(x) for x in (q, k, v, beta))
+    u = _f64(u)
+    lf = None if logf is None else _f64(logf)
+    *lead, T, d = q.shape
+    r = u.shape[-1]
+    BH = int(np.prod(lead)) if lead else 1
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    out = np.zeros((BH * T, d))
+    lse = np.zeros(BH * T)
+    rc = _load().path_oracle_partial_fwd(BH, T, d, r, _ptr(q), _ptr(k), _ptr(v),
+                                         _ptr(u) if r > 0 else None, _ptr(beta), _ptr(lf),
+                                         float(scale), _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise RuntimeError(f"path_oracle_partial_fwd failed with status {rc}")
+    return out.reshape(q.shape), lse.reshape(beta.shape)

@@ -234,3 +234,56 @@ int path_oracle_decode_step(int t, int d, double *kc, double *vc, double *lam,
   free(s);
   return 0;
 }
+
+/*
+ * Partial PaTH (the authors' proposal in the OpenReview discussion, sections
+ * "Efficiency" and "NoPE not included as a baseline": PaTH on a subset of the
+ * head dimensions, no position encoding on the rest).  Reading: the PaTH
+ * subspace is the first r coordinates.  With q = (qa, qb), k = (ka, kb),
+ * qa, ka in R^r, and G_t = I_r - beta_t u_t u_t^T (u_t in R^r):
+ *   log-weight_ij = scale * (ka_j^T G_{j+1} ... G_i qa_i + kb_j^T qb_i) + gate_ij.
+ * q, k, v: [BH, T, d]; u: [BH, T, r]; beta, logf: [BH, T]; 0 <= r <= d.
+ * out: [BH, T, d], lse: [BH, T].  Single-threaded; small problems only.
+ */
+int path_oracle_partial_fwd(int BH, int T, int d, int r, const double *q, const double *k,
+                            const double *v, const double *u, const double *beta,
+                            const double *logf, double scale, double *out, double *lse) {
+  if (BH < 1 || T < 1 || d < 1 || r < 0 || r > d || !q || !k || !v || (r > 0 && !u) ||
+      !beta || !out || !lse)
+    return -1;
+  double *s = (double *)malloc(sizeof(double) * (size_t)T);
+  double *z = (double *)malloc(sizeof(double) * (size_t)(r > 0 ? r : 1));
+  if (!s || !z) {
+    free(s);
+    free(z);
+    return -2;
+  }
+  for (int h = 0; h < BH; ++h) {
+    const double *qh = q + (size_t)h * T * d, *kh = k + (size_t)h * T * d;
+    const double *uh = r > 0 ? u + (size_t)h * T * r : NULL;
+    const double *bh = beta + (size_t)h * T, *fh = logf ? logf + (size_t)h * T : NULL;
+    for (int i = 0; i < T; ++i) {
+      for (int m = 0; m < r; ++m) z[m] = qh[(size_t)i * d + m];
+      double gate = 0.0;
+      for (int j = i; j >= 0; --j) {
+        /* here z = G_{j+1} ... G_i qa_i */
+        const double *kj = kh + (size_t)j * d;
+        double dot = 0.0;
+        for (int m = 0; m < r; ++m) dot += kj[m] * z[m];
+        for (int m = r; m < d; ++m) dot += kj[m] * qh[(size_t)i * d + m];
+        s[j] = scale * dot + gate;
+        const double *uj = r > 0 ? uh + (size_t)j * r : NULL;
+        double uz = 0.0;
+        for (int m = 0; m < r; ++m) uz += uj[m] * z[m];
+        const double c = bh[j] * uz;
+        for (int m = 0; m < r; ++m) z[m] -= c * uj[m];
+        if (fh) gate += fh[j];
+      }
+      path_row_readout(d, v + (size_t)h * T * d, i, s, out + ((size_t)h * T + i) * d,
+                       lse + (size_t)h * T + i);
+    }
+  }
+  free(s);
+  free(z);
+  return 0;
+}

@@ -20,7 +20,7 @@ import pytest
 import torch
 
 from oracle import (path_oracle_decode_step, path_oracle_decoded_keys, path_oracle_fwd,
-                    path_oracle_logits)
+                    path_oracle_logits, path_oracle_partial_fwd)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -413,3 +413,49 @@ def test_decoding_first_token_attends_to_itself():
                                    scale=0.3)
     np.testing.assert_array_equal(o, v[0])
     assert abs(l - 0.3 * (k[0] @ q[0])) < 1e-15
+
+
+# --------------------------------------------------------------- partial PaTH
+def test_partial_path_full_width_is_path_and_zero_width_is_plain_attention():
+    rng = np.random.default_rng(25)
+    T, d = 30, 8
+    q, k, v, w, b = _rand_inputs(rng, T, d)
+    logf = np.log(rng.uniform(0.7, 1.0, T))
+    o1, l1 = path_oracle_partial_fwd(q, k, v, w, b, logf=logf, scale=0.4)
+    o2, l2 = path_oracle_fwd(q, k, v, w, b, logf=logf, scale=0.4)
+    np.testing.assert_allclose(o1, o2, atol=1e-13, rtol=0)
+    np.testing.assert_allclose(l1, l2, atol=1e-13, rtol=0)
+    o0, l0 = path_oracle_partial_fwd(q, k, v, np.zeros((T, 0)), b, scale=0.4)
+    ref_out, ref_lse = _causal_softmax_attention(q, k, v, 0.4)
+    np.testing.assert_allclose(o0, ref_out, atol=1e-13, rtol=0)
+    np.testing.assert_allclose(l0, ref_lse, atol=1e-13, rtol=0)
+
+
+def test_partial_path_matches_block_diagonal_transitions():
+    """Brute force: H_t = blockdiag(I_r - beta u u^T, I_{d-r}) as explicit
+    matrices, and the same logits from full PaTH with u zero-padded to d."""
+    rng = np.random.default_rng(26)
+    T, d, r = 14, 7, 3
+    q, k, v, _, b = _rand_inputs(rng, T, d)
+    u = rng.standard_normal((T, r))
+    u /= np.linalg.norm(u, axis=1, keepdims=True)
+    scale = 0.6
+    out, lse = path_oracle_partial_fwd(q, k, v, u, b, scale=scale)
+    H = []
+    for t in range(T):
+        M = np.eye(d)
+        M[:r, :r] -= b[t] * np.outer(u[t], u[t])
+        H.append(M)
+    for i in range(T):
+        s = np.zeros(i + 1)
+        for j in range(i + 1):
+            P = np.eye(d)
+            for t in range(j + 1, i + 1):
+                P = P @ H[t]
+            s[j] = scale * (k[j] @ P @ q[i])
+        p = np.exp(s - s.max())
+        np.testing.assert_allclose(out[i], p @ v[: i + 1] / p.sum(), atol=1e-12)
+        assert abs(lse[i] - (s.max() + np.log(p.sum()))) < 1e-12
+    wpad = np.concatenate([u, np.zeros((T, d - r))], axis=1)
+    o2, _ = path_oracle_fwd(q, k, v, wpad, b, scale=scale)
+    np.testing.assert_allclose(out, o2, atol=1e-12)
