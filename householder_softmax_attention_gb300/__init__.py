@@ -22,7 +22,7 @@ import threading
 __all__ = [
     "PathAttnError", "load_library", "path_attn_fwd", "path_attn_fwd_host",
     "path_attn_fwd_noalloc", "path_attn_debug_wait_timeout", "path_attn_prefill",
-    "path_attn_decode_step", "DecodeCache",
+    "path_attn_decode_step", "DecodeCache", "path_attn_fwd_partial",
     "path_attn_debug_factors", "path_attn_device_status", "path_attn_workspace_bytes",
     "path_attn_chunk_size", "path_attn_launches_per_call", "path_attn_timing_enable",
     "path_attn_timing_read", "path_attn_version", "path_attn_status_string",
@@ -98,6 +98,9 @@ def load_library(path: str | None = None):
         lib.path_attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, fp, fp, f, vp, fp, vp,
                                               i, i, i, i, i, vp]
         lib.path_attn_fwd_noalloc.restype = i
+        lib.path_attn_fwd_partial.argtypes = [vp, vp, vp, vp, fp, fp, f, vp, fp, i, i, i, i, i,
+                                              i, vp]
+        lib.path_attn_fwd_partial.restype = i
         lib.path_attn_prefill.argtypes = [vp, vp, vp, vp, fp, fp, f, vp, fp, fp, vp, fp, i,
                                           i, i, i, i, i, vp]
         lib.path_attn_prefill.restype = i
@@ -224,6 +227,34 @@ def path_attn_fwd_noalloc(q, k, v, w, beta, logf=None, scale=None, out=None, lse
                                        float(scale), _ptr(out), _ptr(lse), _ptr(status),
                                        B, H, T, d, _dtype_code(q), ctypes.c_void_p(st.cuda_stream))
     _check(rc, "path_attn_fwd_noalloc")
+    return out, lse
+
+
+def path_attn_fwd_partial(q, k, v, u, beta, logf=None, scale=None, out=None, lse=None,
+                          want_lse=True, stream=None):
+    """Partial PaTH on CUDA tensors: PaTH with ``u [B, H, T, r]`` on the first
+    ``r`` head dimensions, no position encoding on the other ``d - r``.  Other
+    arguments as ``path_attn_fwd``."""
+    import torch
+    lib = load_library()
+    _check_inputs(q, k, v, q, beta, logf, True)
+    B, H, T, d = q.shape
+    if (u.dim() != 4 or u.shape[:3] != q.shape[:3] or u.dtype != q.dtype or not u.is_contiguous()
+            or u.device != q.device or u.shape[3] > d):
+        raise ValueError("u must be a contiguous [B, H, T, r] tensor like q, with r <= d")
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, T), device=q.device, dtype=torch.float32)
+    st = stream if stream is not None else torch.cuda.current_stream(q.device)
+    r = u.shape[3]
+    with torch.cuda.device(q.device):
+        rc = lib.path_attn_fwd_partial(_ptr(q), _ptr(k), _ptr(v), _ptr(u) if r > 0 else None,
+                                       _ptr(beta), _ptr(logf), float(scale), _ptr(out), _ptr(lse),
+                                       B, H, T, d, r, _dtype_code(q), ctypes.c_void_p(st.cuda_stream))
+    _check(rc, "path_attn_fwd_partial")
     return out, lse
 
 

@@ -216,6 +216,44 @@ int path_attn_fwd(const void* q, const void* k, const void* v, const void* w,
   return rc;
 }
 
+int path_attn_fwd_partial(const void* q, const void* k, const void* v, const void* w,
+                          const float* beta, const float* logf, float scale, void* out,
+                          float* lse, int B, int H, int T, int d, int r, int dtype, void* stream) {
+  if (!q || !k || !v || (r > 0 && !w) || !beta || !out) return PATH_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(beta) || !aligned16(out) ||
+      (logf && !aligned16(logf)) || (lse && !aligned16(lse)))
+    return PATH_ERR_INVALID_ARG;
+  if (!(scale == scale) || r < 0 || r > d) return PATH_ERR_INVALID_ARG;
+  Geom g;
+  int rc = make_geom(B, H, T, d, dtype, logf != nullptr, &g);
+  if (rc != PATH_OK) return rc;
+  DeviceState* s = nullptr;
+  if ((rc = device_state(&s)) != PATH_OK) return rc;
+  if ((rc = check_device(s)) != PATH_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t es = g.bf16 ? 2 : 4;
+  const size_t rows = static_cast<size_t>(g.BH) * T;
+  const size_t wbytes = align_up(rows * d * es, 256);
+  const size_t bytes = wbytes + workspace_layout(g, nullptr, nullptr);
+  char* buf = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&buf), bytes, s->pool, st);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  // u widened with zeros: H_t is then the identity outside the first r dims
+  if (r < d) e = cudaMemsetAsync(buf, 0, rows * d * es, st);
+  if (e == cudaSuccess && r > 0)
+    e = cudaMemcpy2DAsync(buf, d * es, w, static_cast<size_t>(r) * es, static_cast<size_t>(r) * es,
+                          rows, cudaMemcpyDeviceToDevice, st);
+  if (e != cudaSuccess) {
+    rc = set_cuda_error(e);
+  } else {
+    Inputs in{q, k, v, buf, beta, logf, scale, out, lse};
+    rc = run_forward(g, in, buf + wbytes, s, st);
+  }
+  e = cudaFreeAsync(buf, st);
+  if (rc == PATH_OK && e != cudaSuccess) rc = set_cuda_error(e);
+  return rc;
+}
+
 int path_attn_fwd_host(const void* q, const void* k, const void* v, const void* w,
                        const float* beta, const float* logf, float scale, void* out,
                        float* lse, int B, int H, int T, int d, int dtype, void* stream) {
@@ -335,13 +373,18 @@ int path_attn_decode_step(const void* q, const void* k, const void* v, const voi
   const long long per = (tiles + nsplit - 1) / nsplit;
   nsplit = (tiles + per - 1) / per;
   float* part = nullptr;
-  const size_t part_bytes = static_cast<size_t>(BH) * nsplit * (d + 2) * sizeof(float);
-  cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&part), part_bytes, s->pool, st);
+  const size_t part_bytes =
+      align_up(static_cast<size_t>(BH) * nsplit * (d + 2) * sizeof(float), 256);
+  const size_t cnt_bytes = static_cast<size_t>(BH) * sizeof(int);
+  cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&part), part_bytes + cnt_bytes,
+                                          s->pool, st);
   if (e != cudaSuccess) return set_cuda_error(e);
+  int* counters = reinterpret_cast<int*>(reinterpret_cast<char*>(part) + part_bytes);
   DecodeParams p{q, k, v, w, beta, logf, scale, kcache, vcache, lamcache, pos, H, Tmax, max_len,
-                 static_cast<int>(nsplit), static_cast<int>(per * tile), part, out, lse,
+                 static_cast<int>(nsplit), static_cast<int>(per * tile), part, counters, out, lse,
                  s->status};
-  if ((e = launch_decode(p, static_cast<int>(BH), d, dtype == PATH_DTYPE_BF16, st)) != cudaSuccess)
+  if ((e = cudaMemsetAsync(counters, 0, cnt_bytes, st)) != cudaSuccess ||
+      (e = launch_decode(p, static_cast<int>(BH), d, dtype == PATH_DTYPE_BF16, st)) != cudaSuccess)
     rc = set_cuda_error(e);
   e = cudaFreeAsync(part, st);
   if (rc == PATH_OK && e != cudaSuccess) rc = set_cuda_error(e);

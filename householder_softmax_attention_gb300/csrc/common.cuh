@@ -117,6 +117,7 @@ cudaError_t launch_attn_tc(const Geom& g, const Inputs& in, const Workspace& ws,
 //   kcache [bh][Tmax][d] f32; vcache [bh][Tmax][d] elem; lamcache [bh][Tmax] f32
 //   pos [B] int32: position of the new token of each batch row
 //   part [bh][nsplit][d + 2] f32 scratch: (max, sum, o) of each key span
+// One launch; the last CTA of each head to finish merges its spans.
 struct DecodeParams {
   const void *q, *k, *v, *w;
   const float *beta, *logf;
@@ -128,13 +129,14 @@ struct DecodeParams {
   int H, Tmax, max_len;
   int nsplit, span;  // spans of `span` cached keys (a multiple of the tile)
   float* part;
+  int* counters;  // [bh], zero before the launch: CTAs of the head that have finished
   void* out;
   float* lse;
   int* status;
 };
 // Key rows per pipeline stage of the decoding kernel (spans are multiples).
 int decode_tile_keys(int d);
-// Two launches: the span kernel, then the per-head merge + append.
+// One launch of the span kernel (counters must be zero).
 cudaError_t launch_decode(const DecodeParams& p, int BH, int d, bool bf16, cudaStream_t st);
 // Prefill: kcache rows j < T of each head <- key j carried to token T - 1,
 // from the chunk factors kr and ngt of a prepared workspace.

@@ -16,18 +16,20 @@
 //                       complete on mbarriers.  Each key row is refined in
 //                       shared memory, written back with a bulk store, and its
 //                       logit (k_j . q - beta (w . k_j)(w . q)) feeds an online
-//                       softmax.  The CTA leaves (max, sum, o) of its span in a
-//                       partial buffer.
-// decode_combine_kernel merges the spans of a head with the new token's own
-//                       term, writes out and lse, and appends k_t, v_t and
-//                       lam_t to the cache.
+//                       softmax.  Each CTA leaves (max, sum, o) of its span in
+//                       a partial buffer.
+//                       The CTA that finishes last for a head (an atomic
+//                       ticket per head) merges the head's spans with the new
+//                       token's own term, writes out and lse, and appends
+//                       k_t, v_t and lam_t to the cache.
 // align_keys_kernel     after a prefill of T tokens the cache must hold every
 //                       key carried to the prompt end, H_{T-1} .. H_{j+1} k_j.
 //                       From the forward's chunk factors (kr_c: keys carried to
 //                       the end of their chunk; F_c = H_first .. H_last =
 //                       I + ngt_c) that is the row block kr_c G_c with
 //                       G_c = F_{c+1} .. F_{last}, built from the last chunk
-//                       backwards; each CTA owns 32 columns of G.
+//                       backwards; each CTA owns 32 columns of G (fp32 SIMT
+//                       for fp32 inputs, mma.sync for bf16).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -71,6 +73,64 @@ __device__ __forceinline__ float group_sum(float x) {
 #pragma unroll
   for (int off = G / 2; off >= 1; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
   return x;
+}
+
+// ------------------------------------------------------------ decode: merge
+// Run by the whole CTA that finished last for head bh: merges the spans'
+// (max, sum, o) with the new token's own term (its gate is 0), writes out and
+// lse, and appends k_t, v_t and lam_t.  scratch holds D / 32 floats.
+template <typename ET, int D>
+__device__ __forceinline__ void merge_head(const DecodeParams& p, int bh, int t, bool pos_ok,
+                                           float* scratch) {
+  const int e = threadIdx.x;
+  ET* out = static_cast<ET*>(p.out) + static_cast<size_t>(bh) * D;
+  if (!pos_ok) {
+    if (e == 0) {
+      atomicExch(p.status, PATH_DEV_ERR_BAD_POS);
+      if (p.lse) p.lse[bh] = NAN;
+    }
+    if (e < D) out[e] = from_f<ET>(NAN);
+    return;
+  }
+  const size_t row = static_cast<size_t>(bh) * D + (e < D ? e : 0);
+  const ET ke = static_cast<const ET*>(p.k)[row], ve = static_cast<const ET*>(p.v)[row];
+  const float kf = to_f(ke), vf = to_f(ve), qf = to_f(static_cast<const ET*>(p.q)[row]);
+  float qk = e < D ? qf * kf : 0.f;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) qk += __shfl_xor_sync(0xffffffffu, qk, off);
+  if ((e & 31) == 0 && e < D) scratch[e >> 5] = qk;
+  __syncthreads();
+  if (e >= D) return;
+  qk = 0.f;
+#pragma unroll
+  for (int w2 = 0; w2 < D / 32; ++w2) qk += scratch[w2];
+  const float st = qk * (p.scale * kLog2e);
+  // partials of other CTAs: read through L2
+  const float* pp = p.part + static_cast<size_t>(bh) * p.nsplit * (D + 2);
+  float M = st;
+  bool bad = false;
+  for (int s2 = 0; s2 < p.nsplit; ++s2) {
+    const float ms = __ldcg(pp + s2 * (D + 2));
+    bad |= ms != ms;
+    M = fmaxf(M, ms);
+  }
+  float Lsum = ex2_approx(st - M);
+  float O = Lsum * vf;
+  for (int s2 = 0; s2 < p.nsplit; ++s2) {
+    const float ms = __ldcg(pp + s2 * (D + 2));
+    const float a = ms == -INFINITY ? 0.f : ex2_approx(ms - M);
+    Lsum = fmaf(__ldcg(pp + s2 * (D + 2) + 1), a, Lsum);
+    O = fmaf(__ldcg(pp + s2 * (D + 2) + 2 + e), a, O);
+  }
+  out[e] = from_f<ET>(bad ? NAN : O / Lsum);
+  if (e == 0 && p.lse) p.lse[bh] = bad ? NAN : (M + log2f(Lsum)) * kLn2;
+  const size_t crow = (static_cast<size_t>(bh) * p.Tmax + t) * D + e;
+  p.kcache[crow] = kf;
+  static_cast<ET*>(p.vcache)[crow] = ve;
+  if (e == 0 && p.lamcache) {
+    float* lamc = p.lamcache + static_cast<size_t>(bh) * p.Tmax;
+    lamc[t] = (t > 0 ? lamc[t - 1] : 0.f) + p.logf[bh];
+  }
 }
 
 // ------------------------------------------------------------ decode: split
@@ -275,61 +335,15 @@ __global__ void __launch_bounds__(256, 2) decode_split_kernel(const DecodeParams
       pp[1] = Lsum;
     }
   }
-}
-
-// ---------------------------------------------------------- decode: combine
-template <typename ET, int D>
-__global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeParams p) {
-  __shared__ float wsum[D / 32];
-  const int bh = blockIdx.x, e = threadIdx.x;
-  const int t = p.pos[bh / p.H];
-  ET* out = static_cast<ET*>(p.out) + static_cast<size_t>(bh) * D;
-  if (t < 0 || t >= p.max_len) {
-    if (e == 0) {
-      atomicExch(p.status, PATH_DEV_ERR_BAD_POS);
-      if (p.lse) p.lse[bh] = NAN;
-    }
-    out[e] = from_f<ET>(NAN);
-    return;
-  }
-  const size_t row = static_cast<size_t>(bh) * D + e;
-  const ET ke = static_cast<const ET*>(p.k)[row], ve = static_cast<const ET*>(p.v)[row];
-  const float kf = to_f(ke), vf = to_f(ve), qf = to_f(static_cast<const ET*>(p.q)[row]);
-  float qk = qf * kf;
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) qk += __shfl_xor_sync(0xffffffffu, qk, off);
-  if ((e & 31) == 0) wsum[e >> 5] = qk;
+  // the CTA that finishes last for this head merges all of its spans
+  __shared__ int s_last;
+  __threadfence();
   __syncthreads();
-  qk = 0.f;
-#pragma unroll
-  for (int w2 = 0; w2 < D / 32; ++w2) qk += wsum[w2];
-  const float st = qk * (p.scale * kLog2e);  // the new key's own gate is 0
-  const float* pp = p.part + static_cast<size_t>(bh) * p.nsplit * (D + 2);
-  float M = st;
-  bool bad = false;
-  for (int s = 0; s < p.nsplit; ++s) {
-    const float ms = pp[s * (D + 2)];
-    bad |= ms != ms;
-    M = fmaxf(M, ms);
-  }
-  float Lsum = ex2_approx(st - M);
-  float O = Lsum * vf;
-  for (int s = 0; s < p.nsplit; ++s) {
-    const float ms = pp[s * (D + 2)];
-    const float a = ms == -INFINITY ? 0.f : ex2_approx(ms - M);
-    Lsum = fmaf(pp[s * (D + 2) + 1], a, Lsum);
-    O = fmaf(pp[s * (D + 2) + 2 + e], a, O);
-  }
-  out[e] = from_f<ET>(bad ? NAN : O / Lsum);
-  if (e == 0 && p.lse) p.lse[bh] = bad ? NAN : (M + log2f(Lsum)) * kLn2;
-  // append the new token
-  const size_t crow = (static_cast<size_t>(bh) * p.Tmax + t) * D + e;
-  p.kcache[crow] = kf;
-  static_cast<ET*>(p.vcache)[crow] = ve;
-  if (e == 0 && p.lamcache) {
-    float* lamc = p.lamcache + static_cast<size_t>(bh) * p.Tmax;
-    lamc[t] = (t > 0 ? lamc[t - 1] : 0.f) + p.logf[bh];
-  }
+  if (tid == 0) s_last = atomicAdd(p.counters + bh, 1) == p.nsplit - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  merge_head<ET, D>(p, bh, t, pos_ok, red);
 }
 
 // ------------------------------------------------------- prefill: align keys
@@ -441,16 +455,225 @@ __global__ void __launch_bounds__(256, 1)
   }
 }
 
+// bf16 inputs: the same product on the tensor cores (mma.sync, bf16
+// operands, fp32 accumulation), transposed so that the carried quantity is
+// the operand A of both products: with X = (G[:, cols])^T (32 x D),
+//   keys^T  = X kr_c^T            (phase B, X split into bf16 hi + lo)
+//   X_next  = X + X ngt_c^T       (phase A, fp32 master in the accumulators)
+// Each warp owns 16 keys of phase B and D / 8 / 8 column tiles of phase A;
+// kr_c and ngt_c stream through two cp.async stages.
+template <int D>
+struct AlignTcCfg {
+  static constexpr int kC = 128, kNB = 32, kThreads = 256;
+  static constexpr int kLd = D + 8;  // bf16 row stride of the staged tiles (conflict-free)
+  static constexpr int kKrBytes = kC * kLd * 2;
+  static constexpr int kMBytes = D * kLd * 2;
+  static constexpr int kStageBytes = kKrBytes + kMBytes;
+  static constexpr int kXBytes = kNB * kLd * 2;
+  static constexpr int kXOff = 2 * kStageBytes;  // X: [buffer][hi, lo]
+  static constexpr int kOLd = 36;                // fp32 row stride of the output tile
+  static constexpr int kOOff = kXOff + 4 * kXBytes;
+  static constexpr int kSmem = kOOff + kC * kOLd * 4;
+  static constexpr int kNA = D / 64;             // phase-A column tiles per warp
+};
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// A fragment (16 x 16) of a row-major bf16 shared tile s[row][k], stride S.
+__device__ __forceinline__ void frag_a(uint32_t (&a)[4], const __nv_bfloat16* s, int S, int m0,
+                                       int k0, int g, int t) {
+  a[0] = *reinterpret_cast<const uint32_t*>(s + (m0 + g) * S + k0 + 2 * t);
+  a[1] = *reinterpret_cast<const uint32_t*>(s + (m0 + g + 8) * S + k0 + 2 * t);
+  a[2] = *reinterpret_cast<const uint32_t*>(s + (m0 + g) * S + k0 + 2 * t + 8);
+  a[3] = *reinterpret_cast<const uint32_t*>(s + (m0 + g + 8) * S + k0 + 2 * t + 8);
+}
+
+template <int D>
+__global__ void __launch_bounds__(256, 1)
+    align_keys_tc_kernel(const __nv_bfloat16* kr, const __nv_bfloat16* ngt, float* kcache, int T,
+                         int Np, int Tp, int Tmax) {
+  using Cfg = AlignTcCfg<D>;
+  constexpr int C = Cfg::kC, LD = Cfg::kLd, NA = Cfg::kNA, OLD = Cfg::kOLd;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t4 = lane & 3;
+  const int cb = blockIdx.x, bh = blockIdx.y, col0 = cb * Cfg::kNB;
+  const __nv_bfloat16* krh = kr + static_cast<size_t>(bh) * Tp * D;
+  const __nv_bfloat16* ngh = ngt + static_cast<size_t>(bh) * Np * D * D;
+  float* kch = kcache + static_cast<size_t>(bh) * Tmax * D;
+  float* so = reinterpret_cast<float*>(smem + Cfg::kOOff);
+  auto xbuf = [&](int buf, int lo) {
+    return reinterpret_cast<__nv_bfloat16*>(smem + Cfg::kXOff + (2 * buf + lo) * Cfg::kXBytes);
+  };
+  auto issue = [&](int c, int stage) {
+    __nv_bfloat16* skr = reinterpret_cast<__nv_bfloat16*>(smem + stage * Cfg::kStageBytes);
+    __nv_bfloat16* sm = reinterpret_cast<__nv_bfloat16*>(smem + stage * Cfg::kStageBytes +
+                                                         Cfg::kKrBytes);
+    const __nv_bfloat16* gkr = krh + static_cast<size_t>(c) * C * D;
+    const __nv_bfloat16* gm = ngh + static_cast<size_t>(c) * D * D;
+    constexpr int P = D / 8;  // 16-byte pieces per row
+    for (int x = tid; x < C * P; x += Cfg::kThreads)
+      cp_async16(skr + (x / P) * LD + (x % P) * 8, gkr + (x / P) * D + (x % P) * 8);
+    for (int x = tid; x < D * P; x += Cfg::kThreads)
+      cp_async16(sm + (x / P) * LD + (x % P) * 8, gm + (x / P) * D + (x % P) * 8);
+    cp_async_commit();
+  };
+  issue(Np - 1, 0);
+  // X = (identity columns col0 .. col0 + 31)^T
+  for (int x = tid; x < Cfg::kNB * D; x += Cfg::kThreads) {
+    const int n = x / D, k = x % D;
+    xbuf(0, 0)[n * LD + k] = __float2bfloat16_rn(k == col0 + n ? 1.f : 0.f);
+    xbuf(0, 1)[n * LD + k] = __float2bfloat16_rn(0.f);
+  }
+  float xm[2][NA][4];  // fp32 master of this warp's phase-A tiles of X
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int j = 0; j < NA; ++j)
+#pragma unroll
+      for (int f = 0; f < 4; ++f) {
+        const int n = mt * 16 + g + (f >= 2 ? 8 : 0);
+        const int k = (warp * NA + j) * 8 + 2 * t4 + (f & 1);
+        xm[mt][j][f] = k == col0 + n ? 1.f : 0.f;
+      }
+  for (int it = 0; it < Np; ++it) {
+    const int c = Np - 1 - it, stage = it & 1;
+    cp_async_wait_all();
+    __syncthreads();  // stage `stage`, X buffer it & 1 and the drained output tile are ready
+    if (c > 0) issue(c - 1, stage ^ 1);
+    const __nv_bfloat16* skr =
+        reinterpret_cast<const __nv_bfloat16*>(smem + stage * Cfg::kStageBytes);
+    const __nv_bfloat16* sm =
+        reinterpret_cast<const __nv_bfloat16*>(smem + stage * Cfg::kStageBytes + Cfg::kKrBytes);
+    const __nv_bfloat16* xh = xbuf(it & 1, 0);
+    const __nv_bfloat16* xl = xbuf(it & 1, 1);
+    float ob[2][2][4];
+    float xa[2][NA][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int f = 0; f < 4; ++f) ob[mt][j][f] = 0.f;
+#pragma unroll
+      for (int j = 0; j < NA; ++j)
+#pragma unroll
+        for (int f = 0; f < 4; ++f) xa[mt][j][f] = xm[mt][j][f];
+    }
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      uint32_t ah[2][4], al[2][4];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        frag_a(ah[mt], xh, LD, mt * 16, ks * 16, g, t4);
+        frag_a(al[mt], xl, LD, mt * 16, ks * 16, g, t4);
+      }
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {  // phase B: keys warp * 16 + 8 j ..
+        const __nv_bfloat16* row = skr + (warp * 16 + 8 * j + g) * LD + ks * 16 + 2 * t4;
+        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(row);
+        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(row + 8);
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          mma16816(ob[mt][j], ah[mt], b0, b1);
+          mma16816(ob[mt][j], al[mt], b0, b1);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < NA; ++j) {  // phase A: columns (warp * NA + j) * 8 ..
+        const __nv_bfloat16* row = sm + ((warp * NA + j) * 8 + g) * LD + ks * 16 + 2 * t4;
+        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(row);
+        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(row + 8);
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) mma16816(xa[mt][j], ah[mt], b0, b1);
+      }
+    }
+    // keys of chunk c: so[key][n] = (X kr_c^T)[n][key]
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int key = warp * 16 + 8 * j + 2 * t4, n = mt * 16 + g;
+        so[key * OLD + n] = ob[mt][j][0];
+        so[(key + 1) * OLD + n] = ob[mt][j][1];
+        so[key * OLD + n + 8] = ob[mt][j][2];
+        so[(key + 1) * OLD + n + 8] = ob[mt][j][3];
+      }
+    // the carried product crosses chunk c
+    __nv_bfloat16* nh = xbuf((it + 1) & 1, 0);
+    __nv_bfloat16* nl = xbuf((it + 1) & 1, 1);
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int j = 0; j < NA; ++j)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float x0 = xa[mt][j][2 * h], x1 = xa[mt][j][2 * h + 1];
+          xm[mt][j][2 * h] = x0;
+          xm[mt][j][2 * h + 1] = x1;
+          const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
+          const int n = mt * 16 + g + 8 * h, k = (warp * NA + j) * 8 + 2 * t4;
+          *reinterpret_cast<__nv_bfloat162*>(nh + n * LD + k) = __halves2bfloat162(h0, h1);
+          *reinterpret_cast<__nv_bfloat162*>(nl + n * LD + k) = __halves2bfloat162(
+              __float2bfloat16_rn(x0 - __bfloat162float(h0)),
+              __float2bfloat16_rn(x1 - __bfloat162float(h1)));
+        }
+    __syncthreads();
+    for (int x = tid; x < C * 8; x += Cfg::kThreads) {
+      const int r = x >> 3, q = x & 7, j = c * C + r;
+      if (j < T)
+        *reinterpret_cast<float4*>(kch + static_cast<size_t>(j) * D + col0 + 4 * q) =
+            *reinterpret_cast<const float4*>(so + r * OLD + 4 * q);
+    }
+  }
+}
+
+template <int D>
+cudaError_t launch_align_tc(const Geom& g, const Workspace& ws, float* kcache, int Tmax,
+                            cudaStream_t st) {
+  using Cfg = AlignTcCfg<D>;
+  auto kern = align_keys_tc_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Cfg::kSmem);
+  if (e != cudaSuccess) return e;
+  kern<<<dim3(D / Cfg::kNB, g.BH), Cfg::kThreads, Cfg::kSmem, st>>>(
+      static_cast<const __nv_bfloat16*>(ws.kr), static_cast<const __nv_bfloat16*>(ws.ngt), kcache,
+      g.T, g.Np, g.Tp, Tmax);
+  return cudaGetLastError();
+}
+
 template <typename ET, int D>
 cudaError_t launch_decode_t(const DecodeParams& p, int BH, cudaStream_t st) {
   using Cfg = DecCfg<ET, D>;
   auto kern = decode_split_kernel<ET, D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Cfg::kSmem);
+  static bool attr_set[64] = {};  // once per device (setting it again is harmless)
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  Cfg::kSmem)) != cudaSuccess)
+      return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
   kern<<<dim3(p.nsplit, BH), Cfg::kThreads, Cfg::kSmem, st>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  decode_combine_kernel<ET, D><<<BH, D, 0, st>>>(p);
   return cudaGetLastError();
 }
 
@@ -482,8 +705,8 @@ cudaError_t launch_decode(const DecodeParams& p, int BH, int d, bool bf16, cudaS
 cudaError_t launch_align_keys(const Geom& g, const Workspace& ws, float* kcache, int Tmax,
                               cudaStream_t st) {
   if (g.bf16)
-    return g.d == 128 ? launch_align_t<__nv_bfloat16, 128, 128>(g, ws, kcache, Tmax, st)
-                      : launch_align_t<__nv_bfloat16, 64, 128>(g, ws, kcache, Tmax, st);
+    return g.d == 128 ? launch_align_tc<128>(g, ws, kcache, Tmax, st)
+                      : launch_align_tc<64>(g, ws, kcache, Tmax, st);
   return g.d == 128 ? launch_align_t<float, 128, 64>(g, ws, kcache, Tmax, st)
                     : launch_align_t<float, 64, 64>(g, ws, kcache, Tmax, st);
 }

@@ -88,6 +88,24 @@ int path_attn_fwd_host(const void* q, const void* k, const void* v, const void* 
                        float* lse, int B, int H, int T, int d, int dtype, void* stream);
 
 /*
+ * path_attn_fwd_partial -- partial PaTH: PaTH on the first r of the d head
+ * dimensions, no position encoding on the other d - r (the authors' proposal
+ * in the OpenReview discussion, sections "Efficiency" and "NoPE not included
+ * as a baseline"; the choice of the first r coordinates is this library's):
+ *   s_ij = scale * (ka_j^T G_{j+1} ... G_i qa_i + kb_j^T qb_i) [+ gate],
+ *   G_t = I_r - beta_t u_t u_t^T,  q = (qa, qb), k = (ka, kb), qa, ka in R^r.
+ * Arguments as path_attn_fwd except w, which is u: device, [B,H,T,r], dtype,
+ * any alignment (NULL allowed when r == 0), and 0 <= r <= d.  Since a
+ * transition that is the identity outside the first r coordinates gives
+ * exactly these logits, the call widens u with zeros to [B,H,T,d] in a
+ * stream-ordered buffer (two copy operations) and runs the PaTH kernels; it
+ * costs what path_attn_fwd costs plus that copy.
+ */
+int path_attn_fwd_partial(const void* q, const void* k, const void* v, const void* w,
+                          const float* beta, const float* logf, float scale, void* out,
+                          float* lse, int B, int H, int T, int d, int r, int dtype, void* stream);
+
+/*
  * Decoding with keys rewritten in place (slides' frame "Decoding updates
  * historical keys in place").  A decoder keeps, per (b, h), a key cache in
  * which row j < t holds k_j carried to the latest token t - 1,
@@ -133,8 +151,9 @@ int path_attn_prefill(const void* q, const void* k, const void* v, const void* w
  *               covering rows [0, max_len - 1).
  *   out         device, [B,H,d], dtype;  lse: device, [B,H], fp32, or NULL
  *
- * Two kernel launches on `stream` and a small stream-ordered scratch
- * ([B*H][spans][d+2] fp32) from the library's pool.  A pos[b] outside
+ * One kernel launch on `stream` (after a memset of B*H ints) and a small
+ * stream-ordered scratch ([B*H][spans][d+2] fp32 + B*H ints) from the
+ * library's pool; the last CTA of each head merges that head's spans.  A pos[b] outside
  * [0, max_len) is only visible on the device: that batch row's out and lse
  * become NaN, its cache rows are left as they were, and
  * path_attn_device_status() then returns PATH_ERR_INVALID_ARG.

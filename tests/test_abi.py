@@ -120,3 +120,13 @@ def test_decode_and_prefill_validate_before_any_cuda_call(lib):
     assert pre(Tmax=15) == INVALID                          # cache shorter than the prompt
     assert pre(logf=logf) == INVALID
     assert pre(T=0) == INVALID
+
+
+def test_partial_validates_before_any_cuda_call(lib):
+    q, k, v, w, beta, out = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(6)]
+    part = lambda r, w=w, d=64: lib.path_attn_fwd_partial(q, k, v, w, beta, None, 0.1, out, None,
+                                                         1, 1, 8, d, r, 1, None)
+    assert part(65) == INVALID          # r above d
+    assert part(-1) == INVALID
+    assert part(8, w=None) == INVALID   # u needed when r > 0
+    assert part(0, d=96) == UNSUPPORTED
