@@ -405,6 +405,148 @@ def run_decode_reference(args, wl):
     return 0
 
 
+# ------------------------------------------------------------------ producer
+def producer_bytes(wl):
+    """Algorithmic HBM bytes of one producer step: x read, w and beta written,
+    the weights read once."""
+    es = 2 if wl.dtype == "bf16" else 4
+    BT = wl.B * wl.T
+    return (BT * wl.Dm * es + BT * wl.H * wl.d * es + BT * wl.H * 4
+            + ((wl.R + wl.H) * wl.Dm + wl.H * wl.d * wl.R) * es + wl.H * wl.d * 12 + wl.H * 4)
+
+
+def oracle_producer_sample(wl, budget_s):
+    """Seconds per token of the fp64 producer oracle, timed on windows of
+    consecutive tokens of the workload; returns (seconds per token, text)."""
+    import numpy as np
+
+    from oracle.producer import producer_fwd
+    from seeded_inputs import make_producer_inputs
+
+    x = make_producer_inputs(wl)
+    W = [x[n].double().numpy() for n in ("Wd", "Wu", "cw", "Ub", "bb")]
+    xs = x["x"].double().numpy()
+    n, spent, t = 0, 0.0, 0
+    while spent < budget_s or n == 0:
+        win = xs[:1, t:t + 256]
+        t0 = time.perf_counter()
+        producer_fwd(win, *W, wl.H, wl.d)
+        spent += time.perf_counter() - t0
+        n += win.shape[1]
+        t = (t + 256) % max(1, wl.T - 256)
+    return spent / n, f"{n} tokens of {wl.name} in 256-token windows, {spent:.1f} s; per token"
+
+
+def run_producer(args, wl):
+    import torch
+
+    import householder_softmax_attention_gb300 as pa
+    from seeded_inputs import make_producer_inputs
+
+    rank, world, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pa.load_library()
+    x = make_producer_inputs(wl, device=dev)
+    w = torch.empty((wl.B, wl.H, wl.T, wl.d), device=dev, dtype=x["x"].dtype)
+    beta = torch.empty((wl.B, wl.H, wl.T), device=dev, dtype=torch.float32)
+    st = torch.cuda.current_stream(dev)
+    args_ = [x[n] for n in ("x", "Wd", "Wu", "cw", "Ub", "bb")]
+
+    def step():
+        pa.path_producer_fwd(*args_, wl.H, wl.d, w=w, beta=beta, stream=st)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        e0.record(st)
+        for _ in range(args.steps):
+            step()
+        e1.record(st)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    ms = reduce_max(e0.elapsed_time(e1) / args.steps, world)
+    nbytes = producer_bytes(wl)
+    _, hbm, peak_src = _peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+
+    hx = x["x"].cpu().pin_memory()
+    dx = torch.empty_like(x["x"])
+    hw = torch.empty(w.shape, dtype=w.dtype).pin_memory()
+    hb = torch.empty(beta.shape, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        dx.copy_(hx, non_blocking=True)
+        pa.path_producer_fwd(dx, *args_[1:], wl.H, wl.d, w=w, beta=beta, stream=st)
+        hw.copy_(w, non_blocking=True)
+        hb.copy_(beta, non_blocking=True)
+        st.synchronize()
+
+    for _ in range(2):
+        e2e_step()
+    n_e2e = max(1, min(args.steps, 10))
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        e2e_step()
+    e2e_ms = reduce_max((time.perf_counter() - t0) * 1e3 / n_e2e, world)
+    line = {
+        "metric": f"PaTH w/beta producer GB/s, {wl.name}", "value": world * gbs, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "Dm": wl.Dm, "H": wl.H, "d": wl.d,
+                   "R": wl.R, "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2: {nbytes / 2**20:.0f} MiB moved per step"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": gbs / hbm, "traffic": args.traffic,
+                     "kernel": "producer_proj + producer_mix (the whole step)",
+                     "peak_source": f"{peak_src} copy bandwidth", "avg_launch_ms": ms,
+                     "algorithmic_bytes": nbytes},
+        "e2e": {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": hx.numel() * hx.element_size(),
+                "d2h_bytes_per_step": hw.numel() * hw.element_size() + hb.numel() * 4},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        sec, desc = oracle_producer_sample(wl, min(args.cpu_budget_s, 10.0))
+        est = sec * wl.B * wl.T
+        line["cpu_baseline"] = {"value": nbytes / est / 1e9, "unit": "GB/s", "cores": 1,
+                                "kind": "oracle", "sample": desc, "est_full_step_s": est}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_producer_reference(args, wl):
+    rank, world, _ = dist_setup()
+    if rank != 0:
+        return 0
+    per_step = []
+    for s in range(args.warmup + args.steps):
+        sec, desc = oracle_producer_sample(wl, min(args.ref_step_s, 2.0))
+        if s >= args.warmup:
+            per_step.append(sec * wl.B * wl.T)
+    est = statistics.median(per_step)
+    value = producer_bytes(wl) / est / 1e9
+    print(json.dumps({
+        "impl": "reference", "metric": f"PaTH w/beta producer GB/s, {wl.name}", "value": value,
+        "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": est * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "Dm": wl.Dm, "H": wl.H, "d": wl.d,
+                   "R": wl.R},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+    return 0
+
+
 # ------------------------------------------------------------------ arms
 def run_reference(args, wl, flops):
     rank, world, _ = dist_setup()
@@ -558,7 +700,10 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
-    from seeded_inputs import DECODE_WORKLOADS, WORKLOADS
+    from seeded_inputs import DECODE_WORKLOADS, PRODUCER_WORKLOADS, WORKLOADS
+    if args.workload in PRODUCER_WORKLOADS:
+        wl = PRODUCER_WORKLOADS[args.workload]
+        return run_producer_reference(args, wl) if args.impl == "reference" else run_producer(args, wl)
     if args.workload in DECODE_WORKLOADS:
         wl = DECODE_WORKLOADS[args.workload]
         if args.B or args.H:

@@ -22,7 +22,7 @@ import threading
 __all__ = [
     "PathAttnError", "load_library", "path_attn_fwd", "path_attn_fwd_host",
     "path_attn_fwd_noalloc", "path_attn_debug_wait_timeout", "path_attn_prefill",
-    "path_attn_decode_step", "DecodeCache", "path_attn_fwd_partial",
+    "path_attn_decode_step", "DecodeCache", "path_attn_fwd_partial", "path_producer_fwd",
     "path_attn_debug_factors", "path_attn_device_status", "path_attn_workspace_bytes",
     "path_attn_chunk_size", "path_attn_launches_per_call", "path_attn_timing_enable",
     "path_attn_timing_read", "path_attn_version", "path_attn_status_string",
@@ -101,6 +101,9 @@ def load_library(path: str | None = None):
         lib.path_attn_fwd_partial.argtypes = [vp, vp, vp, vp, fp, fp, f, vp, fp, i, i, i, i, i,
                                               i, vp]
         lib.path_attn_fwd_partial.restype = i
+        lib.path_producer_fwd.argtypes = [vp, vp, vp, fp, vp, fp, vp, fp, i, i, i, i, i, i, i,
+                                          vp]
+        lib.path_producer_fwd.restype = i
         lib.path_attn_prefill.argtypes = [vp, vp, vp, vp, fp, fp, f, vp, fp, fp, vp, fp, i,
                                           i, i, i, i, i, vp]
         lib.path_attn_prefill.restype = i
@@ -256,6 +259,37 @@ def path_attn_fwd_partial(q, k, v, u, beta, logf=None, scale=None, out=None, lse
                                        B, H, T, d, r, _dtype_code(q), ctypes.c_void_p(st.cuda_stream))
     _check(rc, "path_attn_fwd_partial")
     return out, lse
+
+
+def path_producer_fwd(x, Wd, Wu, cw, Ub, bb, H, d, w=None, beta=None, stream=None):
+    """w and beta from hidden states ``x [B, T, Dm]`` (bfloat16 or float32):
+    low-rank projection ``Wd [R, Dm]``, ``Wu [H*d, R]``, causal width-3
+    convolution ``cw [H*d, 3]`` (float32), per-head L2 normalization, and
+    ``beta = 2 sigmoid(x Ub^T + bb)`` with ``Ub [H, Dm]``, ``bb [H]`` (float32).
+    Returns ``(w [B, H, T, d], beta [B, H, T])``."""
+    import torch
+    lib = load_library()
+    if x.dim() != 3 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA [B, T, Dm] tensor")
+    B, T, Dm = x.shape
+    R = Wd.shape[0]
+    shapes = {"Wd": (Wd, (R, Dm), x.dtype), "Wu": (Wu, (H * d, R), x.dtype),
+              "cw": (cw, (H * d, 3), torch.float32), "Ub": (Ub, (H, Dm), x.dtype),
+              "bb": (bb, (H,), torch.float32)}
+    for name, (t, shp, dt) in shapes.items():
+        if tuple(t.shape) != shp or t.dtype != dt or not t.is_contiguous() or t.device != x.device:
+            raise ValueError(f"{name} must be a contiguous {dt} tensor of shape {shp} on x's device")
+    if w is None:
+        w = torch.empty((B, H, T, d), device=x.device, dtype=x.dtype)
+    if beta is None:
+        beta = torch.empty((B, H, T), device=x.device, dtype=torch.float32)
+    st = stream if stream is not None else torch.cuda.current_stream(x.device)
+    with torch.cuda.device(x.device):
+        rc = lib.path_producer_fwd(_ptr(x), _ptr(Wd), _ptr(Wu), _ptr(cw), _ptr(Ub), _ptr(bb),
+                                   _ptr(w), _ptr(beta), B, T, Dm, H, d, R, _dtype_code(x),
+                                   ctypes.c_void_p(st.cuda_stream))
+    _check(rc, "path_producer_fwd")
+    return w, beta
 
 
 class DecodeCache:

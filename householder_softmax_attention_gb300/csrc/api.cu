@@ -391,6 +391,40 @@ int path_attn_decode_step(const void* q, const void* k, const void* v, const voi
   return rc;
 }
 
+int path_producer_fwd(const void* x, const void* Wd, const void* Wu, const float* cw,
+                      const void* Ub, const float* bb, void* w, float* beta, int B, int T,
+                      int Dm, int H, int d, int R, int dtype, void* stream) {
+  if (!x || !Wd || !Wu || !cw || !Ub || !bb || !w || !beta) return PATH_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(Wd) || !aligned16(Wu) || !aligned16(Ub) || !aligned16(w) ||
+      !aligned16(beta) || (reinterpret_cast<uintptr_t>(cw) & 3u) ||
+      (reinterpret_cast<uintptr_t>(bb) & 3u))
+    return PATH_ERR_INVALID_ARG;
+  if (dtype != PATH_DTYPE_F32 && dtype != PATH_DTYPE_BF16) return PATH_ERR_INVALID_ARG;
+  if (B < 1 || T < 1 || H < 1 || Dm < 1 || R < 1) return PATH_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return PATH_ERR_UNSUPPORTED;
+  // tile shapes: Dm in 64-wide stages, R in 16-wide MMA steps, R + H columns
+  // of one projection tile (padded to a multiple of 8)
+  if (Dm % 64 != 0 || Dm > 32768 || R % 16 != 0 || R > 128 || R + H > 128)
+    return PATH_ERR_UNSUPPORTED;
+  const long long BT = static_cast<long long>(B) * T;
+  if (BT > INT_MAX / 2 || BT * H > INT_MAX) return PATH_ERR_UNSUPPORTED;
+  DeviceState* s = nullptr;
+  int rc = device_state(&s);
+  if (rc != PATH_OK) return rc;
+  if ((rc = check_device(s)) != PATH_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float* low = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&low),
+                                          producer_workspace_bytes(B, T, R), s->pool, st);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  if ((e = launch_producer(x, Wd, Wu, cw, Ub, bb, w, beta, low, B, T, Dm, H, d, R,
+                           dtype == PATH_DTYPE_BF16, st)) != cudaSuccess)
+    rc = set_cuda_error(e);
+  e = cudaFreeAsync(low, st);
+  if (rc == PATH_OK && e != cudaSuccess) rc = set_cuda_error(e);
+  return rc;
+}
+
 int path_attn_device_status(int device, int clear) {
   int prev = 0;
   cudaError_t e = cudaGetDevice(&prev);

@@ -164,6 +164,32 @@ int path_attn_decode_step(const void* q, const void* k, const void* v, const voi
                           void* out, float* lse, int B, int H, int Tmax, int d, int dtype,
                           void* stream);
 
+/*
+ * path_producer_fwd -- the producer of w and beta from the hidden states x
+ * (slides' frame "PaTH inserts a learned transformation along every path":
+ * low-rank projection, width-3 convolution, L2 normalization, beta = 2
+ * sigmoid(u^T x + b); OpenReview section "Model Architecture Details": per
+ * head, low-rank).  This library's readings of what the pages leave open:
+ *   p_t  = Wu (Wd x_t)                      (no bias)
+ *   z_t  = cw[:,0] p_{t-2} + cw[:,1] p_{t-1} + cw[:,2] p_t
+ *          (per channel, causal, p = 0 before the sequence start, no activation)
+ *   w_t  = z_t / max(|z_t|, 1e-12)          per head (d channels)
+ *   beta_t[h] = 2 sigmoid(Ub[h] . x_t + bb[h])
+ *
+ *   x     device, [B,T,Dm], dtype           Wd: device, [R,Dm], dtype
+ *   Wu    device, [H*d,R], dtype            cw: device, [H*d,3], fp32
+ *   Ub    device, [H,Dm], dtype             bb: device, [H], fp32
+ *   w     device, [B,H,T,d], dtype (out)    beta: device, [B,H,T], fp32 (out)
+ * The outputs are laid out as path_attn_fwd's w and beta inputs.  Arrays
+ * other than cw and bb must be 16-byte aligned.  Supported: d = 64 or 128;
+ * Dm a multiple of 64 up to 32768; R a multiple of 16 up to 128; R + H up to
+ * 128 (PATH_ERR_UNSUPPORTED otherwise).  Two kernel
+ * launches and a [B*T][R] fp32 stream-ordered scratch from the library's pool.
+ */
+int path_producer_fwd(const void* x, const void* Wd, const void* Wu, const float* cw,
+                      const void* Ub, const float* bb, void* w, float* beta, int B, int T,
+                      int Dm, int H, int d, int R, int dtype, void* stream);
+
 /* Human-readable name of a path_status_t value (static storage). */
 const char* path_attn_status_string(int status);
 

@@ -141,6 +141,53 @@ def make_decode_inputs(wl: Workload, device="cpu"):
                 lamcache=lamcache, scale=1.0 / math.sqrt(d))
 
 
+# The w / beta producer: hidden states x [B, T, Dm] with Dm = H * d, a rank-R
+# projection (R not on the pages: 64).
+@dataclass(frozen=True)
+class ProducerWorkload:
+    name: str
+    B: int
+    T: int
+    Dm: int
+    H: int
+    d: int
+    R: int
+    dtype: str = "bf16"
+    seed: int = 0
+
+    @property
+    def torch_dtype(self):
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+
+PRODUCER_WORKLOADS = {
+    "producer_t16k_d128": ProducerWorkload("producer_t16k_d128", 2, 16384, 2048, 16, 128, 64),
+    "producer_t16k_d64": ProducerWorkload("producer_t16k_d64", 2, 16384, 2048, 32, 64, 64),
+}
+
+
+def make_producer_inputs(wl: ProducerWorkload, device="cpu"):
+    """x ~ N(0, 1); Wd ~ N(0, 1/Dm); Wu ~ N(0, 1/R); conv taps ~ N(0, 1/3);
+    Ub ~ N(0, 1/Dm); bb ~ N(0, 1).  x and the matrices in the workload dtype,
+    taps and bias fp32."""
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(wl.seed + 7)
+    dt = wl.torch_dtype
+
+    def normal(shp, std):
+        return std * torch.randn(shp, generator=g, device=dev, dtype=torch.float32)
+
+    x = normal((wl.B, wl.T, wl.Dm), 1.0)
+    Wd = normal((wl.R, wl.Dm), wl.Dm ** -0.5)
+    Wu = normal((wl.H * wl.d, wl.R), wl.R ** -0.5)
+    cw = normal((wl.H * wl.d, 3), 3 ** -0.5)
+    Ub = normal((wl.H, wl.Dm), wl.Dm ** -0.5)
+    bb = normal((wl.H,), 1.0)
+    return dict(x=x.to(dt).contiguous(), Wd=Wd.to(dt).contiguous(), Wu=Wu.to(dt).contiguous(),
+                cw=cw.contiguous(), Ub=Ub.to(dt).contiguous(), bb=bb.contiguous())
+
+
 def sample_rows(T: int, C: int, n_extra: int, seed: int = 0):
     """A fixed, seeded set of query rows of one head for sampled parity checks:
     the first and last rows, chunk boundaries around the first and last four

@@ -130,3 +130,21 @@ def test_partial_validates_before_any_cuda_call(lib):
     assert part(-1) == INVALID
     assert part(8, w=None) == INVALID   # u needed when r > 0
     assert part(0, d=96) == UNSUPPORTED
+
+
+def test_producer_validates_before_any_cuda_call(lib):
+    p = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(8)]
+    prod = lambda B=1, T=8, Dm=128, H=2, d=64, R=16, dt=1, ptrs=p: lib.path_producer_fwd(
+        *ptrs, B, T, Dm, H, d, R, dt, None)
+    assert prod(Dm=100) == UNSUPPORTED       # Dm not a multiple of 64
+    assert prod(R=24) == UNSUPPORTED         # R not a multiple of 16
+    assert prod(R=128, H=8) == UNSUPPORTED   # R + H above 128
+    assert prod(d=96) == UNSUPPORTED
+    assert prod(T=0) == INVALID
+    assert prod(dt=4) == INVALID
+    bad = list(p)
+    bad[0] = None
+    assert prod(ptrs=bad) == INVALID
+    bad = list(p)
+    bad[6] = ctypes.c_void_p(0x70008)        # misaligned w
+    assert prod(ptrs=bad) == INVALID
