@@ -97,13 +97,10 @@ struct Inputs {
 
 // Kernel-family launchers (each returns the first launch error, if any).
 // Chunk preparation: fills kr, ql, ngt, sdt (and lam2 when gated); bf16 runs
-// one fused tensor-core kernel per chunk (tcgen05 at d = 128, mma.sync at
-// d = 64), fp32 the SIMT kernels.
+// one fused tcgen05 kernel per chunk, fp32 the SIMT kernels.
 cudaError_t launch_prep(const Geom& g, const Inputs& in, const Workspace& ws, int* dev_status,
                         cudaStream_t st, int* launches);
-cudaError_t launch_prep_mma(const Geom& g, const Inputs& in, const Workspace& ws,
-                            cudaStream_t st);
-// bf16, d = 128: the tcgen05 preparation (bounded waits report into dev_status)
+// bf16, d = 64 or 128: the tcgen05 preparation (bounded waits report into dev_status)
 cudaError_t launch_prep_tc(const Geom& g, const Inputs& in, const Workspace& ws, int* dev_status,
                            cudaStream_t st);
 // fp32 attention over the prepared chunks (SIMT, fp32 throughout).

@@ -17,8 +17,7 @@
 //   lam2 = log2(e) * inclusive cumsum of log f  (gate_ij = lam_i - lam_j).
 //
 // All arithmetic is fp32 (inputs widened exactly).  These SIMT kernels serve
-// fp32 inputs; bf16 inputs go to the fused tensor-core kernels (prep_tc.cu,
-// prep_mma.cu).
+// fp32 inputs; bf16 inputs go to the fused tensor-core kernel (prep_tc.cu).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -314,7 +313,7 @@ cudaError_t launch_prep(const Geom& g, const Inputs& in, const Workspace& ws, in
     ++n;
   }
   if (g.bf16) {
-    e = g.d == 128 ? launch_prep_tc(g, in, ws, dev_status, st) : launch_prep_mma(g, in, ws, st);
+    e = launch_prep_tc(g, in, ws, dev_status, st);
     if (e != cudaSuccess) return e;
     if (launches) *launches = n + 1;
     return cudaSuccess;

@@ -1,6 +1,6 @@
 // prep_solve.cuh -- the unit-lower-triangular inverse X = (I + L)^{-1} of a
-// 128 x 128 fp32 matrix in shared memory, used by both chunk-preparation
-// kernels (U = (I + strictLower(D W W^T))^{-1} D in "PaTH Attention: Position
+// 128 x 128 fp32 matrix in shared memory, used by the tensor-core chunk
+// preparation (U = (I + strictLower(D W W^T))^{-1} D in "PaTH Attention: Position
 // Encoding via Accumulating Householder Transformations", frame "A triangular
 // representation makes paths computable").  Recursive doubling: 16 x 16
 // diagonal blocks by substitution, then blocks of 16 on the CUDA cores and of

@@ -1,19 +1,20 @@
-// prep_tc.cu -- chunk preparation for bf16 inputs with d = 128 on tcgen05.
+// prep_tc.cu -- chunk preparation for bf16 inputs (d = 64 or 128) on tcgen05.
 //
-// One CTA (8 warps) per chunk of C = 128 tokens; same outputs as the
-// mma.sync preparation (see prep_mma.cu for the algebra, from "PaTH Attention:
-// Position Encoding via Accumulating Householder Transformations", frames "A
-// triangular representation makes paths computable" and "Backup: fix
-// orientation before implementing UT products").  Phases:
+// One CTA (8 warps) per chunk of C = 128 tokens; the outputs and their algebra
+// are those listed in prep.cu (from "PaTH Attention: Position Encoding via
+// Accumulating Householder Transformations", frames "A triangular
+// representation makes paths computable" and "Backup: fix orientation before
+// implementing UT products").  Phases:
 //
 //   P1  [W W^T | W K^T] = W [W; K]^T and [Q W^T | Q K^T] = Q [W; K]^T:
 //       two MMAs of width 256 per k-step (exact fp32 products of bf16 inputs)
 //   P2  L = strictLower(D W W^T) -> fp32 shared memory;
 //       S = strictLower(W K^T) -> bf16 hi / lo tiles
-//   P3  X = (I + L)^{-1} (shared with prep_mma.cu), U = X D -> bf16 hi / lo
+//   P3  X = (I + L)^{-1} (prep_solve.cuh), U = X D -> bf16 hi / lo
 //   P4  TK = U S (three hi/lo products), UW = U W (two)
 //   P5  TK, UW -> bf16 hi / lo tiles, laid out as [TK | UW]
-//   P6a [kr' | ngt'] = W^T [TK | UW]   (one width-256 MMA per term)
+//   P6a [kr' | ngt'] = W^T [TK | UW]   (one MMA of width C + d per term; at
+//       d = 64 the accumulator rows past d are never read)
 //       kr = K - kr'^T, ngt = -ngt'^T
 //   P6b [sd' | ql'] = -lower(Q W^T) [TK | UW]   (A from TMEM, three terms)
 //       sdt = log2(e) (scale (Q K^T + sd') + gate) transposed, ql = Q + ql'
@@ -34,7 +35,7 @@
 namespace pathattn {
 namespace {
 
-constexpr int kC = 128, kD = 128, kThreads = 256;
+constexpr int kC = 128, kThreads = 256;
 constexpr uint32_t kHalf = 16384;   // one 64-column half of a 128-row bf16 tile
 constexpr uint32_t kTile = 32768;   // a 128 x 128 bf16 tile
 // shared-memory regions (offsets from a 1024-aligned base)
@@ -81,7 +82,7 @@ __device__ __forceinline__ bool wait_mma(Bars* bars, uint32_t parity, int* statu
   return false;
 }
 
-template <bool kGate>
+template <int D, bool kGate>
 __global__ void __launch_bounds__(kThreads, 1)
     prep_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_k,
                    const __grid_constant__ CUtensorMap map_q, const __nv_bfloat16* __restrict__ q,
@@ -128,8 +129,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- P1: TMA loads, then the Gram blocks
   if (tid == 0) {
-    mbar_arrive_expect_tx(&bars->tma, 3 * kTile);
-    for (int h = 0; h < 2; ++h) {
+    mbar_arrive_expect_tx(&bars->tma, 3 * kC * D * 2);
+    for (int h = 0; h < D / 64; ++h) {
       tma_load_3d(base + kRWK + h * 2 * kHalf, &map_w, h * 64, t0, bh, &bars->tma);
       tma_load_3d(base + kRWK + h * 2 * kHalf + kHalf, &map_k, h * 64, t0, bh, &bars->tma);
       tma_load_3d(base + kRQS + h * kHalf, &map_q, h * 64, t0, bh, &bars->tma);
@@ -138,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       tc_fence_after_sync();
       constexpr uint32_t id = idesc_bf16_f32(128, 256, false, false);
-      for (int k = 0; k < kD / 16; ++k) {
+      for (int k = 0; k < D / 16; ++k) {
         const uint32_t kb = k >> 2, kk = (k & 3) * 32;
         const uint64_t bwk = sdesc_sw128(smem_addr(base + kRWK + kb * 2 * kHalf) + kk, 16, 1024);
         const uint64_t aw = sdesc_sw128(smem_addr(base + kRWK + kb * 2 * kHalf) + kk, 16, 1024);
@@ -222,6 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0 && ok) {
     tc_fence_after_sync();
     constexpr uint32_t id = idesc_bf16_f32(128, 128, false, true);
+    constexpr uint32_t id_uw = idesc_bf16_f32(128, D, false, true);
     const uint32_t u_hi = smem_addr(base + kRL), u_lo = u_hi + kTile;
     const uint32_t s_hi = smem_addr(base + kRQS), s_lo = s_hi + kTile;
     const uint32_t w_b = smem_addr(base + kRWK);
@@ -237,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int term = 0; term < 2; ++term) {
       const uint32_t at = term == 0 ? u_hi : u_lo;
       for (int k = 0; k < kC / 16; ++k)
-        mma_bf16_ss(tb + 128, a_desc(at, k), sdesc_sw128(w_b + k * 2048, 2 * kHalf, 1024), id,
+        mma_bf16_ss(tb + 128, a_desc(at, k), sdesc_sw128(w_b + k * 2048, 2 * kHalf, 1024), id_uw,
                     term > 0 || k > 0);
     }
     mma_commit(&bars->mma);
@@ -253,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* hi = base + kRQS;   // TK at +0 (two halves), UW at +kTile
     uint8_t* lo = base + kRL;
 #pragma unroll
-    for (int cc = 0; cc < 128; cc += 32) {
+    for (int cc = 0; cc < (halfc == 0 ? 128 : D); cc += 32) {
       const int c0 = halfc * 128 + cc;   // halfc 0: TK, 1: UW
       uint32_t v[32];
       tmem_ld_x32(tb + lb + c0, v);
@@ -273,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- P6a: [kr' | ngt'] = W^T [TK | UW]: D rows are the feature index f
   if (tid == 0 && ok) {
     tc_fence_after_sync();
-    constexpr uint32_t id = idesc_bf16_f32(128, 256, true, true);
+    constexpr uint32_t id = idesc_bf16_f32(128, kC + D, true, true);
     const uint32_t w_b = smem_addr(base + kRWK);
     const uint32_t b_hi = smem_addr(base + kRQS), b_lo = smem_addr(base + kRL);
     for (int term = 0; term < 2; ++term) {
@@ -309,11 +311,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   ok = wait_mma(bars, mma_phase, status) && ok;
   mma_phase ^= 1;
   tc_fence_after_sync();
-  // epilogue: kr[j][f] = K[j][f] - D[f][j] (half 0), ngt[n][f] = -D[f][128 + n] (half 1)
+  // epilogue: kr[j][f] = K[j][f] - Acc[f][j] (half 0), ngt[n][f] = -Acc[f][128 + n]
+  // (half 1), features f < D
   {
     const int f = row;
-    if (halfc == 0) {
-      __nv_bfloat16* out = kr + static_cast<size_t>(ch) * kC * kD + f;
+    if (f >= D) {
+    } else if (halfc == 0) {
+      __nv_bfloat16* out = kr + static_cast<size_t>(ch) * kC * D + f;
       const uint8_t* kt = base + kRWK + kHalf;  // K rows inside the W|K halves
       for (int cc = 0; cc < 128; cc += 32) {
         uint32_t v[32];
@@ -324,17 +328,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t off = (f >> 6) * 2 * kHalf + j * 128 +
                                ((((f & 63) >> 3) ^ (j & 7)) << 4) + ((f & 7) << 1);
           const float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(kt + off));
-          out[static_cast<size_t>(j) * kD] = __float2bfloat16_rn(kv - __uint_as_float(v[u]));
+          out[static_cast<size_t>(j) * D] = __float2bfloat16_rn(kv - __uint_as_float(v[u]));
         }
       }
     } else {
-      __nv_bfloat16* out = ngt + static_cast<size_t>(ch) * kD * kD + f;
-      for (int cc = 0; cc < 128; cc += 32) {
+      __nv_bfloat16* out = ngt + static_cast<size_t>(ch) * D * D + f;
+      for (int cc = 0; cc < D; cc += 32) {
         uint32_t v[32];
         tmem_ld_x32(tb + lb + 128 + cc, v);
 #pragma unroll
         for (int u = 0; u < 32; ++u)
-          out[static_cast<size_t>(cc + u) * kD] = __float2bfloat16_rn(-__uint_as_float(v[u]));
+          out[static_cast<size_t>(cc + u) * D] = __float2bfloat16_rn(-__uint_as_float(v[u]));
       }
     }
   }
@@ -344,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- P6b: [sd' | ql'] = -lower(Q W^T) [TK | UW], A from TMEM (hi, lo)
   if (tid == 0 && ok) {
     tc_fence_after_sync();
-    constexpr uint32_t id = idesc_bf16_f32(128, 256, false, true);
+    constexpr uint32_t id = idesc_bf16_f32(128, kC + D, false, true);
     const uint32_t b_hi = smem_addr(base + kRQS), b_lo = smem_addr(base + kRL);
     for (int term = 0; term < 3; ++term) {
       const uint32_t acol = term == 2 ? 320 : 256;   // A: hi or lo
@@ -381,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       // ql' rows to shared memory (the lo tiles are dead once the MMA is done)
       float* sq = sL;
-      for (int cc = 0; cc < 128; cc += 32) {
+      for (int cc = 0; cc < D; cc += 32) {
         uint32_t v[32];
         tmem_ld_x32(tb + lb + 128 + cc, v);
 #pragma unroll
@@ -398,18 +402,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   // all Q loads of a thread are issued before they are used
   {
     const float* sq = sL;
-    float* out = ql + static_cast<size_t>(ch) * kC * kD;
-    constexpr int kIter = kC * kD / 4 / kThreads;  // 16
+    float* out = ql + static_cast<size_t>(ch) * kC * D;
+    constexpr int kIter = kC * D / 4 / kThreads;  // 16 at d = 128
     uint2 qv[kIter];
 #pragma unroll
     for (int r = 0; r < kIter; ++r) {
-      const int e = tid + r * kThreads, i = e / (kD / 4), n4 = (e % (kD / 4)) * 4;
-      qv[r] = i < nrows ? __ldg(reinterpret_cast<const uint2*>(q + (row0 + i) * kD + n4))
+      const int e = tid + r * kThreads, i = e / (D / 4), n4 = (e % (D / 4)) * 4;
+      qv[r] = i < nrows ? __ldg(reinterpret_cast<const uint2*>(q + (row0 + i) * D + n4))
                         : make_uint2(0u, 0u);
     }
 #pragma unroll
     for (int r = 0; r < kIter; ++r) {
-      const int e = tid + r * kThreads, i = e / (kD / 4), n4 = (e % (kD / 4)) * 4;
+      const int e = tid + r * kThreads, i = e / (D / 4), n4 = (e % (D / 4)) * 4;
       float4 o = *reinterpret_cast<const float4*>(sq + i * kSL + n4);
       const __nv_bfloat162 q01 = *reinterpret_cast<const __nv_bfloat162*>(&qv[r].x);
       const __nv_bfloat162 q23 = *reinterpret_cast<const __nv_bfloat162*>(&qv[r].y);
@@ -417,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       o.y += __high2float(q01);
       o.z += __low2float(q23);
       o.w += __high2float(q23);
-      *reinterpret_cast<float4*>(out + i * kD + n4) = o;
+      *reinterpret_cast<float4*>(out + i * D + n4) = o;
     }
   }
   if (warp == 1) {
@@ -441,12 +445,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // [BH][T][d] bf16 input seen as a 3D map with 128-byte-swizzled boxes of 64
 // features x 128 tokens (tokens past T read as zero).
-bool make_input_map(CUtensorMap* m, const void* ptr, int T, int BH) {
+bool make_input_map(CUtensorMap* m, const void* ptr, int D, int T, int BH) {
   auto enc = encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(T),
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(T),
                         static_cast<cuuint64_t>(BH)};
-  cuuint64_t strides[2] = {kD * 2, static_cast<cuuint64_t>(T) * kD * 2};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(T) * D * 2};
   cuuint32_t box[3] = {64, kC, 1};
   cuuint32_t es[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
@@ -454,14 +458,14 @@ bool make_input_map(CUtensorMap* m, const void* ptr, int T, int BH) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kGate>
+template <int D, bool kGate>
 cudaError_t launch_one(const Geom& g, const Inputs& in, const Workspace& ws, int* status,
                        cudaStream_t st) {
   CUtensorMap mw, mk, mq;
-  if (!make_input_map(&mw, in.w, g.T, g.BH) || !make_input_map(&mk, in.k, g.T, g.BH) ||
-      !make_input_map(&mq, in.q, g.T, g.BH))
+  if (!make_input_map(&mw, in.w, D, g.T, g.BH) || !make_input_map(&mk, in.k, D, g.T, g.BH) ||
+      !make_input_map(&mq, in.q, D, g.T, g.BH))
     return cudaErrorInvalidValue;
-  auto kern = prep_tc_kernel<kGate>;
+  auto kern = prep_tc_kernel<D, kGate>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
@@ -476,8 +480,14 @@ cudaError_t launch_one(const Geom& g, const Inputs& in, const Workspace& ws, int
 
 cudaError_t launch_prep_tc(const Geom& g, const Inputs& in, const Workspace& ws, int* status,
                            cudaStream_t st) {
-  if (g.C != kC || g.d != kD || !g.bf16) return cudaErrorInvalidValue;
-  return g.gate ? launch_one<true>(g, in, ws, status, st) : launch_one<false>(g, in, ws, status, st);
+  if (g.C != kC || !g.bf16) return cudaErrorInvalidValue;
+  if (g.d == 128)
+    return g.gate ? launch_one<128, true>(g, in, ws, status, st)
+                  : launch_one<128, false>(g, in, ws, status, st);
+  if (g.d == 64)
+    return g.gate ? launch_one<64, true>(g, in, ws, status, st)
+                  : launch_one<64, false>(g, in, ws, status, st);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace pathattn
