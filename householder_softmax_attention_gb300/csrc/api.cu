@@ -417,7 +417,7 @@ int path_producer_fwd(const void* x, const void* Wd, const void* Wu, const float
   cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&low),
                                           producer_workspace_bytes(B, T, R), s->pool, st);
   if (e != cudaSuccess) return set_cuda_error(e);
-  if ((e = launch_producer(x, Wd, Wu, cw, Ub, bb, w, beta, low, B, T, Dm, H, d, R,
+  if ((e = launch_producer(x, Wd, Wu, cw, Ub, bb, w, beta, low, s->status, B, T, Dm, H, d, R,
                            dtype == PATH_DTYPE_BF16, st)) != cudaSuccess)
     rc = set_cuda_error(e);
   e = cudaFreeAsync(low, st);

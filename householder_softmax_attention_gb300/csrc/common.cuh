@@ -139,12 +139,16 @@ cudaError_t launch_decode(const DecodeParams& p, int BH, int d, bool bf16, cudaS
 // from the chunk factors kr and ngt of a prepared workspace.
 cudaError_t launch_align_keys(const Geom& g, const Workspace& ws, float* kcache, int Tmax,
                               cudaStream_t st);
-// w / beta producer (producer.cu): two launches, `low` is [B*T][R] fp32.
+// w / beta producer (producer.cu): two launches, `low` is [B*T][R] (fp32 at most).
 size_t producer_workspace_bytes(int B, int T, int R);
 cudaError_t launch_producer(const void* x, const void* Wd, const void* Wu, const float* cw,
                             const void* Ub, const float* bb, void* w, float* beta, float* low,
-                            int B, int T, int Dm, int H, int d, int R, bool bf16_in,
+                            int* status, int B, int T, int Dm, int H, int d, int R, bool bf16_in,
                             cudaStream_t st);
+// bf16 producer projection on tcgen05 (producer_tc.cu); `low` is [B*T][R] bf16.
+cudaError_t launch_producer_proj_tc(const void* x, const void* Wd, const void* Ub,
+                                    const float* bb, void* low, float* beta, int* status, int B,
+                                    int T, int Dm, int H, int R, cudaStream_t st);
 // Gate prefix: out[bh * out_stride + t] = mult * sum_{s<=t} logf[bh][s] for
 // t < n_out (tokens at or past T add 0).
 cudaError_t launch_gate_prefix(const float* logf, float* out, int BH, int T, int n_out,

@@ -11,11 +11,10 @@
 // no activation; w = z / max(|z|, 1e-12) per (token, head); one u and b per
 // head.
 //
-// producer_proj_kernel  low = x [Wd ; Ub]^T for a tile of 128 tokens (bf16:
-//                       mma.sync with ldmatrix fragments, three cp.async
-//                       stages over Dm; fp32: SIMT).  The first R columns are
-//                       kept (workspace, in the input dtype), the last H
-//                       become beta = 2 sigmoid(. + b) in [B, H, T].
+// projection          low = x [Wd ; Ub]^T: bf16 on tcgen05 (producer_tc.cu),
+//                     fp32 here (SIMT).  The first R columns are kept
+//                     (workspace, in the input dtype), the last H become
+//                     beta = 2 sigmoid(. + b) in [B, H, T].
 // producer_mix_*_kernel per 112-token tile (bf16: and group of 4 heads, whose
 //                       low rows plus 16 of history are loaded once): per
 //                       head, p = low Wu_h^T (bf16: mma.sync in registers,
@@ -35,12 +34,6 @@ namespace pathattn {
 namespace {
 
 using bf16 = __nv_bfloat16;
-
-constexpr int kRows = 128;     // tokens per CTA
-constexpr int kKc = 64;        // Dm per pipeline stage
-constexpr int kXLd = kKc + 8;  // bf16 row stride of staged tiles (conflict-free fragments)
-constexpr int kStages = 3;
-constexpr int kNMax = 128;     // R + H
 
 __device__ __forceinline__ void cp16_zfill(void* dst, const void* src, bool valid) {
   const int bytes = valid ? 16 : 0;
@@ -93,11 +86,6 @@ struct ProdArgs {
   int B, T, Dm, H, R;
 };
 
-__device__ __forceinline__ void store_beta(const ProdArgs& p, int row, int h, float v) {
-  const int b = row / p.T, t = row % p.T;
-  p.beta[(static_cast<size_t>(b) * p.H + h) * p.T + t] = beta_of(v + p.bb[h]);
-}
-
 __device__ __forceinline__ void store_proj(const ProdArgs& p, int row, int c, float v) {
   if (c < p.R) {
     static_cast<float*>(p.low)[static_cast<size_t>(row) * p.R + c] = v;
@@ -108,91 +96,6 @@ __device__ __forceinline__ void store_proj(const ProdArgs& p, int row, int c, fl
 }
 
 // ------------------------------------------------------------- projection
-__global__ void __launch_bounds__(256, 2) producer_proj_bf16_kernel(const ProdArgs p) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  constexpr int kStageElems = 2 * kRows * kXLd;  // x tile then W tile
-  bf16* sbase = reinterpret_cast<bf16*>(smem);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t4 = lane & 3;
-  const int BT = p.B * p.T, N = p.R + p.H, NT = (N + 7) / 8;  // rows N .. 8 NT - 1 are zero
-  const int r0 = blockIdx.x * kRows;
-  const bf16* x = static_cast<const bf16*>(p.x);
-  const bf16* Wd = static_cast<const bf16*>(p.Wd);
-  const bf16* Ub = static_cast<const bf16*>(p.Ub);
-  const int nk = p.Dm / kKc;
-  auto load = [&](int kc, int stage) {
-    bf16* xs = sbase + stage * kStageElems;
-    bf16* ws = xs + kRows * kXLd;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int piece = tid + 256 * i, row = piece >> 3, q = piece & 7;
-      const int grow = r0 + row;
-      const bool ok = grow < BT;
-      cp16_zfill(xs + row * kXLd + q * 8,
-                 x + static_cast<size_t>(ok ? grow : 0) * p.Dm + kc * kKc + q * 8, ok);
-      if (row < 8 * NT) {
-        const bf16* src = row < p.R ? Wd + static_cast<size_t>(row) * p.Dm
-                          : row < N ? Ub + static_cast<size_t>(row - p.R) * p.Dm
-                                    : Wd;
-        cp16_zfill(ws + row * kXLd + q * 8, src + (row < N ? kc * kKc + q * 8 : 0), row < N);
-      }
-    }
-  };
-  float acc[kNMax / 8][4];
-#pragma unroll
-  for (int n = 0; n < kNMax / 8; ++n)
-#pragma unroll
-    for (int f = 0; f < 4; ++f) acc[n][f] = 0.f;
-#pragma unroll
-  for (int s = 0; s < kStages - 1; ++s) {
-    if (s < nk) load(s, s);
-    cp_commit();
-  }
-  for (int kc = 0; kc < nk; ++kc) {
-    cp_wait<kStages - 2>();
-    __syncthreads();
-    if (kc + kStages - 1 < nk) load(kc + kStages - 1, (kc + kStages - 1) % kStages);
-    cp_commit();
-    const bf16* xs = sbase + (kc % kStages) * kStageElems;
-    const bf16* ws = xs + kRows * kXLd;
-#pragma unroll
-    for (int ks = 0; ks < kKc / 16; ++ks) {
-      uint32_t a[4];
-      ldsm_a(a, xs, kXLd, warp * 16, ks * 16, lane);
-#pragma unroll
-      for (int n = 0; n < kNMax / 8; n += 2) {
-        if (n < NT) {
-          uint32_t b[4];
-          ldsm_b2(b, ws, kXLd, n * 8, ks * 16, lane);
-          mma_bf16_16816(acc[n], a, b[0], b[1]);
-          if (n + 1 < NT) mma_bf16_16816(acc[n + 1], a, b[2], b[3]);
-        }
-      }
-    }
-  }
-  cp_wait<0>();
-  // low (first R columns) in bf16, beta from the last H columns
-  bf16* low = static_cast<bf16*>(p.low);
-  const int ra = r0 + warp * 16 + g, rb = ra + 8;
-#pragma unroll
-  for (int n = 0; n < kNMax / 8; ++n) {
-    if (n >= NT) continue;
-    const int c = n * 8 + 2 * t4;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int row = half ? rb : ra;
-      if (row >= BT) continue;
-      const float v0 = acc[n][2 * half], v1 = acc[n][2 * half + 1];
-      if (c + 1 < p.R) {
-        *reinterpret_cast<__nv_bfloat162*>(low + static_cast<size_t>(row) * p.R + c) =
-            __floats2bfloat162_rn(v0, v1);
-      } else {
-        if (c < N) store_beta(p, row, c - p.R, v0);
-        if (c + 1 < N) store_beta(p, row, c + 1 - p.R, v1);
-      }
-    }
-  }
-}
-
 // fp32: one CTA per token, one thread per output column.
 __global__ void __launch_bounds__(128) producer_proj_f32_kernel(const ProdArgs p) {
   extern __shared__ float xrow[];
@@ -281,9 +184,8 @@ __global__ void __launch_bounds__(256, 2) producer_mix_bf16_kernel(const ProdArg
   }
   // the two rows this lane holds: local rows 16 w + g (A) and 16 w + g + 8 (B)
   const int growA = r0 - 16 + warp * 16 + g, growB = growA + 8;
-  const bool outA = warp > 0 && growA < BT, outB = warp > 0 && growB < BT;
-  const int tA = growA >= 0 ? growA % p.T : 0, bA = growA >= 0 ? growA / p.T : 0;
-  const int tB = growB >= 0 ? growB % p.T : 0, bB = growB >= 0 ? growB / p.T : 0;
+  const int tA = growA >= 0 ? growA % p.T : 0;
+  const int tB = growB >= 0 ? growB % p.T : 0;
   const float m1A = tA >= 1 ? 1.f : 0.f, m2A = tA >= 2 ? 1.f : 0.f;
   const float m1B = tB >= 1 ? 1.f : 0.f, m2B = tB >= 2 ? 1.f : 0.f;
   const unsigned full = 0xffffffffu;
@@ -477,18 +379,15 @@ size_t producer_workspace_bytes(int B, int T, int R) {
 
 cudaError_t launch_producer(const void* x, const void* Wd, const void* Wu, const float* cw,
                             const void* Ub, const float* bb, void* w, float* beta, float* low,
-                            int B, int T, int Dm, int H, int d, int R, bool bf16_in,
+                            int* status, int B, int T, int Dm, int H, int d, int R, bool bf16_in,
                             cudaStream_t st) {
   const ProdArgs p{x, Wd, Wu, Ub, cw, bb, w, beta, low, B, T, Dm, H, R};
   const int BT = B * T;
   cudaError_t e;
   if (bf16_in) {
-    constexpr int smem = kStages * 2 * kRows * kXLd * 2;
-    if ((e = cudaFuncSetAttribute(producer_proj_bf16_kernel,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
+    if ((e = launch_producer_proj_tc(x, Wd, Ub, bb, low, beta, status, B, T, Dm, H, R, st)) !=
         cudaSuccess)
       return e;
-    producer_proj_bf16_kernel<<<(BT + kRows - 1) / kRows, 256, smem, st>>>(p);
   } else {
     const int smem = Dm * 4;
     if ((e = cudaFuncSetAttribute(producer_proj_f32_kernel,
@@ -496,8 +395,8 @@ cudaError_t launch_producer(const void* x, const void* Wd, const void* Wu, const
         cudaSuccess)
       return e;
     producer_proj_f32_kernel<<<BT, 128, smem, st>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return d == 128 ? launch_mix<128>(p, bf16_in, st) : launch_mix<64>(p, bf16_in, st);
 }
 

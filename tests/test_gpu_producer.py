@@ -38,6 +38,9 @@ def _tol(dtype):
     ProducerWorkload("p_bf16", 3, 150, 256, 4, 128, 64, "bf16", seed=3),
     ProducerWorkload("p_bf16_d64", 2, 333, 512, 8, 64, 48, "bf16", seed=4),
     ProducerWorkload("p_bf16_short", 4, 1, 64, 8, 64, 16, "bf16", seed=5),
+    ProducerWorkload("p_bf16_d64_r64", 3, 150, 128, 8, 64, 64, "bf16", seed=6),
+    ProducerWorkload("p_bf16_t1_r64", 5, 1, 64, 4, 128, 64, "bf16", seed=7),
+    ProducerWorkload("p_bf16_r64_h3", 2, 260, 192, 3, 128, 64, "bf16", seed=8),
 ], ids=lambda w: w.name)
 def test_producer_matches_oracle(wl):
     x = make_producer_inputs(wl)
@@ -69,3 +72,4 @@ def test_full_size_producer_sampled(name):
         ref_w, ref_b = producer_fwd(xw, W["Wd"], W["Wu"], W["cw"], W["Ub"], W["bb"], wl.H, wl.d)
         assert np.abs(_np(w[b, :, t]) - ref_w[0, :, -1]).max() <= tw, (b, t)
         assert np.abs(_np(beta[b, :, t]) - ref_b[0, :, -1]).max() <= tb, (b, t)
+
