@@ -19,7 +19,8 @@
 //
 // Warp roles (384 threads):
 //   warp 0      TMA producer: kr_c over ngt_c (one B tile), V (own ring)
-//   warp 1      TMEM allocation and the single MMA-issuing thread
+//   warp 1      TMEM allocation; one thread issues the [S | Qm] MMAs
+//   warp 2      one thread issues the O += P V MMAs
 //   warps 4-7   softmax: one query row per thread (TMEM lane = row)
 //   warps 8-11  running-query conversion Qm -> Qw (and its initial load)
 // TMEM columns: S [0,128), Qm (d), O (d), Qw (d/2, packed bf16x2), P (64).
@@ -174,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->p_full, 4);  // one arrival per warp
     mbar_init(&bars->qk_done, 1);
     mbar_init(&bars->pv_done, 1);
-    mbar_init(&bars->final_done, 1);
+    mbar_init(&bars->final_done, 2);  // one commit from each MMA-issuing thread
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -233,13 +234,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ logits issuer
+    // [S | Qm] += Qw [kr_c ; ngt_c]^T for c = b-1 .. 0.  A second thread
+    // (warp 2) issues O += P V: each waits only on its own barriers, so the
+    // tensor pipe is fed while the other is blocked (one issuing thread spent
+    // most of a step in barrier waits with the pipe idle).
     if (lane == 0) {
-      const uint32_t tS = tb + Cfg::kColS, tO = tb + Cfg::kColO, tQm = tb + Cfg::kColQm,
-                     tQw = tb + Cfg::kColQw, tP = tb + Cfg::kColP;
+      const uint32_t tS = tb + Cfg::kColS, tQw = tb + Cfg::kColQw;
       constexpr uint32_t idS = idesc_bf16_f32(128, kC, false, false);       // S only
       constexpr uint32_t idSQ = idesc_bf16_f32(128, kC + D, false, false);  // [S | Qm]
-      constexpr uint32_t idPV = idesc_bf16_f32(128, D, false, true);
       bool ok = true;
       for (int n = 0; n < b && ok; ++n) {
         const int c = b - 1 - n, s = n & 1;
@@ -250,9 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after_sync();
         const uint32_t kg_a = smem_addr(s_kg + s * Cfg::kKgBytes);
-        // [S | Qm] += Qw [kr_c ; ngt_c]^T: the logits and the backward crossing
-        // of chunk c in one MMA of width kC + D (S starts from zero); the last
-        // chunk needs no crossing
+        // the logits and the backward crossing of chunk c in one MMA of width
+        // kC + D (S starts from zero); the last chunk needs no crossing
         const uint32_t id = c > 0 ? idSQ : idS;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
@@ -261,7 +263,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(&bars->qk_done);
         mma_commit(&bars->kg_empty[s]);
-        // O += P_{c+1} V_{c+1}
+      }
+      if (!ok) record_timeout(bars, status);
+      // this thread's MMAs complete before TMEM is released
+      mma_commit(&bars->final_done);
+      mbar_wait(&bars->final_done, 0, nullptr, LIM);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ PV issuer
+    // O += P_{c+1} V_{c+1} for n = 0 .. b (the diagonal's P first)
+    if (lane == 0) {
+      const uint32_t tO = tb + Cfg::kColO, tP = tb + Cfg::kColP;
+      constexpr uint32_t idPV = idesc_bf16_f32(128, D, false, true);
+      bool ok = true;
+      for (int n = 0; n <= b && ok; ++n) {
+        const int s = n & 1;
         ok = mbar_wait(&bars->p_full, n & 1, abort_flag, LIM);
         if (ok) ok = mbar_wait(&bars->v_full[s], (n >> 1) & 1, abort_flag, LIM);
         if (!ok) break;
@@ -272,24 +288,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ts(tO, tP + k * 8, sdesc_sw128(v_a + k * 2048, kC * 128, 1024), idPV,
                       (n > 0 || k > 0));
         mma_commit(&bars->pv_done);
-        mma_commit(&bars->v_empty[s]);
-      }
-      if (ok) {
-        const int s = b & 1;
-        ok = mbar_wait(&bars->p_full, b & 1, abort_flag, LIM);
-        if (ok) ok = mbar_wait(&bars->v_full[s], (b >> 1) & 1, abort_flag, LIM);
-        if (ok) {
-          tc_fence_after_sync();
-          const uint32_t v_a = smem_addr(s_v + s * Cfg::kVBytes);
-#pragma unroll
-          for (int k = 0; k < kC / 16; ++k)
-            mma_bf16_ts(tO, tP + k * 8, sdesc_sw128(v_a + k * 2048, kC * 128, 1024), idPV,
-                        (b > 0 || k > 0));
-          mma_commit(&bars->pv_done);
-        }
+        if (n < b) mma_commit(&bars->v_empty[s]);
       }
       if (!ok) record_timeout(bars, status);
-      // all MMAs of this CTA complete before TMEM is released
       mma_commit(&bars->final_done);
       mbar_wait(&bars->final_done, 0, nullptr, LIM);
     }
