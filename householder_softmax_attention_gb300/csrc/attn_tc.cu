@@ -66,7 +66,7 @@ struct TcCfg {
 
 struct Bars {
   uint64_t kg_full[2], kg_empty[2], v_full[2], v_empty[2];
-  uint64_t q_ready, s_free, p_full, qk_done, pv_done, final_done;
+  uint64_t sq_ready, p_full, qk_done, pv_done, final_done;
   uint32_t tmem_base;
   int abort_flag;
   alignas(16) float gate[2][kC];  // FoX: log2-domain gate prefix, read as float4
@@ -170,8 +170,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
     }
-    mbar_init(&bars->q_ready, 4);  // one arrival per warp
-    mbar_init(&bars->s_free, 4);  // one arrival per warp
+    // the next [S | Qm] MMA may go once Qw is refreshed (4 running-query
+    // warps) and S has been read and zeroed (4 softmax warps)
+    mbar_init(&bars->sq_ready, 8);
     mbar_init(&bars->p_full, 4);  // one arrival per warp
     mbar_init(&bars->qk_done, 1);
     mbar_init(&bars->pv_done, 1);
@@ -246,10 +247,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int n = 0; n < b && ok; ++n) {
         const int c = b - 1 - n, s = n & 1;
-        ok = mbar_wait(&bars->q_ready, n & 1, abort_flag, LIM);
-        // S has been read and zeroed by the softmax warps
-        if (ok) ok = mbar_wait(&bars->s_free, n & 1, abort_flag, LIM);
-        if (ok) ok = mbar_wait(&bars->kg_full[s], (n >> 1) & 1, abort_flag, LIM);
+        // the stage is usually loaded long before: check it first, then wait
+        // for Qw and S (one barrier, the one that blocks)
+        ok = mbar_spin(&bars->kg_full[s], (n >> 1) & 1, abort_flag, LIM);
+        if (ok) ok = mbar_spin(&bars->sq_ready, n & 1, abort_flag, LIM);
         if (!ok) break;
         tc_fence_after_sync();
         const uint32_t kg_a = smem_addr(s_kg + s * Cfg::kKgBytes);
@@ -278,8 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int n = 0; n <= b && ok; ++n) {
         const int s = n & 1;
-        ok = mbar_wait(&bars->p_full, n & 1, abort_flag, LIM);
-        if (ok) ok = mbar_wait(&bars->v_full[s], (n >> 1) & 1, abort_flag, LIM);
+        ok = mbar_spin(&bars->v_full[s], (n >> 1) & 1, abort_flag, LIM);
+        if (ok) ok = mbar_spin(&bars->p_full, n & 1, abort_flag, LIM);
         if (!ok) break;
         tc_fence_after_sync();
         const uint32_t v_a = smem_addr(s_v + s * Cfg::kVBytes);
@@ -316,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int cc = 0; cc < kC; cc += 32) tmem_st_x32(tS + cc, z);
       tmem_st_wait();
       tc_fence_before_sync();
-      warp_arrive(&bars->s_free);
+      warp_arrive(&bars->sq_ready);
     }
     // diagonal chunk: precomputed log2-domain logits sdt[ch][j][i]
     {
@@ -365,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
       }
       tc_fence_before_sync();
-      warp_arrive(&bars->s_free);
+      warp_arrive(&bars->sq_ready);
       float mx = -INFINITY;
       if (kGate) {
         const float4* lg = reinterpret_cast<const float4*>(&bars->gate[n & 1][0]);
@@ -495,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_x32(tQw + cc, *reinterpret_cast<uint32_t(*)[32]>(&qw[cc]));
       tmem_st_wait();
       tc_fence_before_sync();
-      warp_arrive(&bars->q_ready);
+      warp_arrive(&bars->sq_ready);
       bool ok = true;
       for (int n = 0; n + 1 < b; ++n) {
         // Qm (and S) are final for this step once the fused MMA is done
@@ -515,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st_x32(tQw + cc, *reinterpret_cast<uint32_t(*)[32]>(&qw[cc]));
         tmem_st_wait();
         tc_fence_before_sync();
-        warp_arrive(&bars->q_ready);
+        warp_arrive(&bars->sq_ready);
       }
       if (!ok) record_timeout(bars, status);
     }

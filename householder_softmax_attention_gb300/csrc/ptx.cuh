@@ -77,6 +77,34 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+__device__ __forceinline__ uint32_t mbar_test_wait(uint32_t bar_addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar_addr), "r"(parity)
+      : "memory");
+  return ok;
+}
+
+// mbar_wait for a single thread on a pipeline's critical path: polls without
+// suspending (a suspended try_wait wakes up a few hundred cycles after the
+// phase completes), with the same time limit and abort flag.
+__device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity,
+                                          const volatile int* abort, uint64_t limit_ns) {
+  const uint32_t a = smem_addr(bar);
+  if (mbar_test_wait(a, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_test_wait(a, parity)) return true;
+    if ((i & 31) == 0) {
+      if (abort && *abort) return false;
+      if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
