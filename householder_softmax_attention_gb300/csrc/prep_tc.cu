@@ -85,8 +85,7 @@ __device__ __forceinline__ bool wait_mma(Bars* bars, uint32_t parity, int* statu
 template <int D, bool kGate>
 __global__ void __launch_bounds__(kThreads, 1)
     prep_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_k,
-                   const __grid_constant__ CUtensorMap map_q, const __nv_bfloat16* __restrict__ q,
-                   const float* __restrict__ beta, const float* __restrict__ lam2,
+                   const __grid_constant__ CUtensorMap map_q, const float* __restrict__ beta, const float* __restrict__ lam2,
                    __nv_bfloat16* __restrict__ kr, float* __restrict__ ql,
                    __nv_bfloat16* __restrict__ ngt, float* __restrict__ sdt, int* status, int T,
                    int Np, float sl2) {
@@ -342,8 +341,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   tc_fence_before_sync();
   __syncthreads();
+
+  // Q again, into the W | K region (free from here on), for the final pass
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&bars->tma, kC * D * 2);
+    for (int h = 0; h < D / 64; ++h)
+      tma_load_3d(base + kRWK + h * kHalf, &map_q, h * 64, t0, bh, &bars->tma);
+  }
 
   // ---- P6b: [sd' | ql'] = -lower(Q W^T) [TK | UW], A from TMEM (hi, lo)
   if (tid == 0 && ok) {
@@ -398,8 +405,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before_sync();
   __syncthreads();
-  // ql = Q + ql', one row per warp instruction: coalesced loads and stores;
-  // all Q loads of a thread are issued before they are used
+  // ql = Q + ql', one row per warp instruction: coalesced stores; Q from the
+  // copy that landed during P6b (rows past T read as zero)
+  if (!mbar_wait(&bars->tma, 1, &bars->abort_flag, kWaitLimitNs)) {
+    bars->abort_flag = 1;
+    atomicExch(status, PATH_DEV_ERR_TIMEOUT);
+  }
   {
     const float* sq = sL;
     float* out = ql + static_cast<size_t>(ch) * kC * D;
@@ -408,8 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int r = 0; r < kIter; ++r) {
       const int e = tid + r * kThreads, i = e / (D / 4), n4 = (e % (D / 4)) * 4;
-      qv[r] = i < nrows ? __ldg(reinterpret_cast<const uint2*>(q + (row0 + i) * D + n4))
-                        : make_uint2(0u, 0u);
+      qv[r] = *reinterpret_cast<const uint2*>(base + kRWK + tile_off(i, n4));
     }
 #pragma unroll
     for (int r = 0; r < kIter; ++r) {
@@ -470,7 +480,7 @@ cudaError_t launch_one(const Geom& g, const Inputs& in, const Workspace& ws, int
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
   kern<<<g.nch, kThreads, kSmemBytes, st>>>(
-      mw, mk, mq, static_cast<const __nv_bfloat16*>(in.q), in.beta, ws.lam2,
+      mw, mk, mq, in.beta, ws.lam2,
       static_cast<__nv_bfloat16*>(ws.kr), ws.ql, static_cast<__nv_bfloat16*>(ws.ngt), ws.sdt,
       status, g.T, g.Np, in.scale * kLog2e);
   return cudaGetLastError();
