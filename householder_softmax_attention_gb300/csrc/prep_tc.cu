@@ -13,9 +13,9 @@
 //   P3  X = (I + L)^{-1} (prep_solve.cuh), U = X D -> bf16 hi / lo
 //   P4  TK = U S (three hi/lo products), UW = U W (two)
 //   P5  TK, UW -> bf16 hi / lo tiles, laid out as [TK | UW]
-//   P6a [kr' | ngt'] = W^T [TK | UW]   (one MMA of width C + d per term; at
-//       d = 64 the accumulator rows past d are never read)
-//       kr = K - kr'^T, ngt = -ngt'^T
+//   P6a kr' = TK^T W, ngt' = UW^T W   (two terms each; at d = 64 the
+//       accumulator rows of ngt' past d are never read)
+//       kr = K - kr', ngt = -ngt'
 //   P6b [sd' | ql'] = -lower(Q W^T) [TK | UW]   (A from TMEM, three terms)
 //       sdt = log2(e) (scale (Q K^T + sd') + gate) transposed, ql = Q + ql'
 //
@@ -271,18 +271,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before_sync();
   __syncthreads();
 
-  // ---- P6a: [kr' | ngt'] = W^T [TK | UW]: D rows are the feature index f
+  // ---- P6a: kr' = TK^T W and ngt' = UW^T W (A = the MN-major [TK | UW] tiles,
+  // B = W): one output row per TMEM lane, so that the epilogue writes rows
   if (tid == 0 && ok) {
     tc_fence_after_sync();
-    constexpr uint32_t id = idesc_bf16_f32(128, kC + D, true, true);
+    constexpr uint32_t id = idesc_bf16_f32(128, D, true, true);
     const uint32_t w_b = smem_addr(base + kRWK);
     const uint32_t b_hi = smem_addr(base + kRQS), b_lo = smem_addr(base + kRL);
-    for (int term = 0; term < 2; ++term) {
-      const uint32_t bt = term == 0 ? b_hi : b_lo;
-      for (int k = 0; k < kC / 16; ++k)
-        mma_bf16_ss(tb + 0, sdesc_sw128(w_b + k * 2048, 2 * kHalf, 1024),
-                    sdesc_sw128(bt + k * 2048, kHalf, 1024), id, term > 0 || k > 0);
-    }
+    for (int part = 0; part < 2; ++part)        // TK^T W -> cols [0, D), UW^T W -> [128, 128 + D)
+      for (int term = 0; term < 2; ++term) {    // hi, lo
+        const uint32_t at = (term == 0 ? b_hi : b_lo) + part * kTile;
+        for (int k = 0; k < kC / 16; ++k)
+          mma_bf16_ss(tb + part * 128, sdesc_sw128(at + k * 2048, kHalf, 1024),
+                      sdesc_sw128(w_b + k * 2048, 2 * kHalf, 1024), id, term > 0 || k > 0);
+      }
     mma_commit(&bars->mma);
   } else if (tid == 0) {
     mma_commit(&bars->mma);
@@ -310,35 +312,44 @@ __global__ void __launch_bounds__(kThreads, 1)
   ok = wait_mma(bars, mma_phase, status) && ok;
   mma_phase ^= 1;
   tc_fence_after_sync();
-  // epilogue: kr[j][f] = K[j][f] - Acc[f][j] (half 0), ngt[n][f] = -Acc[f][128 + n]
-  // (half 1), features f < D
-  {
-    const int f = row;
-    if (f >= D) {
-    } else if (halfc == 0) {
-      __nv_bfloat16* out = kr + static_cast<size_t>(ch) * kC * D + f;
-      const uint8_t* kt = base + kRWK + kHalf;  // K rows inside the W|K halves
-      for (int cc = 0; cc < 128; cc += 32) {
-        uint32_t v[32];
-        tmem_ld_x32(tb + lb + cc, v);
+  // epilogue: kr[j][:] = K[j][:] - kr'[j][:] (half 0, row j = lane), ngt[n][:] =
+  // -ngt'[n][:] (half 1, rows n < D): whole rows, 16 bytes per store
+  if (halfc == 0) {
+    const int j = row;
+    uint4* out = reinterpret_cast<uint4*>(kr + (static_cast<size_t>(ch) * kC + j) * D);
+    const uint8_t* kt = base + kRWK + kHalf;  // K rows inside the W|K halves
+    for (int cc = 0; cc < D; cc += 32) {
+      uint32_t v[32];
+      tmem_ld_x32(tb + lb + cc, v);
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-          const int j = cc + u;
-          const uint32_t off = (f >> 6) * 2 * kHalf + j * 128 +
-                               ((((f & 63) >> 3) ^ (j & 7)) << 4) + ((f & 7) << 1);
-          const float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(kt + off));
-          out[static_cast<size_t>(j) * D] = __float2bfloat16_rn(kv - __uint_as_float(v[u]));
-        }
-      }
-    } else {
-      __nv_bfloat16* out = ngt + static_cast<size_t>(ch) * D * D + f;
-      for (int cc = 0; cc < D; cc += 32) {
-        uint32_t v[32];
-        tmem_ld_x32(tb + lb + 128 + cc, v);
+      for (int u8 = 0; u8 < 32; u8 += 8) {
+        const int f0 = cc + u8;  // features f0 .. f0 + 7: one 16-byte chunk of K's row j
+        const uint32_t off =
+            (f0 >> 6) * 2 * kHalf + j * 128 + ((((f0 & 63) >> 3) ^ (j & 7)) << 4);
+        const uint4 kq = *reinterpret_cast<const uint4*>(kt + off);
+        const uint32_t kw[4] = {kq.x, kq.y, kq.z, kq.w};
+        uint32_t o[4];
 #pragma unroll
-        for (int u = 0; u < 32; ++u)
-          out[static_cast<size_t>(cc + u) * D] = __float2bfloat16_rn(-__uint_as_float(v[u]));
+        for (int e = 0; e < 4; ++e)
+          o[e] = pack_bf16x2(__uint_as_float(kw[e] << 16) - __uint_as_float(v[u8 + 2 * e]),
+                             __uint_as_float(kw[e] & 0xffff0000u) -
+                                 __uint_as_float(v[u8 + 2 * e + 1]));
+        out[f0 / 8] = make_uint4(o[0], o[1], o[2], o[3]);
       }
+    }
+  } else if (row < D) {
+    const int n = row;
+    uint4* out = reinterpret_cast<uint4*>(ngt + (static_cast<size_t>(ch) * D + n) * D);
+    for (int cc = 0; cc < D; cc += 32) {
+      uint32_t v[32];
+      tmem_ld_x32(tb + lb + 128 + cc, v);
+#pragma unroll
+      for (int u8 = 0; u8 < 32; u8 += 8)
+        out[(cc + u8) / 8] =
+            make_uint4(pack_bf16x2(-__uint_as_float(v[u8]), -__uint_as_float(v[u8 + 1])),
+                       pack_bf16x2(-__uint_as_float(v[u8 + 2]), -__uint_as_float(v[u8 + 3])),
+                       pack_bf16x2(-__uint_as_float(v[u8 + 4]), -__uint_as_float(v[u8 + 5])),
+                       pack_bf16x2(-__uint_as_float(v[u8 + 6]), -__uint_as_float(v[u8 + 7])));
     }
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
