@@ -94,9 +94,11 @@ def _chunk_backward(W, K, Q, beta, f, dQl, dKr, dF, dAdiag):
     return dQ, dK, dW, dbeta
 
 
-def path_chunked_bwd(q, k, v, w, beta, dout, C, logf=None, scale=None):
-    """Gradients (dq, dk, dv, dw, dbeta[, dlogf]) of sum(out * dout) for one
-    head by the blockwise backward; q, k, v, w: [T, d]; beta, logf: [T]."""
+def path_chunked_bwd(q, k, v, w, beta, dout, C, logf=None, scale=None, dlse=None):
+    """Gradients (dq, dk, dv, dw, dbeta[, dlogf]) of sum(out * dout)
+    (+ sum(lse * dlse)) for one head by the blockwise backward; q, k, v, w:
+    [T, d]; beta, logf, dlse: [T].  lse_i = log sum_j exp(S_ij), so its
+    gradient adds dlse_i P_ij to dS_ij."""
     q, k, v, w, dout = (np.asarray(x, np.float64) for x in (q, k, v, w, dout))
     beta = np.asarray(beta, np.float64)
     T, d = q.shape
@@ -133,6 +135,8 @@ def path_chunked_bwd(q, k, v, w, beta, dout, C, logf=None, scale=None):
     O = P @ vp
     dP = dop @ vp.T
     Dr = (dop * O).sum(axis=1, keepdims=True)
+    if dlse is not None:
+        Dr = Dr - pad_to_chunks(np.asarray(dlse, np.float64), T, C)[:, None]
     dS = P * (dP - Dr)                       # gradient of the log-weights
     dv = P.T @ dop
     # attention side
