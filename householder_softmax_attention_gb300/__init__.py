@@ -23,6 +23,7 @@ __all__ = [
     "PathAttnError", "load_library", "path_attn_fwd", "path_attn_fwd_host",
     "path_attn_fwd_noalloc", "path_attn_debug_wait_timeout", "path_attn_prefill",
     "path_attn_decode_step", "DecodeCache", "path_attn_fwd_partial", "path_producer_fwd",
+    "path_attn_bwd", "path_attn_bwd_workspace_bytes",
     "path_attn_debug_factors", "path_attn_device_status", "path_attn_workspace_bytes",
     "path_attn_chunk_size", "path_attn_launches_per_call", "path_attn_timing_enable",
     "path_attn_timing_read", "path_attn_version", "path_attn_status_string",
@@ -110,6 +111,12 @@ def load_library(path: str | None = None):
         lib.path_attn_decode_step.argtypes = [vp, vp, vp, vp, fp, fp, f, fp, vp, fp, vp, i,
                                               vp, fp, i, i, i, i, i, vp]
         lib.path_attn_decode_step.restype = i
+        lib.path_attn_bwd.argtypes = [vp, vp, vp, vp, fp, fp, f, vp, fp, vp, fp, vp, vp, vp, vp,
+                                      fp, fp, i, i, i, i, i, vp]
+        lib.path_attn_bwd.restype = i
+        lib.path_attn_bwd_workspace_bytes.argtypes = [i, i, i, i, i, i,
+                                                      ctypes.POINTER(ctypes.c_size_t)]
+        lib.path_attn_bwd_workspace_bytes.restype = i
         _lib = lib
         return lib
 
@@ -259,6 +266,51 @@ def path_attn_fwd_partial(q, k, v, u, beta, logf=None, scale=None, out=None, lse
                                        B, H, T, d, r, _dtype_code(q), ctypes.c_void_p(st.cuda_stream))
     _check(rc, "path_attn_fwd_partial")
     return out, lse
+
+
+def path_attn_bwd(q, k, v, w, beta, out, lse, dout, logf=None, scale=None, dlse=None,
+                  grads=None, stream=None):
+    """Gradients of a ``path_attn_fwd`` call on CUDA tensors.
+
+    ``out`` and ``lse`` are the forward's results; ``dout [B, H, T, d]`` (q's
+    dtype) and ``dlse [B, H, T]`` (float32, optional) are the gradients of the
+    loss with respect to them.  Returns ``(dq, dk, dv, dw, dbeta, dlogf)``;
+    dlogf is None without a gate.  ``grads`` may supply that tuple of output
+    tensors to be written in place."""
+    import torch
+    lib = load_library()
+    _check_inputs(q, k, v, w, beta, logf, True)
+    B, H, T, d = q.shape
+    for name, t, shape, dt in (("out", out, q.shape, q.dtype), ("dout", dout, q.shape, q.dtype),
+                               ("lse", lse, q.shape[:-1], torch.float32),
+                               ("dlse", dlse, q.shape[:-1], torch.float32)):
+        if t is None and name == "dlse":
+            continue
+        if (t is None or t.shape != shape or t.dtype != dt or not t.is_contiguous()
+                or t.device != q.device):
+            raise ValueError(f"{name} must be a contiguous {dt} {tuple(shape)} tensor on q's device")
+    if scale is None:
+        scale = d ** -0.5
+    if grads is None:
+        grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(w),
+                 torch.empty_like(beta), torch.empty_like(logf) if logf is not None else None)
+    dq, dk, dv, dw, dbeta, dlogf = grads
+    st = stream if stream is not None else torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        rc = lib.path_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(beta), _ptr(logf),
+                               float(scale), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dlse),
+                               _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dw), _ptr(dbeta), _ptr(dlogf),
+                               B, H, T, d, _dtype_code(q), ctypes.c_void_p(st.cuda_stream))
+    _check(rc, "path_attn_bwd")
+    return dq, dk, dv, dw, dbeta, dlogf
+
+
+def path_attn_bwd_workspace_bytes(B, H, T, d, dtype_code, with_gate=False) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load_library().path_attn_bwd_workspace_bytes(B, H, T, d, dtype_code, int(with_gate),
+                                                        ctypes.byref(n)),
+           "path_attn_bwd_workspace_bytes")
+    return n.value
 
 
 def path_producer_fwd(x, Wd, Wu, cw, Ub, bb, H, d, w=None, beta=None, stream=None):

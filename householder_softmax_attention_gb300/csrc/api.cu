@@ -216,6 +216,67 @@ int path_attn_fwd(const void* q, const void* k, const void* v, const void* w,
   return rc;
 }
 
+int path_attn_bwd_workspace_bytes(int B, int H, int T, int d, int dtype, int with_gate,
+                                  size_t* bytes) {
+  if (!bytes) return PATH_ERR_INVALID_ARG;
+  Geom g;
+  const int rc = make_geom(B, H, T, d, dtype, with_gate != 0, &g);
+  if (rc != PATH_OK) return rc;
+  *bytes = workspace_layout(g, nullptr, nullptr) + bwd_workspace_layout(g, nullptr, nullptr, nullptr);
+  return PATH_OK;
+}
+
+int path_attn_bwd(const void* q, const void* k, const void* v, const void* w,
+                  const float* beta, const float* logf, float scale, const void* out,
+                  const float* lse, const void* dout, const float* dlse, void* dq, void* dk,
+                  void* dv, void* dw, float* dbeta, float* dlogf, int B, int H, int T, int d,
+                  int dtype, void* stream) {
+  if (!q || !k || !v || !w || !beta || !out || !lse || !dout || !dq || !dk || !dv || !dw ||
+      !dbeta)
+    return PATH_ERR_INVALID_ARG;
+  if ((logf != nullptr) != (dlogf != nullptr)) return PATH_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, w, beta, out, lse, dout, dq, dk, dv, dw, dbeta};
+  for (const void* x : ptrs)
+    if (!aligned16(x)) return PATH_ERR_INVALID_ARG;
+  if ((logf && !aligned16(logf)) || (dlogf && !aligned16(dlogf)) || (dlse && !aligned16(dlse)))
+    return PATH_ERR_INVALID_ARG;
+  if (!(scale == scale)) return PATH_ERR_INVALID_ARG;
+  Geom g;
+  int rc = make_geom(B, H, T, d, dtype, logf != nullptr, &g);
+  if (rc != PATH_OK) return rc;
+  DeviceState* s = nullptr;
+  if ((rc = device_state(&s)) != PATH_OK) return rc;
+  if ((rc = check_device(s)) != PATH_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t fwd_bytes = workspace_layout(g, nullptr, nullptr);
+  const size_t bytes = fwd_bytes + bwd_workspace_layout(g, nullptr, nullptr, nullptr);
+  char* base = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&base), bytes, s->pool, st);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  Workspace ws;
+  workspace_layout(g, base, &ws);
+  BwdParams p;
+  ChunkBufs cb;
+  bwd_workspace_layout(g, base + fwd_bytes, &p, &cb);
+  Inputs in{q, k, v, w, beta, logf, scale, nullptr, nullptr};
+  e = launch_prep(g, in, ws, s->status, st, nullptr);
+  if (e == cudaSuccess) {
+    p.q = q; p.k = k; p.v = v; p.w = w; p.out = out; p.dout = dout;
+    p.beta = beta; p.lse = lse; p.dlse = dlse;
+    p.scale = scale; p.scale_log2e = scale * kLog2e;
+    p.dq = dq; p.dk = dk; p.dv = dv; p.dw = dw; p.dbeta = dbeta; p.dlogf = dlogf;
+    p.kr = ws.kr; p.ql = ws.ql; p.ngt = ws.ngt; p.sdt = ws.sdt;
+    p.lam2 = g.gate ? ws.lam2 : nullptr;
+    p.BH = g.BH; p.T = g.T; p.Tp = g.Tp; p.Np = g.Np; p.C = g.C; p.d = g.d; p.nch = g.nch;
+    p.bf16 = g.bf16;
+    e = launch_bwd(p, cb, st);
+  }
+  if (e != cudaSuccess) rc = set_cuda_error(e);
+  e = cudaFreeAsync(base, st);
+  if (rc == PATH_OK && e != cudaSuccess) rc = set_cuda_error(e);
+  return rc;
+}
+
 int path_attn_fwd_partial(const void* q, const void* k, const void* v, const void* w,
                           const float* beta, const float* logf, float scale, void* out,
                           float* lse, int B, int H, int T, int d, int r, int dtype, void* stream) {

@@ -1,0 +1,712 @@
+// bwd.cu -- backward pass of PaTH / PaTH-FoX attention (gradients of the
+// outputs with respect to q, k, v, w, beta and log f).
+//
+// The pages time the forward and the backward together ("PaTH Attention:
+// Position Encoding via Accumulating Householder Transformations", OpenReview
+// discussion, section "Efficiency Evaluation") but spell out only the
+// forward; the backward below is the derivative of the blockwise forward of
+// the slides ("A triangular representation makes paths computable", "A
+// right-to-left scan accumulates cross-block paths").  Per head, with chunks
+// c < b, F_c = H_{first(c)} ... H_{last(c)} = I + ngt_c and
+//   X_b^(b-1) = Ql_b,   X_b^(c-1) = X_b^(c) F_c^T        (query b crossing c)
+//   S_bc = scale X_b^(c) Kr_c^T + gate,   S_bb = scale Adiag_b + gate.
+// With dS = P (dP - D), D_i = dO_i . O_i - dlse_i:
+//   dV_c  = sum_{b>=c} P_bc^T dO_b
+//   dKr_c = scale sum_{b>c} dS_bc^T X_b^(c)
+//   G_b^(c) = scale dS_bc Kr_c + G_b^(c-1) F_c  (c = 0 .. b-1),  dQl_b = G_b^(b-1)
+//   dF_c  = sum_{b>c} G_b^(c-1)^T X_b^(c)
+//   dAdiag_b = scale lower(dS_bb)
+// and the chunk factors (UT transform) are differentiated chunk by chunk.
+//
+// Kernels (all fp32 arithmetic on the CUDA cores):
+//   rowdot        D_i, and lse in the log2 domain
+//   query walk    one warp per query row: walks X down (c = b-1 .. 0), storing
+//                 X_b^(c); walks back up accumulating G, storing G_b^(c-1);
+//                 writes dQl.  X and G are stored per (b, c) pair.
+//   key pass      one warp per key row: the diagonal chunk from the prepared
+//                 intra-chunk logits, then every later query chunk from the
+//                 stored X: dV, dKr, lower(dS_cc), column sums of dS
+//   dF            dF_c = sum_b G^T X over the stored pairs
+//   chunk pass    batched GEMMs through the UT factors to dQ, dK, dW, dbeta
+//   gate          dlog f_t = sum_{s >= t} (rowsum_s dS - colsum_s dS)
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace pathattn {
+namespace {
+
+using bf16 = __nv_bfloat16;
+
+__device__ __forceinline__ float ldf(const float* p) { return *p; }
+__device__ __forceinline__ float ldf(const bf16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void stf(float* p, float x) { *p = x; }
+__device__ __forceinline__ void stf(bf16* p, float x) { *p = __float2bfloat16_rn(x); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ size_t pair_index(int b, int c) {
+  return static_cast<size_t>(b) * (b - 1) / 2 + c;
+}
+
+constexpr int kRowWarps = 8;
+
+// ------------------------------------------------------------------- rowdot
+template <typename ET, int D>
+__global__ void __launch_bounds__(kRowWarps * 32) bwd_rowdot_kernel(BwdParams p) {
+  constexpr int E = D / 32;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int bh = blockIdx.y, t = blockIdx.x * kRowWarps + warp;
+  if (t >= p.Tp) return;
+  const size_t r = static_cast<size_t>(bh) * p.Tp + t;
+  if (t >= p.T) {
+    if (lane == 0) {
+      p.dvec[r] = 0.f;
+      p.lse2[r] = 0.f;
+    }
+    return;
+  }
+  const size_t row = (static_cast<size_t>(bh) * p.T + t) * D;
+  const ET* o = static_cast<const ET*>(p.out) + row;
+  const ET* go = static_cast<const ET*>(p.dout) + row;
+  float s = 0.f;
+#pragma unroll
+  for (int e = 0; e < E; ++e) s = fmaf(ldf(o + lane + 32 * e), ldf(go + lane + 32 * e), s);
+  s = warp_sum(s);
+  if (lane == 0) {
+    const size_t it = static_cast<size_t>(bh) * p.T + t;
+    p.dvec[r] = s - (p.dlse ? p.dlse[it] : 0.f);
+    p.lse2[r] = p.lse[it] * kLog2e;
+  }
+}
+
+// --------------------------------------------------------------- query walk
+template <typename ET, int D>
+__global__ void __launch_bounds__(kRowWarps * 32) bwd_query_kernel(BwdParams p) {
+  constexpr int E = D / 32;
+  __shared__ float sz[kRowWarps][D];
+  __shared__ float sg[kRowWarps][D];
+  __shared__ float sdo[kRowWarps][D];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int bh = blockIdx.y, t = blockIdx.x * kRowWarps + warp;
+  if (t >= p.Tp) return;  // warp-uniform; no block-wide barrier follows
+  const int C = p.C, b = t / C, i = t - b * C;
+  const size_t chb = static_cast<size_t>(bh) * p.Np + b;
+  if (t >= p.T) {  // padded query: no gradient
+#pragma unroll
+    for (int e = 0; e < E; ++e) p.dql[(chb * C + i) * D + lane + 32 * e] = 0.f;
+    return;
+  }
+  const ET* kr = static_cast<const ET*>(p.kr);
+  const ET* ngt = static_cast<const ET*>(p.ngt);
+  const ET* vv = static_cast<const ET*>(p.v) + static_cast<size_t>(bh) * p.T * D;
+  ET* xs = static_cast<ET*>(p.xs) + static_cast<size_t>(bh) * p.npairs * C * D;
+  ET* gs = static_cast<ET*>(p.gs) + static_cast<size_t>(bh) * p.npairs * C * D;
+  float* z = sz[warp];
+  float* gg = sg[warp];
+  float* dor = sdo[warp];
+  const ET* go = static_cast<const ET*>(p.dout) + (static_cast<size_t>(bh) * p.T + t) * D;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    dor[lane + 32 * e] = ldf(go + lane + 32 * e);
+    z[lane + 32 * e] = p.ql[(chb * C + i) * D + lane + 32 * e];
+  }
+  __syncwarp();
+  // walk down: store X_b^(c) as the element type, then cross chunk c
+  for (int c = b - 1; c >= 0; --c) {
+    ET* xr = xs + (pair_index(b, c) * C + i) * D;
+#pragma unroll
+    for (int e = 0; e < E; ++e) stf(xr + lane + 32 * e, z[lane + 32 * e]);
+    if (c == 0) break;
+    const ET* G = ngt + (static_cast<size_t>(bh) * p.Np + c) * D * D;
+    float zn[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int n = lane + 32 * e;
+      float acc = z[n];
+      for (int kk = 0; kk < D; ++kk) acc = fmaf(z[kk], ldf(G + n * D + kk), acc);
+      zn[e] = acc;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int e = 0; e < E; ++e) z[lane + 32 * e] = zn[e];
+    __syncwarp();
+  }
+  // walk up: G_b^(c) = scale dS_bc Kr_c + G_b^(c-1) F_c
+  const size_t rt = static_cast<size_t>(bh) * p.Tp + t;
+  const float lse2 = p.lse2[rt], Dv = p.dvec[rt];
+  const float lrow = p.lam2 ? p.lam2[rt] : 0.f;
+  // row sum of dS over the diagonal chunk (keys j <= i)
+  float rs = 0.f;
+  for (int j0 = 0; j0 <= i; j0 += 32) {
+    const int j = j0 + lane;
+    if (j <= i) {
+      const float pr = exp2f(p.sdt[(chb * C + j) * C + i] - lse2);
+      const ET* vj = vv + static_cast<size_t>(b * C + j) * D;
+      float dp = 0.f;
+      for (int m = 0; m < D; ++m) dp = fmaf(dor[m], ldf(vj + m), dp);
+      rs += pr * (dp - Dv);
+    }
+  }
+  float g[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) g[e] = 0.f;
+  for (int c = 0; c < b; ++c) {
+    const ET* xr = xs + (pair_index(b, c) * C + i) * D;
+    __syncwarp();
+#pragma unroll
+    for (int e = 0; e < E; ++e) z[lane + 32 * e] = ldf(xr + lane + 32 * e);
+    __syncwarp();
+    const size_t chc = static_cast<size_t>(bh) * p.Np + c;
+    float gn[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) gn[e] = 0.f;
+    for (int j0 = 0; j0 < C; j0 += 32) {
+      const int j = j0 + lane;
+      const ET* kj = kr + (chc * C + j) * D;
+      const ET* vj = vv + static_cast<size_t>(c * C + j) * D;
+      float s = 0.f, dp = 0.f;
+      for (int m = 0; m < D; ++m) {
+        s = fmaf(z[m], ldf(kj + m), s);
+        dp = fmaf(dor[m], ldf(vj + m), dp);
+      }
+      float s2 = s * p.scale_log2e;
+      if (p.lam2) s2 += lrow - p.lam2[static_cast<size_t>(bh) * p.Tp + c * C + j];
+      const float pr = exp2f(s2 - lse2);
+      const float ds = pr * (dp - Dv);
+      rs += ds;
+      for (int u = 0; u < 32; ++u) {
+        const float du = __shfl_sync(0xffffffffu, ds, u);
+        const ET* ku = kr + (chc * C + j0 + u) * D;
+#pragma unroll
+        for (int e = 0; e < E; ++e) gn[e] = fmaf(du, ldf(ku + lane + 32 * e), gn[e]);
+      }
+    }
+    if (c >= 1) {
+      ET* gr = gs + (pair_index(b, c) * C + i) * D;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        stf(gr + lane + 32 * e, g[e]);
+        gg[lane + 32 * e] = g[e];
+      }
+      __syncwarp();
+      const ET* G = ngt + chc * D * D;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const int n = lane + 32 * e;
+        float acc = g[e];
+        for (int kk = 0; kk < D; ++kk) acc = fmaf(gg[kk], ldf(G + kk * D + n), acc);
+        g[e] = acc + p.scale * gn[e];
+      }
+      __syncwarp();
+    } else {
+#pragma unroll
+      for (int e = 0; e < E; ++e) g[e] = p.scale * gn[e];
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) p.dql[(chb * C + i) * D + lane + 32 * e] = g[e];
+  rs = warp_sum(rs);
+  if (lane == 0) p.rowsum[rt] = rs;
+}
+
+// ----------------------------------------------------------------- key pass
+template <typename ET, int D>
+__global__ void __launch_bounds__(kRowWarps * 32) bwd_key_kernel(BwdParams p) {
+  constexpr int E = D / 32;
+  __shared__ float skr[kRowWarps][D];
+  __shared__ float sv[kRowWarps][D];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int bh = blockIdx.y, t = blockIdx.x * kRowWarps + warp;
+  if (t >= p.Tp) return;
+  const int C = p.C, c = t / C, jj = t - c * C;
+  const size_t chc = static_cast<size_t>(bh) * p.Np + c;
+  float* dkr = p.dkr + (chc * C + jj) * D;
+  if (t >= p.T) {  // padded key: no gradient
+#pragma unroll
+    for (int e = 0; e < E; ++e) dkr[lane + 32 * e] = 0.f;
+    return;
+  }
+  const ET* kr = static_cast<const ET*>(p.kr);
+  const ET* vv = static_cast<const ET*>(p.v) + static_cast<size_t>(bh) * p.T * D;
+  const ET* go = static_cast<const ET*>(p.dout) + static_cast<size_t>(bh) * p.T * D;
+  const ET* xs = static_cast<const ET*>(p.xs) + static_cast<size_t>(bh) * p.npairs * C * D;
+  float* kj = skr[warp];
+  float* vj = sv[warp];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    kj[lane + 32 * e] = ldf(kr + (chc * C + jj) * D + lane + 32 * e);
+    vj[lane + 32 * e] = ldf(vv + static_cast<size_t>(t) * D + lane + 32 * e);
+  }
+  __syncwarp();
+  const float* lam2 = p.lam2 ? p.lam2 + static_cast<size_t>(bh) * p.Tp : nullptr;
+  const float* lse2 = p.lse2 + static_cast<size_t>(bh) * p.Tp;
+  const float* dvec = p.dvec + static_cast<size_t>(bh) * p.Tp;
+  const float lcol = lam2 ? lam2[t] : 0.f;
+  float dv[E], dk[E], cs = 0.f;
+#pragma unroll
+  for (int e = 0; e < E; ++e) dv[e] = dk[e] = 0.f;
+  // diagonal chunk: queries i >= jj
+  for (int i0 = jj; i0 < C; i0 += 32) {
+    const int i = i0 + lane, tq = c * C + i;
+    const bool ok = i < C && tq < p.T;
+    float pr = 0.f, ds = 0.f;
+    if (ok) {
+      const float s2 = p.sdt[(chc * C + jj) * C + i];
+      pr = exp2f(s2 - lse2[tq]);
+      const ET* gr = go + static_cast<size_t>(tq) * D;
+      float dp = 0.f;
+      for (int m = 0; m < D; ++m) dp = fmaf(ldf(gr + m), vj[m], dp);
+      ds = pr * (dp - dvec[tq]);
+      p.dad[(chc * C + i) * C + jj] = p.scale * ds;
+    }
+    cs += ds;
+    const int n = min(32, min(C, p.T - c * C) - i0);
+    for (int u = 0; u < n; ++u) {
+      const float pu = __shfl_sync(0xffffffffu, pr, u);
+      const ET* gr = go + static_cast<size_t>(c * C + i0 + u) * D;
+#pragma unroll
+      for (int e = 0; e < E; ++e) dv[e] = fmaf(pu, ldf(gr + lane + 32 * e), dv[e]);
+    }
+  }
+  // later chunks from the stored walked queries
+  for (int b = c + 1; b < p.Np; ++b) {
+    const ET* xb = xs + pair_index(b, c) * C * D;
+    for (int i0 = 0; i0 < C; i0 += 32) {
+      if (b * C + i0 >= p.T) break;
+      const int i = i0 + lane, tq = b * C + i;
+      const bool ok = tq < p.T;
+      float pr = 0.f, ds = 0.f;
+      if (ok) {
+        const ET* xr = xb + static_cast<size_t>(i) * D;
+        const ET* gr = go + static_cast<size_t>(tq) * D;
+        float s = 0.f, dp = 0.f;
+        for (int m = 0; m < D; ++m) {
+          s = fmaf(ldf(xr + m), kj[m], s);
+          dp = fmaf(ldf(gr + m), vj[m], dp);
+        }
+        float s2 = s * p.scale_log2e;
+        if (lam2) s2 += lam2[tq] - lcol;
+        pr = exp2f(s2 - lse2[tq]);
+        ds = pr * (dp - dvec[tq]);
+      }
+      cs += ds;
+      const int n = min(32, p.T - (b * C + i0));
+      for (int u = 0; u < n; ++u) {
+        const float pu = __shfl_sync(0xffffffffu, pr, u);
+        const float du = __shfl_sync(0xffffffffu, ds, u) * p.scale;
+        const ET* gr = go + static_cast<size_t>(b * C + i0 + u) * D;
+        const ET* xr = xb + static_cast<size_t>(i0 + u) * D;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          dv[e] = fmaf(pu, ldf(gr + lane + 32 * e), dv[e]);
+          dk[e] = fmaf(du, ldf(xr + lane + 32 * e), dk[e]);
+        }
+      }
+    }
+  }
+  cs = warp_sum(cs);
+  ET* dvo = static_cast<ET*>(p.dv) + (static_cast<size_t>(bh) * p.T + t) * D;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    stf(dvo + lane + 32 * e, dv[e]);
+    dkr[lane + 32 * e] = dk[e];
+  }
+  if (lane == 0) p.colsum[static_cast<size_t>(bh) * p.Tp + t] = cs;
+}
+
+// --------------------------------------------------------------------- dF
+// dF_c = sum_{b>c} G_b^(c-1)^T X_b^(c); one block per chunk, thread-owned
+// output entries, rows staged through shared memory 32 at a time.
+template <typename ET, int D>
+__global__ void __launch_bounds__(256) bwd_dF_kernel(BwdParams p) {
+  constexpr int R = 32;
+  constexpr int PER = D * D / 256;
+  __shared__ float sgr[R][D];
+  __shared__ float sxr[R][D];
+  const int ch = blockIdx.x, bh = ch / p.Np, c = ch - bh * p.Np;
+  const int C = p.C;
+  const ET* xs = static_cast<const ET*>(p.xs) + static_cast<size_t>(bh) * p.npairs * C * D;
+  const ET* gs = static_cast<const ET*>(p.gs) + static_cast<size_t>(bh) * p.npairs * C * D;
+  float acc[PER];
+#pragma unroll
+  for (int u = 0; u < PER; ++u) acc[u] = 0.f;
+  if (c >= 1) {
+    for (int b = c + 1; b < p.Np; ++b) {
+      const size_t base = pair_index(b, c) * C * D;
+      const int rows = min(C, p.T - b * C);
+      for (int r0 = 0; r0 < rows; r0 += R) {
+        __syncthreads();
+        for (int x = threadIdx.x; x < R * D; x += 256) {
+          const int rr = x / D, cc = x % D;
+          const bool ok = r0 + rr < rows;
+          sgr[rr][cc] = ok ? ldf(gs + base + static_cast<size_t>(r0 + rr) * D + cc) : 0.f;
+          sxr[rr][cc] = ok ? ldf(xs + base + static_cast<size_t>(r0 + rr) * D + cc) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+          const int o = threadIdx.x + 256 * u, e = o / D, f = o % D;
+          float a = acc[u];
+          for (int rr = 0; rr < R; ++rr) a = fmaf(sgr[rr][e], sxr[rr][f], a);
+          acc[u] = a;
+        }
+      }
+    }
+  }
+  float* out = p.dF + static_cast<size_t>(ch) * D * D;
+#pragma unroll
+  for (int u = 0; u < PER; ++u) out[threadIdx.x + 256 * u] = acc[u];
+}
+
+// ---------------------------------------------------------- chunk helpers
+// fp32 copies of w, k, q (zero rows past T) and beta (zero past T), per chunk
+template <typename ET>
+__global__ void bwd_chunk_inputs_kernel(BwdParams p, ChunkBufs cb) {
+  const size_t total = static_cast<size_t>(p.BH) * p.Tp * p.d;
+  for (size_t x = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; x < total;
+       x += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t row = x / p.d;
+    const int e = static_cast<int>(x % p.d);
+    const int bh = static_cast<int>(row / p.Tp), t = static_cast<int>(row % p.Tp);
+    const bool ok = t < p.T;
+    const size_t src = (static_cast<size_t>(bh) * p.T + t) * p.d + e;
+    cb.Wf[x] = ok ? ldf(static_cast<const ET*>(p.w) + src) : 0.f;
+    cb.Kf[x] = ok ? ldf(static_cast<const ET*>(p.k) + src) : 0.f;
+    cb.Qf[x] = ok ? ldf(static_cast<const ET*>(p.q) + src) : 0.f;
+    if (e == 0) cb.bf[row] = ok ? p.beta[static_cast<size_t>(bh) * p.T + t] : 0.f;
+  }
+}
+
+// Batched C = mask(alpha op(A) op(B) + (acc ? C : 0)); 64 x 64 tiles, 4 x 4
+// per thread.  op(A)(m, k) = tA ? A[k][m] : A[m][k]; op(B)(k, n) = tB ? B[n][k] : B[k][n].
+// mask 0: none, 1: m >= n kept, 2: m > n kept (others written as 0).
+struct GemmArg {
+  const float* A;
+  const float* B;
+  float* Cm;
+  long long sA, sB, sC;
+  int lda, ldb, ldc, M, N, K, batch, mask;
+  bool tA, tB, acc;
+  float alpha;
+};
+
+__global__ void __launch_bounds__(256) gemm_batched_kernel(GemmArg g) {
+  __shared__ float As[16][64 + 4];
+  __shared__ float Bs[16][64 + 4];
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+  for (int z = blockIdx.z; z < g.batch; z += gridDim.z) {
+    const float* A = g.A + z * g.sA;
+    const float* B = g.B + z * g.sB;
+    float* Cm = g.Cm + z * g.sC;
+    float acc[4][4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int s = 0; s < 4; ++s) acc[r][s] = 0.f;
+    for (int k0 = 0; k0 < g.K; k0 += 16) {
+      __syncthreads();
+      for (int x = threadIdx.x; x < 1024; x += 256) {
+        int mm, kk;
+        if (g.tA) { kk = x / 64; mm = x % 64; } else { mm = x / 16; kk = x % 16; }
+        As[kk][mm] = g.tA ? A[static_cast<size_t>(k0 + kk) * g.lda + m0 + mm]
+                          : A[static_cast<size_t>(m0 + mm) * g.lda + k0 + kk];
+        int nn, kb;
+        if (g.tB) { nn = x / 16; kb = x % 16; } else { kb = x / 64; nn = x % 64; }
+        Bs[kb][nn] = g.tB ? B[static_cast<size_t>(n0 + nn) * g.ldb + k0 + kb]
+                          : B[static_cast<size_t>(k0 + kb) * g.ldb + n0 + nn];
+      }
+      __syncthreads();
+#pragma unroll
+      for (int kk = 0; kk < 16; ++kk) {
+        float a[4], bv[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) a[r] = As[kk][ty * 4 + r];
+#pragma unroll
+        for (int s = 0; s < 4; ++s) bv[s] = Bs[kk][tx * 4 + s];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int s = 0; s < 4; ++s) acc[r][s] = fmaf(a[r], bv[s], acc[r][s]);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        const int m = m0 + ty * 4 + r, n = n0 + tx * 4 + s;
+        float* cp = Cm + static_cast<size_t>(m) * g.ldc + n;
+        float v = g.alpha * acc[r][s] + (g.acc ? *cp : 0.f);
+        if ((g.mask == 1 && m < n) || (g.mask == 2 && m <= n)) v = 0.f;
+        *cp = v;
+      }
+  }
+}
+
+// Xi = (I + Lm)^{-1} for unit lower triangular I + Lm: forward substitution,
+// one thread per column.
+__global__ void bwd_tri_inv_kernel(const float* Lm, float* Xi, int C) {
+  extern __shared__ float sl[];
+  const int ch = blockIdx.x;
+  const float* L = Lm + static_cast<size_t>(ch) * C * C;
+  float* X = Xi + static_cast<size_t>(ch) * C * C;
+  for (int x = threadIdx.x; x < C * C; x += blockDim.x) sl[x] = L[x];
+  __syncthreads();
+  float* col = sl + C * C;  // [C][C] solution, column j owned by thread j
+  const int j = threadIdx.x;
+  if (j < C) {
+    for (int i = 0; i < C; ++i) {
+      float v = (i == j) ? 1.f : 0.f;
+      if (i > j)
+        for (int k = j; k < i; ++k) v = fmaf(-sl[i * C + k], col[k * C + j], v);
+      col[i * C + j] = v;
+    }
+  }
+  __syncthreads();
+  for (int x = threadIdx.x; x < C * C; x += blockDim.x) X[x] = col[x];
+}
+
+// Elementwise steps of the chunk pass, one block per chunk.
+//  op 0: Lm  = strictLower(beta_i GWW_ij)
+//  op 1: U   = Xi diag(beta)  (and dXi = dU diag(beta) when `in2` is dU)
+//  op 2: BL  = diag(beta) dLm
+__global__ void bwd_chunk_elem_kernel(const float* in, float* out, const float* bf, int C, int op) {
+  const int ch = blockIdx.x;
+  const float* a = in + static_cast<size_t>(ch) * C * C;
+  float* o = out + static_cast<size_t>(ch) * C * C;
+  const float* be = bf + static_cast<size_t>(ch) * C;
+  for (int x = threadIdx.x; x < C * C; x += blockDim.x) {
+    const int i = x / C, j = x % C;
+    float v;
+    if (op == 0) v = i > j ? be[i] * a[x] : 0.f;
+    else if (op == 1) v = a[x] * be[j];
+    else v = be[i] * a[x];
+    o[x] = v;
+  }
+}
+
+// dbeta_j = sum_i Xi_ij dU_ij + sum_m dLm_jm GWW_jm
+__global__ void bwd_dbeta_kernel(const float* Xi, const float* dU, const float* dLm,
+                                 const float* GWW, float* dbf, int C) {
+  const int ch = blockIdx.x, j = threadIdx.x;
+  if (j >= C) return;
+  const size_t o = static_cast<size_t>(ch) * C * C;
+  float s = 0.f;
+  for (int i = 0; i < C; ++i) s = fmaf(Xi[o + i * C + j], dU[o + i * C + j], s);
+  for (int m = 0; m < C; ++m) s = fmaf(dLm[o + j * C + m], GWW[o + j * C + m], s);
+  dbf[static_cast<size_t>(ch) * C + j] = s;
+}
+
+template <typename ET>
+__global__ void bwd_chunk_outputs_kernel(BwdParams p, ChunkBufs cb) {
+  const size_t total = static_cast<size_t>(p.BH) * p.T * p.d;
+  for (size_t x = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; x < total;
+       x += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t row = x / p.d;
+    const int e = static_cast<int>(x % p.d);
+    const int bh = static_cast<int>(row / p.T), t = static_cast<int>(row % p.T);
+    const size_t src = (static_cast<size_t>(bh) * p.Tp + t) * p.d + e;
+    stf(static_cast<ET*>(p.dq) + x, cb.dQf[src]);
+    stf(static_cast<ET*>(p.dk) + x, cb.dKf[src]);
+    stf(static_cast<ET*>(p.dw) + x, cb.dWf[src]);
+    if (e == 0) p.dbeta[row] = cb.dbf[static_cast<size_t>(bh) * p.Tp + t];
+  }
+}
+
+// dlog f_t = sum_{s >= t, s < T} (rowsum_s - colsum_s) of dS (the row sum
+// is dlse_s in exact arithmetic; taking both sums from the same dS keeps
+// dlog f_0 = 0, as it is exactly): one block per head,
+// tiles of 1024 walked from the end with a carried suffix sum.
+__global__ void __launch_bounds__(1024) bwd_gate_kernel(BwdParams p) {
+  __shared__ float wsum[32];
+  __shared__ float carry_s;
+  const int bh = blockIdx.x, lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  if (threadIdx.x == 0) carry_s = 0.f;
+  __syncthreads();
+  for (int end = p.T; end > 0; end -= 1024) {
+    // position end - 1 - threadIdx.x (reverse order, so a prefix scan is a suffix scan)
+    const int t = end - 1 - threadIdx.x;
+    float v = 0.f;
+    if (t >= 0) {
+      const size_t r = static_cast<size_t>(bh) * p.Tp + t;
+      v = p.rowsum[r] - p.colsum[r];
+    }
+    float x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      float w = wsum[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      wsum[lane] = w;
+    }
+    __syncthreads();
+    const float carry = carry_s;
+    const float incl = x + (warp > 0 ? wsum[warp - 1] : 0.f) + carry;
+    if (t >= 0) p.dlogf[static_cast<size_t>(bh) * p.T + t] = incl;
+    __syncthreads();
+    if (threadIdx.x == 0) carry_s = carry + wsum[31];
+    __syncthreads();
+  }
+}
+
+cudaError_t gemm(cudaStream_t st, int batch, int M, int N, int K, float alpha, const float* A,
+                 int lda, long long sA, bool tA, const float* B, int ldb, long long sB, bool tB,
+                 float* Cm, int ldc, long long sC, bool acc, int mask) {
+  GemmArg g{A, B, Cm, sA, sB, sC, lda, ldb, ldc, M, N, K, batch, mask, tA, tB, acc, alpha};
+  const dim3 grid(N / 64, M / 64, batch < 65535 ? batch : 65535);
+  gemm_batched_kernel<<<grid, 256, 0, st>>>(g);
+  return cudaGetLastError();
+}
+
+template <typename ET, int D>
+cudaError_t launch_bwd_t(const BwdParams& p, const ChunkBufs& cb, cudaStream_t st) {
+  const int C = p.C;
+  const dim3 rows_tp((p.Tp + kRowWarps - 1) / kRowWarps, p.BH);
+  bwd_rowdot_kernel<ET, D><<<rows_tp, kRowWarps * 32, 0, st>>>(p);
+  bwd_query_kernel<ET, D><<<rows_tp, kRowWarps * 32, 0, st>>>(p);
+  cudaError_t e = cudaMemsetAsync(p.dad, 0, static_cast<size_t>(p.nch) * C * C * 4, st);
+  if (e != cudaSuccess) return e;
+  bwd_key_kernel<ET, D><<<rows_tp, kRowWarps * 32, 0, st>>>(p);
+  bwd_dF_kernel<ET, D><<<p.nch, 256, 0, st>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // ---- chunk pass (fp32, batched over chunks)
+  const int nch = p.nch;
+  const long long cc = static_cast<long long>(C) * C, cd = static_cast<long long>(C) * D,
+                  dd = static_cast<long long>(D) * D;
+  bwd_chunk_inputs_kernel<ET><<<1024, 256, 0, st>>>(p, cb);
+  const float *W = cb.Wf, *K = cb.Kf, *Q = cb.Qf;
+  // forward factors
+  if ((e = gemm(st, nch, C, C, D, 1.f, W, D, cd, false, W, D, cd, true, cb.GWW, C, cc, false, 0)))
+    return e;
+  bwd_chunk_elem_kernel<<<nch, 256, 0, st>>>(cb.GWW, cb.Lm, cb.bf, C, 0);
+  const int tri_smem = 2 * C * C * static_cast<int>(sizeof(float));
+  if ((e = cudaFuncSetAttribute(bwd_tri_inv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                tri_smem)) != cudaSuccess)
+    return e;
+  bwd_tri_inv_kernel<<<nch, C, tri_smem, st>>>(cb.Lm, cb.Xi, C);
+  bwd_chunk_elem_kernel<<<nch, 256, 0, st>>>(cb.Xi, cb.U, cb.bf, C, 1);
+  if ((e = gemm(st, nch, C, C, D, 1.f, W, D, cd, false, K, D, cd, true, cb.Nm, C, cc, false, 2)) ||
+      (e = gemm(st, nch, C, C, C, 1.f, cb.U, C, cc, false, cb.Nm, C, cc, false, cb.TK, C, cc, false, 0)) ||
+      (e = gemm(st, nch, C, D, C, 1.f, cb.U, C, cc, false, W, D, cd, false, cb.UW, D, cd, false, 0)) ||
+      (e = gemm(st, nch, C, C, D, 1.f, Q, D, cd, false, W, D, cd, true, cb.Mm, C, cc, false, 1)))
+    return e;
+  const float *dQl = p.dql, *dKr = p.dkr, *dF = p.dF, *dA = p.dad;
+  // dM = -dQl UW^T - dA TK^T, dMl = lower(dM)
+  if ((e = gemm(st, nch, C, C, D, -1.f, dQl, D, cd, false, cb.UW, D, cd, true, cb.dM, C, cc, false, 0)) ||
+      (e = gemm(st, nch, C, C, C, -1.f, dA, C, cc, false, cb.TK, C, cc, true, cb.dM, C, cc, true, 1)))
+    return e;
+  // dQ = dQl + dA K + dMl W
+  if ((e = cudaMemcpyAsync(cb.dQf, dQl, static_cast<size_t>(nch) * cd * 4, cudaMemcpyDeviceToDevice, st)) ||
+      (e = gemm(st, nch, C, D, C, 1.f, dA, C, cc, false, K, D, cd, false, cb.dQf, D, cd, true, 0)) ||
+      (e = gemm(st, nch, C, D, C, 1.f, cb.dM, C, cc, false, W, D, cd, false, cb.dQf, D, cd, true, 0)))
+    return e;
+  // dTK = -W dKr^T - M^T dA ; dUW = -M^T dQl
+  if ((e = gemm(st, nch, C, C, D, -1.f, W, D, cd, false, dKr, D, cd, true, cb.dTK, C, cc, false, 0)) ||
+      (e = gemm(st, nch, C, C, C, -1.f, cb.Mm, C, cc, true, dA, C, cc, false, cb.dTK, C, cc, true, 0)) ||
+      (e = gemm(st, nch, C, D, C, -1.f, cb.Mm, C, cc, true, dQl, D, cd, false, cb.dUW, D, cd, false, 0)))
+    return e;
+  // dN = strictLower(U^T dTK); dK = dKr + dA^T Q + dN^T W
+  if ((e = gemm(st, nch, C, C, C, 1.f, cb.U, C, cc, true, cb.dTK, C, cc, false, cb.dN, C, cc, false, 2)) ||
+      (e = cudaMemcpyAsync(cb.dKf, dKr, static_cast<size_t>(nch) * cd * 4, cudaMemcpyDeviceToDevice, st)) ||
+      (e = gemm(st, nch, C, D, C, 1.f, dA, C, cc, true, Q, D, cd, false, cb.dKf, D, cd, true, 0)) ||
+      (e = gemm(st, nch, C, D, C, 1.f, cb.dN, C, cc, true, W, D, cd, false, cb.dKf, D, cd, true, 0)))
+    return e;
+  // P1 = W dF, P2 = W dF^T
+  if ((e = gemm(st, nch, C, D, D, 1.f, W, D, cd, false, dF, D, dd, false, cb.P1, D, cd, false, 0)) ||
+      (e = gemm(st, nch, C, D, D, 1.f, W, D, cd, false, dF, D, dd, true, cb.P2, D, cd, false, 0)))
+    return e;
+  // dU = -P2 W^T + dTK N^T + dUW W^T
+  if ((e = gemm(st, nch, C, C, D, -1.f, cb.P2, D, cd, false, W, D, cd, true, cb.dU, C, cc, false, 0)) ||
+      (e = gemm(st, nch, C, C, C, 1.f, cb.dTK, C, cc, false, cb.Nm, C, cc, true, cb.dU, C, cc, true, 0)) ||
+      (e = gemm(st, nch, C, C, D, 1.f, cb.dUW, D, cd, false, W, D, cd, true, cb.dU, C, cc, true, 0)))
+    return e;
+  // dW = -TK dKr - U P1 - U^T P2 + dMl^T Q + dN K + U^T dUW  (+ the Lm terms below)
+  if ((e = gemm(st, nch, C, D, C, -1.f, cb.TK, C, cc, false, dKr, D, cd, false, cb.dWf, D, cd, false, 0)) ||
+      (e = gemm(st, nch, C, D, C, -1.f, cb.U, C, cc, false, cb.P1, D, cd, false, cb.dWf, D, cd, true, 0)) ||
+      (e = gemm(st, nch, C, D, C, -1.f, cb.U, C, cc, true, cb.P2, D, cd, false, cb.dWf, D, cd, true, 0)) ||
+      (e = gemm(st, nch, C, D, C, 1.f, cb.dM, C, cc, true, Q, D, cd, false, cb.dWf, D, cd, true, 0)) ||
+      (e = gemm(st, nch, C, D, C, 1.f, cb.dN, C, cc, false, K, D, cd, false, cb.dWf, D, cd, true, 0)) ||
+      (e = gemm(st, nch, C, D, C, 1.f, cb.U, C, cc, true, cb.dUW, D, cd, false, cb.dWf, D, cd, true, 0)))
+    return e;
+  // dXi = dU diag(beta); T1 = Xi^T dXi; dLm = strictLower(-T1 Xi^T)
+  bwd_chunk_elem_kernel<<<nch, 256, 0, st>>>(cb.dU, cb.dXi, cb.bf, C, 1);
+  if ((e = gemm(st, nch, C, C, C, 1.f, cb.Xi, C, cc, true, cb.dXi, C, cc, false, cb.T1, C, cc, false, 0)) ||
+      (e = gemm(st, nch, C, C, C, -1.f, cb.T1, C, cc, false, cb.Xi, C, cc, true, cb.dLm, C, cc, false, 2)))
+    return e;
+  bwd_dbeta_kernel<<<nch, C, 0, st>>>(cb.Xi, cb.dU, cb.dLm, cb.GWW, cb.dbf, C);
+  // BL = diag(beta) dLm; dW += BL W + BL^T W
+  bwd_chunk_elem_kernel<<<nch, 256, 0, st>>>(cb.dLm, cb.BL, cb.bf, C, 2);
+  if ((e = gemm(st, nch, C, D, C, 1.f, cb.BL, C, cc, false, W, D, cd, false, cb.dWf, D, cd, true, 0)) ||
+      (e = gemm(st, nch, C, D, C, 1.f, cb.BL, C, cc, true, W, D, cd, false, cb.dWf, D, cd, true, 0)))
+    return e;
+  bwd_chunk_outputs_kernel<ET><<<1024, 256, 0, st>>>(p, cb);
+  if (p.dlogf) bwd_gate_kernel<<<p.BH, 1024, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t bwd_workspace_layout(const Geom& g, char* base, BwdParams* p, ChunkBufs* cb) {
+  const size_t es = g.bf16 ? 2 : 4;
+  const size_t nch = static_cast<size_t>(g.nch), C = g.C, d = g.d;
+  const size_t BH = g.BH, Tp = g.Tp;
+  const size_t npairs = static_cast<size_t>(g.Np) * (g.Np - 1) / 2;
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> char* {
+    char* q = base ? base + off : nullptr;
+    off = align_up(off + bytes, 256);
+    return q;
+  };
+  BwdParams b{};
+  b.dvec = reinterpret_cast<float*>(take(BH * Tp * 4));
+  b.lse2 = reinterpret_cast<float*>(take(BH * Tp * 4));
+  b.colsum = reinterpret_cast<float*>(take(BH * Tp * 4));
+  b.rowsum = reinterpret_cast<float*>(take(BH * Tp * 4));
+  b.xs = take(BH * npairs * C * d * es);
+  b.gs = take(BH * npairs * C * d * es);
+  b.dql = reinterpret_cast<float*>(take(nch * C * d * 4));
+  b.dkr = reinterpret_cast<float*>(take(nch * C * d * 4));
+  b.dF = reinterpret_cast<float*>(take(nch * d * d * 4));
+  b.dad = reinterpret_cast<float*>(take(nch * C * C * 4));
+  ChunkBufs c{};
+  float** cd_bufs[] = {&c.Wf, &c.Kf, &c.Qf, &c.UW, &c.dUW, &c.P1, &c.P2, &c.dQf, &c.dKf, &c.dWf};
+  for (float** q : cd_bufs) *q = reinterpret_cast<float*>(take(nch * C * d * 4));
+  float** cc_bufs[] = {&c.GWW, &c.Lm, &c.Xi, &c.U, &c.Nm, &c.TK, &c.Mm, &c.dM,
+                       &c.dTK, &c.dN, &c.dU, &c.dXi, &c.T1, &c.dLm, &c.BL};
+  for (float** q : cc_bufs) *q = reinterpret_cast<float*>(take(nch * C * C * 4));
+  c.bf = reinterpret_cast<float*>(take(nch * C * 4));
+  c.dbf = reinterpret_cast<float*>(take(nch * C * 4));
+  b.npairs = npairs;
+  if (p) *p = b;
+  if (cb) *cb = c;
+  return off;
+}
+
+cudaError_t launch_bwd(const BwdParams& p, const ChunkBufs& cb, cudaStream_t st) {
+  if (p.bf16) {
+    if (p.d == 64) return launch_bwd_t<bf16, 64>(p, cb, st);
+    return launch_bwd_t<bf16, 128>(p, cb, st);
+  }
+  if (p.d == 64) return launch_bwd_t<float, 64>(p, cb, st);
+  return launch_bwd_t<float, 128>(p, cb, st);
+}
+
+}  // namespace pathattn

@@ -153,6 +153,46 @@ cudaError_t launch_producer_proj_tc(const void* x, const void* Wd, const void* U
 // t < n_out (tokens at or past T add 0).
 cudaError_t launch_gate_prefix(const float* logf, float* out, int BH, int T, int n_out,
                                size_t out_stride, double mult, cudaStream_t st);
+// Backward pass (bwd.cu).  Geometry and pointers of one call; the forward
+// preparation's workspace (kr, ql, ngt, sdt, lam2) comes first, then, from
+// bwd_workspace_layout:
+//   dvec, lse2, colsum, rowsum [bh][Tp] f32   D_i = dO_i . O_i - dlse_i,
+//                                     lse log2(e), column and row sums of dS
+//   xs, gs [bh][pair][C][d] elem      X_b^(c) and G_b^(c-1) of every chunk pair
+//                                     c < b, pair = b (b - 1) / 2 + c
+//   dql, dkr [ch][C][d] f32           gradients of the boundary-adjusted queries / keys
+//   dF [ch][d][d] f32                 gradient of the chunk transition F_c
+//   dad [ch][C][C] f32                scale lower(dS_cc), [i][j]
+struct BwdParams {
+  const void *q, *k, *v, *w, *out, *dout;
+  const float *beta, *lse, *dlse;
+  float scale, scale_log2e;
+  void *dq, *dk, *dv, *dw;
+  float *dbeta, *dlogf;
+  // forward preparation
+  const void* kr;
+  const float* ql;
+  const void* ngt;
+  const float* sdt;
+  const float* lam2;
+  // backward scratch
+  float *dvec, *lse2, *colsum, *rowsum;
+  void *xs, *gs;
+  float *dql, *dkr, *dF, *dad;
+  size_t npairs;
+  int BH, T, Tp, Np, C, d, nch;
+  bool bf16;
+};
+// fp32 scratch of the chunk pass ([ch][C][d] or [ch][C][C] or [ch][C]).
+struct ChunkBufs {
+  float *Wf, *Kf, *Qf, *UW, *dUW, *P1, *P2, *dQf, *dKf, *dWf;
+  float *GWW, *Lm, *Xi, *U, *Nm, *TK, *Mm, *dM, *dTK, *dN, *dU, *dXi, *T1, *dLm, *BL;
+  float *bf, *dbf;
+};
+// Lays out the backward scratch over `base` (null: count bytes only); the
+// geometry and scratch pointers go to *p, the chunk-pass buffers to *cb.
+size_t bwd_workspace_layout(const Geom& g, char* base, BwdParams* p, ChunkBufs* cb);
+cudaError_t launch_bwd(const BwdParams& p, const ChunkBufs& cb, cudaStream_t st);
 // Diagnostics: a kernel whose bounded wait can only expire (sets *status).
 cudaError_t launch_debug_wait(int* status, unsigned long long limit_ns, cudaStream_t st);
 

@@ -106,6 +106,42 @@ int path_attn_fwd_partial(const void* q, const void* k, const void* v, const voi
                           float* lse, int B, int H, int T, int d, int r, int dtype, void* stream);
 
 /*
+ * path_attn_bwd -- gradients of a path_attn_fwd call: with a loss L whose
+ * gradients with respect to out and lse are dout and dlse, returns
+ * dq, dk, dv, dw = dL/d(q, k, v, w), dbeta = dL/dbeta and (PaTH-FoX)
+ * dlogf = dL/dlog f.  The pages time the forward and backward together
+ * (OpenReview discussion, section "Efficiency Evaluation") and define only
+ * the forward ("PaTH Attention: ..." slides, frames "PaTH inserts a learned
+ * transformation along every path", "FoX adds a separate mechanism for
+ * forgetting"); these are the exact derivatives of that forward, taken
+ * through its blockwise form (frames "A triangular representation makes paths
+ * computable", "A right-to-left scan accumulates cross-block paths").
+ *
+ *   q, k, v, w, beta, logf, scale, B, H, T, d, dtype   as given to path_attn_fwd
+ *   out   device, [B,H,T,d], dtype      the forward's output
+ *   lse   device, [B,H,T], fp32         the forward's lse (required)
+ *   dout  device, [B,H,T,d], dtype      dL/dout
+ *   dlse  device, [B,H,T], fp32, or NULL (taken as zero)
+ *   dq, dk, dv, dw   device, [B,H,T,d], dtype (written)
+ *   dbeta device, [B,H,T], fp32 (written)
+ *   dlogf device, [B,H,T], fp32 (written), required iff logf is not NULL
+ * All arrays 16-byte aligned, outputs distinct from inputs.  The call reruns
+ * the forward's chunk preparation, then walks every chunk pair; the walked
+ * queries X_b^(c) and their gradients are kept for each pair c < b, so the
+ * stream-ordered scratch from the library's pool grows as T^2 d / C
+ * (path_attn_bwd_workspace_bytes reports it).  Errors as path_attn_fwd.
+ */
+int path_attn_bwd(const void* q, const void* k, const void* v, const void* w,
+                  const float* beta, const float* logf, float scale, const void* out,
+                  const float* lse, const void* dout, const float* dlse, void* dq, void* dk,
+                  void* dv, void* dw, float* dbeta, float* dlogf, int B, int H, int T, int d,
+                  int dtype, void* stream);
+
+/* Bytes of stream-ordered scratch one path_attn_bwd call takes from the pool. */
+int path_attn_bwd_workspace_bytes(int B, int H, int T, int d, int dtype, int with_gate,
+                                  size_t* bytes);
+
+/*
  * Decoding with keys rewritten in place (slides' frame "Decoding updates
  * historical keys in place").  A decoder keeps, per (b, h), a key cache in
  * which row j < t holds k_j carried to the latest token t - 1,

@@ -103,6 +103,20 @@ def make_inputs(wl: Workload, device="cpu"):
                 beta=beta, logf=logf, scale=1.0 / math.sqrt(wl.d))
 
 
+def make_grad_inputs(wl: Workload, device="cpu", with_dlse=True):
+    """Upstream gradients for the backward of ``wl``'s forward: dout
+    ([B,H,T,d], workload dtype) ~ N(0, 1) and dlse ([B,H,T] fp32) ~ N(0, 1)
+    (None without ``with_dlse``), from their own seed."""
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(wl.seed + 7919)
+    shape = (wl.B, wl.H, wl.T, wl.d)
+    dout = torch.randn(shape, generator=g, device=dev, dtype=torch.float32)
+    dlse = torch.randn(shape[:-1], generator=g, device=dev, dtype=torch.float32)
+    return dict(dout=dout.to(wl.torch_dtype).contiguous(),
+                dlse=dlse.contiguous() if with_dlse else None)
+
+
 # Decoding: one new token per (b, h) against a cache of Tmax rows.
 DECODE_WORKLOADS = {
     "decode_t16k_d128": Workload("decode_t16k_d128", 2, 16, 16384, 128,
