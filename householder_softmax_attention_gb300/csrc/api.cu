@@ -269,6 +269,7 @@ int path_attn_bwd(const void* q, const void* k, const void* v, const void* w,
     p.lam2 = g.gate ? ws.lam2 : nullptr;
     p.BH = g.BH; p.T = g.T; p.Tp = g.Tp; p.Np = g.Np; p.C = g.C; p.d = g.d; p.nch = g.nch;
     p.bf16 = g.bf16;
+    p.status = s->status;
     e = launch_bwd(p, cb, st);
   }
   if (e != cudaSuccess) rc = set_cuda_error(e);

@@ -581,12 +581,19 @@ cudaError_t launch_bwd_t(const BwdParams& p, const ChunkBufs& cb, cudaStream_t s
   const int C = p.C;
   const dim3 rows_tp((p.Tp + kRowWarps - 1) / kRowWarps, p.BH);
   bwd_rowdot_kernel<ET, D><<<rows_tp, kRowWarps * 32, 0, st>>>(p);
-  bwd_query_kernel<ET, D><<<rows_tp, kRowWarps * 32, 0, st>>>(p);
-  cudaError_t e = cudaMemsetAsync(p.dad, 0, static_cast<size_t>(p.nch) * C * C * 4, st);
-  if (e != cudaSuccess) return e;
-  bwd_key_kernel<ET, D><<<rows_tp, kRowWarps * 32, 0, st>>>(p);
-  bwd_dF_kernel<ET, D><<<p.nch, 256, 0, st>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  cudaError_t e;
+  if (p.bf16) {
+    // bf16: the chunk pairs on the tensor cores
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_bwd_pairs_tc(p, p.status, st)) != cudaSuccess) return e;
+  } else {
+    bwd_query_kernel<ET, D><<<rows_tp, kRowWarps * 32, 0, st>>>(p);
+    e = cudaMemsetAsync(p.dad, 0, static_cast<size_t>(p.nch) * C * C * 4, st);
+    if (e != cudaSuccess) return e;
+    bwd_key_kernel<ET, D><<<rows_tp, kRowWarps * 32, 0, st>>>(p);
+    bwd_dF_kernel<ET, D><<<p.nch, 256, 0, st>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   // ---- chunk pass (fp32, batched over chunks)
   const int nch = p.nch;
   const long long cc = static_cast<long long>(C) * C, cd = static_cast<long long>(C) * D,
@@ -682,6 +689,7 @@ size_t bwd_workspace_layout(const Geom& g, char* base, BwdParams* p, ChunkBufs* 
   b.rowsum = reinterpret_cast<float*>(take(BH * Tp * 4));
   b.xs = take(BH * npairs * C * d * es);
   b.gs = take(BH * npairs * C * d * es);
+  b.ds = g.bf16 ? take(BH * npairs * C * C * 2) : nullptr;
   b.dql = reinterpret_cast<float*>(take(nch * C * d * 4));
   b.dkr = reinterpret_cast<float*>(take(nch * C * d * 4));
   b.dF = reinterpret_cast<float*>(take(nch * d * d * 4));

@@ -160,6 +160,7 @@ cudaError_t launch_gate_prefix(const float* logf, float* out, int BH, int T, int
 //                                     lse log2(e), column and row sums of dS
 //   xs, gs [bh][pair][C][d] elem      X_b^(c) and G_b^(c-1) of every chunk pair
 //                                     c < b, pair = b (b - 1) / 2 + c
+//   ds [bh][pair][C][C] bf16          dS_bc^T, [key][query] (bf16 inputs only)
 //   dql, dkr [ch][C][d] f32           gradients of the boundary-adjusted queries / keys
 //   dF [ch][d][d] f32                 gradient of the chunk transition F_c
 //   dad [ch][C][C] f32                scale lower(dS_cc), [i][j]
@@ -177,8 +178,9 @@ struct BwdParams {
   const float* lam2;
   // backward scratch
   float *dvec, *lse2, *colsum, *rowsum;
-  void *xs, *gs;
+  void *xs, *gs, *ds;
   float *dql, *dkr, *dF, *dad;
+  int* status;  // device status word (bounded waits of the tensor-core kernels)
   size_t npairs;
   int BH, T, Tp, Np, C, d, nch;
   bool bf16;
@@ -193,6 +195,9 @@ struct ChunkBufs {
 // geometry and scratch pointers go to *p, the chunk-pass buffers to *cb.
 size_t bwd_workspace_layout(const Geom& g, char* base, BwdParams* p, ChunkBufs* cb);
 cudaError_t launch_bwd(const BwdParams& p, const ChunkBufs& cb, cudaStream_t st);
+// bf16, d = 64 or 128, C = 128: the chunk-pair kernels on tcgen05 (bwd_tc.cu):
+// fills xs, gs, ds, dql, dkr, dF, dad, dv, colsum, rowsum from dvec and lse2.
+cudaError_t launch_bwd_pairs_tc(const BwdParams& p, int* status, cudaStream_t st);
 // Diagnostics: a kernel whose bounded wait can only expire (sets *status).
 cudaError_t launch_debug_wait(int* status, unsigned long long limit_ns, cudaStream_t st);
 
