@@ -26,7 +26,8 @@ __all__ = [
     "path_attn_bwd", "path_attn_bwd_workspace_bytes",
     "path_attn_debug_factors", "path_attn_device_status", "path_attn_workspace_bytes",
     "path_attn_chunk_size", "path_attn_launches_per_call", "path_attn_timing_enable",
-    "path_attn_timing_read", "path_attn_version", "path_attn_status_string",
+    "path_attn_timing_read", "path_attn_bwd_timing_read", "BWD_PHASES", "path_attn_version",
+    "path_attn_status_string",
     "LIBRARY_PATH", "HEADER_PATH", "PATH_DTYPE_F32", "PATH_DTYPE_BF16",
 ]
 
@@ -89,6 +90,9 @@ def load_library(path: str | None = None):
                                               ctypes.POINTER(ctypes.c_double),
                                               ctypes.POINTER(ctypes.c_long)]
         lib.path_attn_timing_read.restype = i
+        lib.path_attn_bwd_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double),
+                                                  ctypes.POINTER(ctypes.c_long)]
+        lib.path_attn_bwd_timing_read.restype = i
         lib.path_attn_launches_per_call.argtypes = [i, i, i]
         lib.path_attn_launches_per_call.restype = i
         lib.path_attn_debug_factors.argtypes = [vp, vp, vp, fp, fp, f, i, i, i, i, i,
@@ -524,6 +528,19 @@ def path_attn_timing_read():
     _check(load_library().path_attn_timing_read(ctypes.byref(p), ctypes.byref(a), ctypes.byref(c)),
            "path_attn_timing_read")
     return p.value, a.value, c.value
+
+
+BWD_PHASES = ("prep", "rowdot", "xwalk", "key", "gwalk", "dF", "chunk")
+
+
+def path_attn_bwd_timing_read():
+    """({phase: ms_total}, calls) of path_attn_bwd since timing was enabled;
+    phases in launch order (``BWD_PHASES``)."""
+    ms = (ctypes.c_double * len(BWD_PHASES))()
+    c = ctypes.c_long(0)
+    _check(load_library().path_attn_bwd_timing_read(ms, ctypes.byref(c)),
+           "path_attn_bwd_timing_read")
+    return dict(zip(BWD_PHASES, list(ms))), c.value
 
 
 def path_attn_version() -> int:

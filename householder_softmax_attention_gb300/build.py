@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpathattn.so")
-SOURCES = ["api.cu", "prep.cu", "prep_tc.cu", "attn_f32.cu", "attn_tc.cu", "bwd.cu", "bwd_tc.cu",
+SOURCES = ["api.cu", "prep.cu", "prep_tc.cu", "attn_f32.cu", "attn_tc.cu", "bwd.cu", "bwd_tc.cu", "bwd_gemm_tc.cu",
            "decode.cu", "producer.cu", "producer_tc.cu"]
 HEADERS = ["common.cuh", "ptx.cuh", "prep_solve.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

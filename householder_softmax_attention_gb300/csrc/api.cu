@@ -41,6 +41,25 @@ struct TimingRec {
 bool g_timing = false;
 std::vector<TimingRec> g_timing_recs;
 size_t g_timing_used = 0;
+struct BwdTimingRec {
+  cudaEvent_t ev[kBwdPhases + 1];
+};
+std::vector<BwdTimingRec> g_bwd_recs;
+size_t g_bwd_used = 0;
+
+// The next backward timing record (events created on first use), or null
+// when timing is off or events cannot be created.
+cudaEvent_t* next_bwd_rec() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_timing) return nullptr;
+  if (g_bwd_used == g_bwd_recs.size()) {
+    BwdTimingRec r{};
+    for (auto& e : r.ev)
+      if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    g_bwd_recs.push_back(r);
+  }
+  return g_bwd_recs[g_bwd_used++].ev;
+}
 
 int set_cuda_error(cudaError_t e) {
   std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s", cudaGetErrorName(e),
@@ -259,7 +278,10 @@ int path_attn_bwd(const void* q, const void* k, const void* v, const void* w,
   ChunkBufs cb;
   bwd_workspace_layout(g, base + fwd_bytes, &p, &cb);
   Inputs in{q, k, v, w, beta, logf, scale, nullptr, nullptr};
+  p.ev = next_bwd_rec();
+  bwd_mark(p.ev, kBwdEvPrep, st);
   e = launch_prep(g, in, ws, s->status, st, nullptr);
+  bwd_mark(p.ev, kBwdEvRowdot, st);
   if (e == cudaSuccess) {
     p.q = q; p.k = k; p.v = v; p.w = w; p.out = out; p.dout = dout;
     p.beta = beta; p.lse = lse; p.dlse = dlse;
@@ -511,6 +533,30 @@ int path_attn_timing_enable(int enable) {
   std::lock_guard<std::mutex> lk(g_mu);
   g_timing = enable != 0;
   g_timing_used = 0;
+  g_bwd_used = 0;
+  return PATH_OK;
+}
+
+int path_attn_bwd_timing_read(double* phase_ms, long* calls) {
+  std::vector<BwdTimingRec> recs;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    recs.assign(g_bwd_recs.begin(), g_bwd_recs.begin() + g_bwd_used);
+  }
+  double acc[kBwdPhases] = {};
+  for (auto& r : recs) {
+    cudaError_t e = cudaEventSynchronize(r.ev[kBwdPhases]);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    for (int i = 0; i < kBwdPhases; ++i) {
+      float x = 0;
+      if ((e = cudaEventElapsedTime(&x, r.ev[i], r.ev[i + 1])) != cudaSuccess)
+        return set_cuda_error(e);
+      acc[i] += x;
+    }
+  }
+  if (phase_ms)
+    for (int i = 0; i < kBwdPhases; ++i) phase_ms[i] = acc[i];
+  if (calls) *calls = static_cast<long>(recs.size());
   return PATH_OK;
 }
 

@@ -567,9 +567,23 @@ __global__ void __launch_bounds__(1024) bwd_gate_kernel(BwdParams p) {
   }
 }
 
-cudaError_t gemm(cudaStream_t st, int batch, int M, int N, int K, float alpha, const float* A,
+// Where the chunk-pass GEMMs run: bf16 inputs take the tensor-core kernel
+// (fp32 operands as bf16 hi + lo), fp32 inputs the fp32 SIMT kernel.
+struct GemmCtx {
+  cudaStream_t st;
+  bool tc;
+  int* status;
+};
+
+cudaError_t gemm(const GemmCtx& gx, int batch, int M, int N, int K, float alpha, const float* A,
                  int lda, long long sA, bool tA, const float* B, int ldb, long long sB, bool tB,
                  float* Cm, int ldc, long long sC, bool acc, int mask) {
+  if (gx.tc && gemm_tc_supported(M, N, K, lda, ldb, ldc)) {
+    TcGemm t{A, B, Cm, sA, sB, sC, lda, ldb, ldc, M, N, K, batch, mask, tA, tB, acc, alpha,
+             gx.status};
+    return launch_gemm_tc(t, gx.st);
+  }
+  cudaStream_t st = gx.st;
   GemmArg g{A, B, Cm, sA, sB, sC, lda, ldb, ldc, M, N, K, batch, mask, tA, tB, acc, alpha};
   const dim3 grid(N / 64, M / 64, batch < 65535 ? batch : 65535);
   gemm_batched_kernel<<<grid, 256, 0, st>>>(g);
@@ -581,6 +595,7 @@ cudaError_t launch_bwd_t(const BwdParams& p, const ChunkBufs& cb, cudaStream_t s
   const int C = p.C;
   const dim3 rows_tp((p.Tp + kRowWarps - 1) / kRowWarps, p.BH);
   bwd_rowdot_kernel<ET, D><<<rows_tp, kRowWarps * 32, 0, st>>>(p);
+  bwd_mark(p.ev, kBwdEvXwalk, st);
   cudaError_t e;
   if (p.bf16) {
     // bf16: the chunk pairs on the tensor cores
@@ -593,15 +608,18 @@ cudaError_t launch_bwd_t(const BwdParams& p, const ChunkBufs& cb, cudaStream_t s
     bwd_key_kernel<ET, D><<<rows_tp, kRowWarps * 32, 0, st>>>(p);
     bwd_dF_kernel<ET, D><<<p.nch, 256, 0, st>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    for (int i = kBwdEvKey; i <= kBwdEvDf; ++i) bwd_mark(p.ev, i, st);
   }
+  bwd_mark(p.ev, kBwdEvChunk, st);
   // ---- chunk pass (fp32, batched over chunks)
   const int nch = p.nch;
+  const GemmCtx gx{st, p.bf16, p.status};
   const long long cc = static_cast<long long>(C) * C, cd = static_cast<long long>(C) * D,
                   dd = static_cast<long long>(D) * D;
   bwd_chunk_inputs_kernel<ET><<<1024, 256, 0, st>>>(p, cb);
   const float *W = cb.Wf, *K = cb.Kf, *Q = cb.Qf;
   // forward factors
-  if ((e = gemm(st, nch, C, C, D, 1.f, W, D, cd, false, W, D, cd, true, cb.GWW, C, cc, false, 0)))
+  if ((e = gemm(gx, nch, C, C, D, 1.f, W, D, cd, false, W, D, cd, true, cb.GWW, C, cc, false, 0)))
     return e;
   bwd_chunk_elem_kernel<<<nch, 256, 0, st>>>(cb.GWW, cb.Lm, cb.bf, C, 0);
   const int tri_smem = 2 * C * C * static_cast<int>(sizeof(float));
@@ -610,62 +628,63 @@ cudaError_t launch_bwd_t(const BwdParams& p, const ChunkBufs& cb, cudaStream_t s
     return e;
   bwd_tri_inv_kernel<<<nch, C, tri_smem, st>>>(cb.Lm, cb.Xi, C);
   bwd_chunk_elem_kernel<<<nch, 256, 0, st>>>(cb.Xi, cb.U, cb.bf, C, 1);
-  if ((e = gemm(st, nch, C, C, D, 1.f, W, D, cd, false, K, D, cd, true, cb.Nm, C, cc, false, 2)) ||
-      (e = gemm(st, nch, C, C, C, 1.f, cb.U, C, cc, false, cb.Nm, C, cc, false, cb.TK, C, cc, false, 0)) ||
-      (e = gemm(st, nch, C, D, C, 1.f, cb.U, C, cc, false, W, D, cd, false, cb.UW, D, cd, false, 0)) ||
-      (e = gemm(st, nch, C, C, D, 1.f, Q, D, cd, false, W, D, cd, true, cb.Mm, C, cc, false, 1)))
+  if ((e = gemm(gx, nch, C, C, D, 1.f, W, D, cd, false, K, D, cd, true, cb.Nm, C, cc, false, 2)) ||
+      (e = gemm(gx, nch, C, C, C, 1.f, cb.U, C, cc, false, cb.Nm, C, cc, false, cb.TK, C, cc, false, 0)) ||
+      (e = gemm(gx, nch, C, D, C, 1.f, cb.U, C, cc, false, W, D, cd, false, cb.UW, D, cd, false, 0)) ||
+      (e = gemm(gx, nch, C, C, D, 1.f, Q, D, cd, false, W, D, cd, true, cb.Mm, C, cc, false, 1)))
     return e;
   const float *dQl = p.dql, *dKr = p.dkr, *dF = p.dF, *dA = p.dad;
   // dM = -dQl UW^T - dA TK^T, dMl = lower(dM)
-  if ((e = gemm(st, nch, C, C, D, -1.f, dQl, D, cd, false, cb.UW, D, cd, true, cb.dM, C, cc, false, 0)) ||
-      (e = gemm(st, nch, C, C, C, -1.f, dA, C, cc, false, cb.TK, C, cc, true, cb.dM, C, cc, true, 1)))
+  if ((e = gemm(gx, nch, C, C, D, -1.f, dQl, D, cd, false, cb.UW, D, cd, true, cb.dM, C, cc, false, 0)) ||
+      (e = gemm(gx, nch, C, C, C, -1.f, dA, C, cc, false, cb.TK, C, cc, true, cb.dM, C, cc, true, 1)))
     return e;
   // dQ = dQl + dA K + dMl W
   if ((e = cudaMemcpyAsync(cb.dQf, dQl, static_cast<size_t>(nch) * cd * 4, cudaMemcpyDeviceToDevice, st)) ||
-      (e = gemm(st, nch, C, D, C, 1.f, dA, C, cc, false, K, D, cd, false, cb.dQf, D, cd, true, 0)) ||
-      (e = gemm(st, nch, C, D, C, 1.f, cb.dM, C, cc, false, W, D, cd, false, cb.dQf, D, cd, true, 0)))
+      (e = gemm(gx, nch, C, D, C, 1.f, dA, C, cc, false, K, D, cd, false, cb.dQf, D, cd, true, 0)) ||
+      (e = gemm(gx, nch, C, D, C, 1.f, cb.dM, C, cc, false, W, D, cd, false, cb.dQf, D, cd, true, 0)))
     return e;
   // dTK = -W dKr^T - M^T dA ; dUW = -M^T dQl
-  if ((e = gemm(st, nch, C, C, D, -1.f, W, D, cd, false, dKr, D, cd, true, cb.dTK, C, cc, false, 0)) ||
-      (e = gemm(st, nch, C, C, C, -1.f, cb.Mm, C, cc, true, dA, C, cc, false, cb.dTK, C, cc, true, 0)) ||
-      (e = gemm(st, nch, C, D, C, -1.f, cb.Mm, C, cc, true, dQl, D, cd, false, cb.dUW, D, cd, false, 0)))
+  if ((e = gemm(gx, nch, C, C, D, -1.f, W, D, cd, false, dKr, D, cd, true, cb.dTK, C, cc, false, 0)) ||
+      (e = gemm(gx, nch, C, C, C, -1.f, cb.Mm, C, cc, true, dA, C, cc, false, cb.dTK, C, cc, true, 0)) ||
+      (e = gemm(gx, nch, C, D, C, -1.f, cb.Mm, C, cc, true, dQl, D, cd, false, cb.dUW, D, cd, false, 0)))
     return e;
   // dN = strictLower(U^T dTK); dK = dKr + dA^T Q + dN^T W
-  if ((e = gemm(st, nch, C, C, C, 1.f, cb.U, C, cc, true, cb.dTK, C, cc, false, cb.dN, C, cc, false, 2)) ||
+  if ((e = gemm(gx, nch, C, C, C, 1.f, cb.U, C, cc, true, cb.dTK, C, cc, false, cb.dN, C, cc, false, 2)) ||
       (e = cudaMemcpyAsync(cb.dKf, dKr, static_cast<size_t>(nch) * cd * 4, cudaMemcpyDeviceToDevice, st)) ||
-      (e = gemm(st, nch, C, D, C, 1.f, dA, C, cc, true, Q, D, cd, false, cb.dKf, D, cd, true, 0)) ||
-      (e = gemm(st, nch, C, D, C, 1.f, cb.dN, C, cc, true, W, D, cd, false, cb.dKf, D, cd, true, 0)))
+      (e = gemm(gx, nch, C, D, C, 1.f, dA, C, cc, true, Q, D, cd, false, cb.dKf, D, cd, true, 0)) ||
+      (e = gemm(gx, nch, C, D, C, 1.f, cb.dN, C, cc, true, W, D, cd, false, cb.dKf, D, cd, true, 0)))
     return e;
   // P1 = W dF, P2 = W dF^T
-  if ((e = gemm(st, nch, C, D, D, 1.f, W, D, cd, false, dF, D, dd, false, cb.P1, D, cd, false, 0)) ||
-      (e = gemm(st, nch, C, D, D, 1.f, W, D, cd, false, dF, D, dd, true, cb.P2, D, cd, false, 0)))
+  if ((e = gemm(gx, nch, C, D, D, 1.f, W, D, cd, false, dF, D, dd, false, cb.P1, D, cd, false, 0)) ||
+      (e = gemm(gx, nch, C, D, D, 1.f, W, D, cd, false, dF, D, dd, true, cb.P2, D, cd, false, 0)))
     return e;
   // dU = -P2 W^T + dTK N^T + dUW W^T
-  if ((e = gemm(st, nch, C, C, D, -1.f, cb.P2, D, cd, false, W, D, cd, true, cb.dU, C, cc, false, 0)) ||
-      (e = gemm(st, nch, C, C, C, 1.f, cb.dTK, C, cc, false, cb.Nm, C, cc, true, cb.dU, C, cc, true, 0)) ||
-      (e = gemm(st, nch, C, C, D, 1.f, cb.dUW, D, cd, false, W, D, cd, true, cb.dU, C, cc, true, 0)))
+  if ((e = gemm(gx, nch, C, C, D, -1.f, cb.P2, D, cd, false, W, D, cd, true, cb.dU, C, cc, false, 0)) ||
+      (e = gemm(gx, nch, C, C, C, 1.f, cb.dTK, C, cc, false, cb.Nm, C, cc, true, cb.dU, C, cc, true, 0)) ||
+      (e = gemm(gx, nch, C, C, D, 1.f, cb.dUW, D, cd, false, W, D, cd, true, cb.dU, C, cc, true, 0)))
     return e;
   // dW = -TK dKr - U P1 - U^T P2 + dMl^T Q + dN K + U^T dUW  (+ the Lm terms below)
-  if ((e = gemm(st, nch, C, D, C, -1.f, cb.TK, C, cc, false, dKr, D, cd, false, cb.dWf, D, cd, false, 0)) ||
-      (e = gemm(st, nch, C, D, C, -1.f, cb.U, C, cc, false, cb.P1, D, cd, false, cb.dWf, D, cd, true, 0)) ||
-      (e = gemm(st, nch, C, D, C, -1.f, cb.U, C, cc, true, cb.P2, D, cd, false, cb.dWf, D, cd, true, 0)) ||
-      (e = gemm(st, nch, C, D, C, 1.f, cb.dM, C, cc, true, Q, D, cd, false, cb.dWf, D, cd, true, 0)) ||
-      (e = gemm(st, nch, C, D, C, 1.f, cb.dN, C, cc, false, K, D, cd, false, cb.dWf, D, cd, true, 0)) ||
-      (e = gemm(st, nch, C, D, C, 1.f, cb.U, C, cc, true, cb.dUW, D, cd, false, cb.dWf, D, cd, true, 0)))
+  if ((e = gemm(gx, nch, C, D, C, -1.f, cb.TK, C, cc, false, dKr, D, cd, false, cb.dWf, D, cd, false, 0)) ||
+      (e = gemm(gx, nch, C, D, C, -1.f, cb.U, C, cc, false, cb.P1, D, cd, false, cb.dWf, D, cd, true, 0)) ||
+      (e = gemm(gx, nch, C, D, C, -1.f, cb.U, C, cc, true, cb.P2, D, cd, false, cb.dWf, D, cd, true, 0)) ||
+      (e = gemm(gx, nch, C, D, C, 1.f, cb.dM, C, cc, true, Q, D, cd, false, cb.dWf, D, cd, true, 0)) ||
+      (e = gemm(gx, nch, C, D, C, 1.f, cb.dN, C, cc, false, K, D, cd, false, cb.dWf, D, cd, true, 0)) ||
+      (e = gemm(gx, nch, C, D, C, 1.f, cb.U, C, cc, true, cb.dUW, D, cd, false, cb.dWf, D, cd, true, 0)))
     return e;
   // dXi = dU diag(beta); T1 = Xi^T dXi; dLm = strictLower(-T1 Xi^T)
   bwd_chunk_elem_kernel<<<nch, 256, 0, st>>>(cb.dU, cb.dXi, cb.bf, C, 1);
-  if ((e = gemm(st, nch, C, C, C, 1.f, cb.Xi, C, cc, true, cb.dXi, C, cc, false, cb.T1, C, cc, false, 0)) ||
-      (e = gemm(st, nch, C, C, C, -1.f, cb.T1, C, cc, false, cb.Xi, C, cc, true, cb.dLm, C, cc, false, 2)))
+  if ((e = gemm(gx, nch, C, C, C, 1.f, cb.Xi, C, cc, true, cb.dXi, C, cc, false, cb.T1, C, cc, false, 0)) ||
+      (e = gemm(gx, nch, C, C, C, -1.f, cb.T1, C, cc, false, cb.Xi, C, cc, true, cb.dLm, C, cc, false, 2)))
     return e;
   bwd_dbeta_kernel<<<nch, C, 0, st>>>(cb.Xi, cb.dU, cb.dLm, cb.GWW, cb.dbf, C);
   // BL = diag(beta) dLm; dW += BL W + BL^T W
   bwd_chunk_elem_kernel<<<nch, 256, 0, st>>>(cb.dLm, cb.BL, cb.bf, C, 2);
-  if ((e = gemm(st, nch, C, D, C, 1.f, cb.BL, C, cc, false, W, D, cd, false, cb.dWf, D, cd, true, 0)) ||
-      (e = gemm(st, nch, C, D, C, 1.f, cb.BL, C, cc, true, W, D, cd, false, cb.dWf, D, cd, true, 0)))
+  if ((e = gemm(gx, nch, C, D, C, 1.f, cb.BL, C, cc, false, W, D, cd, false, cb.dWf, D, cd, true, 0)) ||
+      (e = gemm(gx, nch, C, D, C, 1.f, cb.BL, C, cc, true, W, D, cd, false, cb.dWf, D, cd, true, 0)))
     return e;
   bwd_chunk_outputs_kernel<ET><<<1024, 256, 0, st>>>(p, cb);
   if (p.dlogf) bwd_gate_kernel<<<p.BH, 1024, 0, st>>>(p);
+  bwd_mark(p.ev, kBwdEvEnd, st);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,208 @@
+// bwd_gemm_tc.cu -- batched small GEMMs of the backward's chunk pass on the
+// sm_103a tensor cores.
+//
+//   C[z] = mask(alpha op(A[z]) op(B[z]) + (acc ? C[z] : 0)),   z = 0 .. batch-1
+//
+// fp32 row-major operands (M = 128 rows, N and K in {64, 128}), one CTA of
+// four warps per batch item.  Each fp32 operand enters the MMA as
+// x_hi + x_lo with x_hi = bf16(x), x_lo = bf16(x - x_hi) (about 16
+// significant bits); the three products hi*hi + hi*lo + lo*hi accumulate in
+// fp32 in TMEM.  K is consumed in slices of 64: the CTA converts a slice of A
+// and B into 128-byte-swizzled shared-memory tiles (op(A) K-major unless A is
+// transposed, op(B) MN-major unless B is transposed, so that every global
+// read is along a stored row), one thread issues the twelve MMAs of the
+// slice, and the next slice is written once they have completed.  The
+// epilogue (alpha, accumulate, mask) runs from TMEM, one output row per
+// thread.  Three CTAs fit on an SM, so conversion, MMAs and epilogues of
+// different batch items overlap.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace pathattn {
+namespace {
+
+constexpr int kM = 128, kKs = 64, kThreads = 128;
+constexpr uint32_t kSliceA = kM * kKs * 2;      // one bf16 copy of an A slice
+constexpr uint32_t kSliceB = kKs * 128 * 2;     // one bf16 copy of a B slice (N <= 128)
+constexpr uint32_t kOffAlo = kSliceA, kOffBhi = 2 * kSliceA, kOffBlo = 2 * kSliceA + kSliceB;
+constexpr size_t kSmemBytes = 2 * kSliceA + 2 * kSliceB + 1024 + 64;
+
+struct GemmBars {
+  uint64_t mma;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// Byte offset of (row, col) in a tile of `rows` stored rows whose columns are
+// split into 64-column halves of rows * 128 bytes, 128-byte swizzled.
+__device__ __forceinline__ uint32_t swz_off(int rows, int row, int col) {
+  return (col >> 6) * (rows * 128) + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4) +
+         ((col & 7) << 1);
+}
+
+// Converts a stored tile (rows x cols fp32, global, leading dimension ld)
+// into bf16 hi / lo swizzled tiles.
+__device__ __forceinline__ void load_split(const float* __restrict__ src, int ld, int rows, int cols,
+                                           uint8_t* hi, uint8_t* lo) {
+  const int groups = rows * cols / 8;
+  const int gpr = cols / 8;
+  for (int gi = threadIdx.x; gi < groups; gi += kThreads) {
+    const int r = gi / gpr, c8 = gi - r * gpr;
+    const float4* p = reinterpret_cast<const float4*>(src + static_cast<size_t>(r) * ld + c8 * 8);
+    const float4 a = __ldg(p), b = __ldg(p + 1);
+    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * u]), h1 = __float2bfloat16_rn(v[2 * u + 1]);
+      h[u] = pack_bf16x2(__bfloat162float(h0), __bfloat162float(h1));
+      l[u] = pack_bf16x2(v[2 * u] - __bfloat162float(h0), v[2 * u + 1] - __bfloat162float(h1));
+    }
+    const uint32_t off = swz_off(rows, r, c8 * 8);
+    *reinterpret_cast<uint4*>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+  }
+}
+
+template <int N, bool kTA, bool kTB>
+__global__ void __launch_bounds__(kThreads, 3)
+    gemm_tc_kernel(const float* __restrict__ A, const float* __restrict__ B, float* __restrict__ Cm,
+                   long long sA, long long sB, long long sC, int lda, int ldb, int ldc, int K,
+                   int mask, int acc, float alpha, int* __restrict__ status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  GemmBars* bars = reinterpret_cast<GemmBars*>(base + 2 * kSliceA + 2 * kSliceB);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const size_t z = blockIdx.x;
+  const float* Az = A + z * sA;
+  const float* Bz = B + z * sB;
+  float* Cz = Cm + z * sC;
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->mma, 1);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&bars->tmem_base, N);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tb = bars->tmem_base;
+  constexpr uint32_t id = idesc_bf16_f32(kM, N, kTA, !kTB);
+  bool ok = true;
+  const int nslices = K / kKs;
+  for (int s = 0; s < nslices && ok; ++s) {
+    const int k0 = s * kKs;
+    // op(A) slice: A[m][k0..] (K-major) or A[k0..][m] (MN-major)
+    if (kTA)
+      load_split(Az + static_cast<size_t>(k0) * lda, lda, kKs, kM, base, base + kOffAlo);
+    else
+      load_split(Az + k0, lda, kM, kKs, base, base + kOffAlo);
+    // op(B) slice: B[k0..][n] (MN-major) or B[n][k0..] (K-major)
+    if (kTB)
+      load_split(Bz + k0, ldb, N, kKs, base + kOffBhi, base + kOffBlo);
+    else
+      load_split(Bz + static_cast<size_t>(k0) * ldb, ldb, kKs, N, base + kOffBhi, base + kOffBlo);
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      tc_fence_after_sync();
+      const uint32_t a0 = smem_addr(base), b0 = smem_addr(base + kOffBhi);
+#pragma unroll
+      for (int term = 0; term < 3; ++term) {
+        const uint32_t at = a0 + (term == 2 ? kOffAlo : 0);
+        const uint32_t bt = b0 + (term == 1 ? kSliceB : 0);
+#pragma unroll
+        for (int k = 0; k < kKs / 16; ++k) {
+          const uint64_t ad = kTA ? sdesc_sw128(at + k * 2048, kKs * 128, 1024)
+                                  : sdesc_sw128(at + k * 32, 16, 1024);
+          const uint64_t bd = kTB ? sdesc_sw128(bt + k * 32, 16, 1024)
+                                  : sdesc_sw128(bt + k * 2048, kKs * 128, 1024);
+          mma_bf16_ss(tb, ad, bd, id, (s > 0 || term > 0 || k > 0));
+        }
+      }
+      mma_commit(&bars->mma);
+    }
+    // the slice's tiles are free (and, after the last, the accumulator final)
+    // once its MMAs have completed
+    ok = mbar_wait(&bars->mma, s & 1, &bars->abort_flag, kWaitLimitNs);
+    tc_fence_after_sync();
+  }
+  if (ok) {
+    const int m = warp * 32 + lane;
+    const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
+    float* crow = Cz + static_cast<size_t>(m) * ldc;
+#pragma unroll
+    for (int cc = 0; cc < N; cc += 32) {
+      uint32_t v[32];
+      tmem_ld_x32(tb + lb + cc, v);
+#pragma unroll
+      for (int u4 = 0; u4 < 8; ++u4) {
+        float4 o = make_float4(alpha * __uint_as_float(v[4 * u4]), alpha * __uint_as_float(v[4 * u4 + 1]),
+                               alpha * __uint_as_float(v[4 * u4 + 2]), alpha * __uint_as_float(v[4 * u4 + 3]));
+        float4* dst = reinterpret_cast<float4*>(crow + cc + 4 * u4);
+        if (acc) {
+          const float4 c = *dst;
+          o.x += c.x; o.y += c.y; o.z += c.z; o.w += c.w;
+        }
+        const int n0 = cc + 4 * u4;
+        if (mask != 0) {
+          const int lim = mask == 1 ? m : m - 1;  // keep n <= lim
+          if (n0 > lim) o.x = 0.f;
+          if (n0 + 1 > lim) o.y = 0.f;
+          if (n0 + 2 > lim) o.z = 0.f;
+          if (n0 + 3 > lim) o.w = 0.f;
+        }
+        *dst = o;
+      }
+    }
+  } else if (threadIdx.x == 0) {
+    atomicExch(status, PATH_DEV_ERR_TIMEOUT);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after_sync();
+    tmem_dealloc(tb, N);
+  }
+}
+
+template <int N, bool kTA, bool kTB>
+cudaError_t launch_t(const TcGemm& g, cudaStream_t st) {
+  auto kern = gemm_tc_kernel<N, kTA, kTB>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  kern<<<g.batch, kThreads, kSmemBytes, st>>>(g.A, g.B, g.Cm, g.sA, g.sB, g.sC, g.lda, g.ldb,
+                                              g.ldc, g.K, g.mask, g.acc ? 1 : 0, g.alpha,
+                                              g.status);
+  return cudaGetLastError();
+}
+
+template <int N>
+cudaError_t launch_n(const TcGemm& g, cudaStream_t st) {
+  if (g.tA) return g.tB ? launch_t<N, true, true>(g, st) : launch_t<N, true, false>(g, st);
+  return g.tB ? launch_t<N, false, true>(g, st) : launch_t<N, false, false>(g, st);
+}
+
+}  // namespace
+
+bool gemm_tc_supported(int M, int N, int K, int lda, int ldb, int ldc) {
+  return M == kM && (N == 64 || N == 128) && (K == 64 || K == 128) && lda % 8 == 0 &&
+         ldb % 8 == 0 && ldc % 4 == 0;
+}
+
+cudaError_t launch_gemm_tc(const TcGemm& g, cudaStream_t st) {
+  if (!gemm_tc_supported(g.M, g.N, g.K, g.lda, g.ldb, g.ldc) || g.batch < 1)
+    return cudaErrorInvalidValue;
+  return g.N == 128 ? launch_n<128>(g, st) : launch_n<64>(g, st);
+}
+
+}  // namespace pathattn

@@ -964,6 +964,7 @@ cudaError_t launch_pairs_tc(const BwdParams& p, int* status, cudaStream_t st) {
                                                               p.npairs);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
+  bwd_mark(p.ev, kBwdEvKey, st);
   if (kGate) {
     if ((e = cudaMemsetAsync(p.rowsum, 0, static_cast<size_t>(p.BH) * p.Tp * 4, st)) != cudaSuccess)
       return e;
@@ -975,11 +976,13 @@ cudaError_t launch_pairs_tc(const BwdParams& p, int* status, cudaStream_t st) {
       static_cast<bf16*>(p.dv), p.dkr, p.colsum, p.rowsum, status, p.T, p.Np, p.BH, p.npairs,
       p.scale, p.scale_log2e);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  bwd_mark(p.ev, kBwdEvGwalk, st);
   auto kg = bwd_gwalk_tc_kernel<D>;
   if ((e = set_smem(kg, GwCfg<D>::kSmemBytes)) != cudaSuccess) return e;
   kg<<<p.nch, 192, GwCfg<D>::kSmemBytes, st>>>(mng, mds, mkr, gs, p.dql, status, p.Np, p.BH,
                                                 p.npairs, p.scale);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  bwd_mark(p.ev, kBwdEvDf, st);
   auto kf = bwd_dF_tc_kernel<D>;
   if ((e = set_smem(kf, DfCfg<D>::kSmemBytes)) != cudaSuccess) return e;
   kf<<<p.nch, 192, DfCfg<D>::kSmemBytes, st>>>(mgs, mxs, p.dF, status, p.Np, p.BH, p.npairs,

@@ -181,10 +181,21 @@ struct BwdParams {
   void *xs, *gs, *ds;
   float *dql, *dkr, *dF, *dad;
   int* status;  // device status word (bounded waits of the tensor-core kernels)
+  // optional timing: events recorded on the stream at the phase boundaries
+  // (index kBwdEv* below), null when timing is off
+  cudaEvent_t* ev;
   size_t npairs;
   int BH, T, Tp, Np, C, d, nch;
   bool bf16;
 };
+// Phase boundaries of one backward call (events 0 .. kBwdPhases):
+// prep | rowdot | X walk | key pass | G walk | dF | chunk pass and gate.
+constexpr int kBwdPhases = 7;
+enum { kBwdEvPrep = 0, kBwdEvRowdot, kBwdEvXwalk, kBwdEvKey, kBwdEvGwalk, kBwdEvDf, kBwdEvChunk,
+       kBwdEvEnd };
+inline void bwd_mark(const cudaEvent_t* ev, int i, cudaStream_t st) {
+  if (ev) cudaEventRecord(ev[i], st);
+}
 // fp32 scratch of the chunk pass ([ch][C][d] or [ch][C][C] or [ch][C]).
 struct ChunkBufs {
   float *Wf, *Kf, *Qf, *UW, *dUW, *P1, *P2, *dQf, *dKf, *dWf;
@@ -198,6 +209,22 @@ cudaError_t launch_bwd(const BwdParams& p, const ChunkBufs& cb, cudaStream_t st)
 // bf16, d = 64 or 128, C = 128: the chunk-pair kernels on tcgen05 (bwd_tc.cu):
 // fills xs, gs, ds, dql, dkr, dF, dad, dv, colsum, rowsum from dvec and lse2.
 cudaError_t launch_bwd_pairs_tc(const BwdParams& p, int* status, cudaStream_t st);
+// Batched C[z] = mask(alpha op(A[z]) op(B[z]) + (acc ? C[z] : 0)) for the
+// backward's chunk pass on tcgen05 (bwd_gemm_tc.cu): fp32 row-major operands
+// split into bf16 hi + lo, M = 128, N and K in {64, 128}.  mask 0: none,
+// 1: keep n <= m, 2: keep n < m (others written as 0).
+struct TcGemm {
+  const float* A;
+  const float* B;
+  float* Cm;
+  long long sA, sB, sC;
+  int lda, ldb, ldc, M, N, K, batch, mask;
+  bool tA, tB, acc;
+  float alpha;
+  int* status;
+};
+bool gemm_tc_supported(int M, int N, int K, int lda, int ldb, int ldc);
+cudaError_t launch_gemm_tc(const TcGemm& g, cudaStream_t st);
 // Diagnostics: a kernel whose bounded wait can only expire (sets *status).
 cudaError_t launch_debug_wait(int* status, unsigned long long limit_ns, cudaStream_t st);
 

@@ -269,6 +269,16 @@ int path_attn_timing_enable(int enable);
 int path_attn_timing_read(double* prep_ms, double* attn_ms, long* calls);
 
 /*
+ * The same for path_attn_bwd (while timing is enabled): phase_ms[0..6]
+ * receives the summed milliseconds of its seven phases, in launch order:
+ * chunk preparation, the per-row D_i, the X walk, the key pass, the G walk,
+ * the dF reduction, and the chunk pass with the gate scan (for fp32 inputs
+ * the row kernels appear as one phase, the dF slot).  Either pointer may be
+ * NULL; calls receives the number of path_attn_bwd calls timed.
+ */
+int path_attn_bwd_timing_read(double* phase_ms, long* calls);
+
+/*
  * Number of kernel launches one path_attn_fwd call makes for this problem
  * (host arithmetic only).
  */
