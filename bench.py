@@ -8,7 +8,9 @@ batch of seeded synthetic inputs of the named workload, inputs resident in
 HBM.  With a decoding workload (``--workload decode_t16k_d128``) one step is
 one decoding step of every (b, h) at the last position of a full key/value
 cache (keys rewritten in place); that line reports GB/s of algorithmic HBM
-traffic against the measured copy bandwidth.  The JSON line reports issued TFLOP/s (formulas in ``step_flops``),
+traffic against the measured copy bandwidth.  With ``--workload bwd_<name>``
+one step is the forward and the backward of workload <name> (the pages time
+PaTH forward + backward together) and the line reports ms per step.  The JSON line reports issued TFLOP/s (formulas in ``step_flops``),
 ms per step, the roofline of the attention kernel, an end-to-end number
 through the host-buffer C-ABI entry, sampled SM clocks and a CPU-oracle
 baseline.  ``--impl reference`` times the fp64 CPU oracle instead, on a
@@ -547,6 +549,231 @@ def run_producer_reference(args, wl):
     return 0
 
 
+# ------------------------------------------------------------------ backward
+BWD_PAGES_MS = {  # PaTH-triton fwd+bwd latency on the pages (hardware unstated)
+    ("t2k_d128"): 17.59, ("t2k_d64"): 11.95, ("t4k_d128_refl"): 21.88, ("t4k_d64_refl"): 16.64,
+    ("t16k_d128"): 48.49, ("t16k_d64"): 43.89,
+}
+
+
+def bwd_flops(B, H, T, d, C=128):
+    """Issued tensor-core FLOPs of one backward, by phase.  Per (b, h) with
+    N = ceil(T / C) chunks, P = N(N-1)/2 chunk pairs, X = (N-1)(N-2)/2
+    chunk crossings:
+      X walk    X += Xw ngt^T                  2 C d^2 * X
+      key pass  S^T, dP^T, dV, dKr per pair    8 C^2 d * P;  dP^T, dV per diagonal 4 C^2 d * N
+      G walk    dS Kr per pair, Gw ngt per crossing   2 C^2 d * P + 2 C d^2 * X
+      dF        G^T X per crossing             2 C d^2 * X
+      chunk pass  30 products of 128-row operands (C x C or C x d), counted once
+                  (the kernel issues each as three bf16 products)
+    """
+    N = -(-T // C)
+    P, X = N * (N - 1) // 2, max(N - 1, 0) * max(N - 2, 0) // 2
+    BH = B * H
+    f = {
+        "xwalk": 2 * C * d * d * X,
+        "key": 8 * C * C * d * P + 4 * C * C * d * N,
+        "gwalk": 2 * C * C * d * P + 2 * C * d * d * X,
+        "dF": 2 * C * d * d * X,
+        "chunk": N * 30 * 2 * C * C * max(C, d) * min(C, d) // C,
+    }
+    return {k: BH * v for k, v in f.items()}
+
+
+def oracle_bwd_sample(wl, budget_s, threads):
+    """Seconds of the fp64 oracle's forward + blockwise backward for one
+    (b, h) problem of the workload, timed on its first Ts tokens (a causal
+    prefix is itself a valid problem) and extrapolated by (T / Ts)^2."""
+    import numpy as np
+
+    from oracle import path_oracle_fwd
+    from oracle.chunked_bwd import path_chunked_bwd
+    from seeded_inputs import make_grad_inputs, make_inputs
+
+    Ts = min(wl.T, 1024)
+    one = wl.with_(B=1, H=1, T=Ts)
+    x = make_inputs(one)
+    gi = make_grad_inputs(one)
+    f = lambda t: None if t is None else t[0, 0].double().numpy()
+    q, k, v, w, b, lf = (f(x[n]) for n in ("q", "k", "v", "w", "beta", "logf"))
+    per, spent = [], 0.0
+    while spent < budget_s or not per:
+        t0 = time.perf_counter()
+        path_oracle_fwd(x["q"][0, 0].float().numpy(), x["k"][0, 0].float().numpy(),
+                        x["v"][0, 0].float().numpy(), x["w"][0, 0].float().numpy(),
+                        x["beta"][0, 0].numpy(),
+                        None if lf is None else x["logf"][0, 0].numpy(), x["scale"],
+                        threads=threads)
+        path_chunked_bwd(q, k, v, w, b, f(gi["dout"]), 64, logf=lf, scale=x["scale"],
+                         dlse=f(gi["dlse"]))
+        dt = time.perf_counter() - t0
+        spent += dt
+        per.append(dt)
+    sec = statistics.median(per) * (wl.T / Ts) ** 2
+    desc = (f"fp64 oracle forward + blockwise backward of one (b,h) problem of {wl.name} "
+            f"on its first {Ts} tokens, {len(per)} runs in {spent:.1f} s; extrapolated by "
+            f"(T/{Ts})^2 to a head and by B*H to the workload")
+    return sec, desc
+
+
+def run_bwd(args, wl):
+    """One step = the forward and the backward of the workload (the pages time
+    PaTH fwd+bwd together); value = ms per step."""
+    import torch
+
+    import householder_softmax_attention_gb300 as pa
+    from seeded_inputs import make_grad_inputs, make_inputs
+
+    rank, world, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pa.load_library()
+    x = make_inputs(wl, device=dev)
+    gi = make_grad_inputs(wl, device=dev)
+    q, k, v, w, beta, logf, scale = (x[n] for n in ("q", "k", "v", "w", "beta", "logf", "scale"))
+    dout, dlse = gi["dout"], gi["dlse"]
+    out = torch.empty_like(q)
+    lse = torch.empty(beta.shape, device=dev, dtype=torch.float32)
+    grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(w),
+             torch.empty_like(beta), torch.empty_like(logf) if logf is not None else None)
+    st = torch.cuda.current_stream(dev)
+
+    def step():
+        pa.path_attn_fwd(q, k, v, w, beta, logf, scale, out=out, lse=lse, stream=st)
+        pa.path_attn_bwd(q, k, v, w, beta, out, lse, dout, logf=logf, scale=scale, dlse=dlse,
+                         grads=grads, stream=st)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    assert pa.path_attn_device_status(local, True) == 0, "a kernel wait expired"
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pa.path_attn_timing_enable(True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        e0.record(st)
+        for _ in range(args.steps):
+            step()
+        e1.record(st)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    ms = reduce_max(e0.elapsed_time(e1) / args.steps, world)
+    prep_ms, attn_ms, fcalls = pa.path_attn_timing_read()
+    phases, bcalls = pa.path_attn_bwd_timing_read()
+    pa.path_attn_timing_enable(False)
+    assert fcalls == args.steps and bcalls == args.steps
+    assert pa.path_attn_device_status(local, True) == 0, "a kernel wait expired"
+    phase_ms = {n: t / bcalls for n, t in phases.items()}
+    fwd_ms = (prep_ms + attn_ms) / fcalls
+
+    ff = step_flops(wl.B, wl.H, wl.T, wl.d)
+    bf = bwd_flops(wl.B, wl.H, wl.T, wl.d)
+    total = ff["attn"] + ff["prep"] + ff["prep"] + sum(bf.values())  # bwd reruns the prep
+    peak, hbm, peak_src = _peaks()
+    # dominant backward kernel: the key pass
+    key_ms = phase_ms["key"]
+    achieved = bf["key"] / (key_ms * 1e-3) / 1e12
+    N, C = -(-wl.T // 128), 128
+    P = N * (N - 1) // 2
+    key_bytes = wl.B * wl.H * (P * (2 * C * wl.d * 2 + C * C * 2 + 2 * C * 4)
+                               + N * (2 * C * wl.d * 2 + C * wl.d * 2 + C * wl.d * 4
+                                      + 2 * C * C * 4 + C * wl.d * 2))
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": args.traffic, "kernel": "bwd_key_tc_kernel",
+                "peak_source": f"{peak_src} bf16 burst", "avg_launch_ms": key_ms,
+                "algorithmic_bytes": key_bytes,
+                "hbm_frac": key_bytes / (key_ms * 1e-3) / 1e9 / hbm}
+
+    # end to end through the Python API: inputs and upstream gradients from
+    # pinned host memory, forward + backward, every gradient back to the host
+    names = ("q", "k", "v", "w", "beta") + (("logf",) if logf is not None else ())
+    hin = {n: x[n].cpu().pin_memory() for n in names}
+    hin["dout"], hin["dlse"] = dout.cpu().pin_memory(), dlse.cpu().pin_memory()
+    din = {n: torch.empty_like(t, device=dev) for n, t in hin.items()}
+    hgr = [torch.empty(g.shape, dtype=g.dtype).pin_memory() for g in grads if g is not None]
+
+    def e2e_step():
+        for n, t in hin.items():
+            din[n].copy_(t, non_blocking=True)
+        pa.path_attn_fwd(din["q"], din["k"], din["v"], din["w"], din["beta"], din.get("logf"),
+                         scale, out=out, lse=lse, stream=st)
+        pa.path_attn_bwd(din["q"], din["k"], din["v"], din["w"], din["beta"], out, lse,
+                         din["dout"], logf=din.get("logf"), scale=scale, dlse=din["dlse"],
+                         grads=grads, stream=st)
+        for h, g in zip(hgr, [g for g in grads if g is not None]):
+            h.copy_(g, non_blocking=True)
+        st.synchronize()
+
+    for _ in range(2):
+        e2e_step()
+    n_e2e = max(1, min(args.steps, 5))
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        e2e_step()
+    e2e_ms = reduce_max((time.perf_counter() - t0) * 1e3 / n_e2e, world)
+    h2d = sum(t.numel() * t.element_size() for t in hin.values())
+    d2h = sum(t.numel() * t.element_size() for t in hgr)
+    pages = BWD_PAGES_MS.get(wl.name)
+    dt = 1 if wl.dtype == "bf16" else 0
+    line = {
+        "metric": f"PaTH-attn fwd+bwd ms, {wl.name}", "value": ms, "unit": "ms",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": (ms / pages) if pages else None,
+        "pages_triton_fwd_bwd_ms": pages, "pages_hardware": "unstated",
+        "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": "bwd_" + wl.name, "B": wl.B, "H": wl.H, "T": wl.T, "d": wl.d,
+                   "fox": wl.fox, "parallelism": f"replicas x{world}",
+                   "l2": "inputs and pair buffers larger than L2"},
+        "tflops": world * total / (ms * 1e-3) / 1e12,
+        "fwd_ms": fwd_ms, "bwd_ms": sum(phase_ms.values()), "bwd_phase_ms": phase_ms,
+        "flops_per_step": {"fwd": ff["attn"] + ff["prep"], "bwd": sum(bf.values()) + ff["prep"]},
+        "roofline": roofline,
+        "e2e": {"value": e2e_ms, "unit": "ms", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * (
+            pa.path_attn_launches_per_call(wl.d, dt, logf is not None)
+            + pa.path_attn_bwd_launches_per_call(wl.T, wl.d, dt, logf is not None)),
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        sec, desc = oracle_bwd_sample(wl, min(args.cpu_budget_s, 10.0), threads)
+        est = sec * wl.B * wl.H
+        line["cpu_baseline"] = {"value": est * 1e3, "unit": "ms", "cores": threads,
+                                "kind": "oracle", "sample": desc, "est_full_step_s": est}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_bwd_reference(args, wl):
+    rank, world, _ = dist_setup()
+    if rank != 0:
+        return 0
+    threads = os.cpu_count() or 1
+    per_step, desc = [], ""
+    for _ in range(args.warmup + args.steps):
+        sec, desc = oracle_bwd_sample(wl, min(args.ref_step_s, 2.0), threads)
+        per_step.append(sec * wl.B * wl.H)
+    est = statistics.median(per_step[args.warmup:])
+    line = {
+        "impl": "reference", "metric": f"PaTH-attn fwd+bwd ms, {wl.name}", "value": est * 1e3,
+        "unit": "ms", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": est * 1e3, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "bwd_" + wl.name, "B": wl.B, "H": wl.H, "T": wl.T, "d": wl.d},
+        "cpu_baseline": {"value": est * 1e3, "unit": "ms", "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": est * 1e3, "unit": "ms", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 # ------------------------------------------------------------------ arms
 def run_reference(args, wl, flops):
     rank, world, _ = dist_setup()
@@ -709,6 +936,12 @@ def main(argv=None):
         if args.B or args.H:
             wl = wl.with_(B=args.B or wl.B, H=args.H or wl.H)
         return run_decode_reference(args, wl) if args.impl == "reference" else run_decode(args, wl)
+    if args.workload.startswith("bwd_") and args.workload[4:] in WORKLOADS:
+        wl = WORKLOADS[args.workload[4:]]
+        if args.B or args.H:
+            wl = wl.with_(B=args.B or wl.B, H=args.H or wl.H,
+                          name=f"{wl.name}_B{args.B or wl.B}H{args.H or wl.H}")
+        return run_bwd_reference(args, wl) if args.impl == "reference" else run_bwd(args, wl)
     wl = WORKLOADS[args.workload]
     if args.B or args.H:
         wl = wl.with_(B=args.B or wl.B, H=args.H or wl.H, name=f"{wl.name}_B{args.B or wl.B}H{args.H or wl.H}")

@@ -23,7 +23,7 @@ __all__ = [
     "PathAttnError", "load_library", "path_attn_fwd", "path_attn_fwd_host",
     "path_attn_fwd_noalloc", "path_attn_debug_wait_timeout", "path_attn_prefill",
     "path_attn_decode_step", "DecodeCache", "path_attn_fwd_partial", "path_producer_fwd",
-    "path_attn_bwd", "path_attn_bwd_workspace_bytes",
+    "path_attn_bwd", "path_attn_bwd_workspace_bytes", "path_attn_bwd_launches_per_call",
     "path_attn_debug_factors", "path_attn_device_status", "path_attn_workspace_bytes",
     "path_attn_chunk_size", "path_attn_launches_per_call", "path_attn_timing_enable",
     "path_attn_timing_read", "path_attn_bwd_timing_read", "BWD_PHASES", "path_attn_version",
@@ -95,6 +95,8 @@ def load_library(path: str | None = None):
         lib.path_attn_bwd_timing_read.restype = i
         lib.path_attn_launches_per_call.argtypes = [i, i, i]
         lib.path_attn_launches_per_call.restype = i
+        lib.path_attn_bwd_launches_per_call.argtypes = [i, i, i, i]
+        lib.path_attn_bwd_launches_per_call.restype = i
         lib.path_attn_debug_factors.argtypes = [vp, vp, vp, fp, fp, f, i, i, i, i, i,
                                                 vp, vp, vp, vp, vp, vp]
         lib.path_attn_debug_factors.restype = i
@@ -307,6 +309,13 @@ def path_attn_bwd(q, k, v, w, beta, out, lse, dout, logf=None, scale=None, dlse=
                                B, H, T, d, _dtype_code(q), ctypes.c_void_p(st.cuda_stream))
     _check(rc, "path_attn_bwd")
     return dq, dk, dv, dw, dbeta, dlogf
+
+
+def path_attn_bwd_launches_per_call(T, d, dtype_code, with_gate=False) -> int:
+    n = load_library().path_attn_bwd_launches_per_call(T, d, dtype_code, int(with_gate))
+    if n < 0:
+        raise PathAttnError(n, "path_attn_bwd_launches_per_call")
+    return n
 
 
 def path_attn_bwd_workspace_bytes(B, H, T, d, dtype_code, with_gate=False) -> int:

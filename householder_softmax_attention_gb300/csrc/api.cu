@@ -209,6 +209,22 @@ int path_attn_launches_per_call(int d, int dtype, int with_gate) {
   return prep + (with_gate ? 1 : 0) + 1;
 }
 
+int path_attn_bwd_launches_per_call(int T, int d, int dtype, int with_gate) {
+  const int C = chunk_size(d, dtype);
+  if (C < 0) return C;
+  if (T < 1) return PATH_ERR_INVALID_ARG;
+  const int g = with_gate ? 1 : 0;
+  // chunk pass: fp32 copies, 30 GEMMs, 4 elementwise steps, inverse, dbeta,
+  // outputs, gate scan
+  const int chunk = 1 + 30 + 4 + 1 + 1 + 1 + g;
+  if (dtype == PATH_DTYPE_BF16) {
+    // preparation (+ gate prefix), rowdot, [X walk], key pass, G walk, dF
+    return (1 + g) + 1 + (T > C ? 1 : 0) + 3 + chunk;
+  }
+  // SIMT preparation (+ gate prefix), rowdot, query walk, key pass, dF
+  return (11 + g) + 1 + 3 + chunk;
+}
+
 int path_attn_fwd(const void* q, const void* k, const void* v, const void* w,
                   const float* beta, const float* logf, float scale, void* out, float* lse,
                   int B, int H, int T, int d, int dtype, void* stream) {

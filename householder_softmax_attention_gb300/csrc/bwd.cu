@@ -36,6 +36,7 @@
 #include <cstdint>
 
 #include "common.cuh"
+#include "prep_solve.cuh"
 
 namespace pathattn {
 namespace {
@@ -475,6 +476,32 @@ __global__ void bwd_tri_inv_kernel(const float* Lm, float* Xi, int C) {
   for (int x = threadIdx.x; x < C * C; x += blockDim.x) X[x] = col[x];
 }
 
+// The same inverse for C = 128 by recursive doubling (the forward
+// preparation's solver, tensor cores for the 32- and 64-blocks); 256 threads.
+constexpr int kSolveStride = 132;
+__global__ void __launch_bounds__(256) bwd_tri_inv128_kernel(const float* Lm, float* Xi) {
+  extern __shared__ float sl[];
+  const size_t ch = blockIdx.x;
+  const float* L = Lm + ch * 128 * 128;
+  float* X = Xi + ch * 128 * 128;
+  for (int x = threadIdx.x; x < 128 * 32; x += 256) {
+    const int i = x >> 5, c4 = (x & 31) * 4;
+    *reinterpret_cast<float4*>(sl + i * kSolveStride + c4) =
+        *reinterpret_cast<const float4*>(L + i * 128 + c4);
+  }
+  __syncthreads();
+  invert_unit_lower<kSolveStride>(sl, threadIdx.x);
+  for (int x = threadIdx.x; x < 128 * 32; x += 256) {
+    const int i = x >> 5, c4 = (x & 31) * 4;
+    float4 v = *reinterpret_cast<const float4*>(sl + i * kSolveStride + c4);
+    if (c4 > i) v.x = 0.f;
+    if (c4 + 1 > i) v.y = 0.f;
+    if (c4 + 2 > i) v.z = 0.f;
+    if (c4 + 3 > i) v.w = 0.f;
+    *reinterpret_cast<float4*>(X + i * 128 + c4) = v;
+  }
+}
+
 // Elementwise steps of the chunk pass, one block per chunk.
 //  op 0: Lm  = strictLower(beta_i GWW_ij)
 //  op 1: U   = Xi diag(beta)  (and dXi = dU diag(beta) when `in2` is dU)
@@ -622,11 +649,19 @@ cudaError_t launch_bwd_t(const BwdParams& p, const ChunkBufs& cb, cudaStream_t s
   if ((e = gemm(gx, nch, C, C, D, 1.f, W, D, cd, false, W, D, cd, true, cb.GWW, C, cc, false, 0)))
     return e;
   bwd_chunk_elem_kernel<<<nch, 256, 0, st>>>(cb.GWW, cb.Lm, cb.bf, C, 0);
-  const int tri_smem = 2 * C * C * static_cast<int>(sizeof(float));
-  if ((e = cudaFuncSetAttribute(bwd_tri_inv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                tri_smem)) != cudaSuccess)
-    return e;
-  bwd_tri_inv_kernel<<<nch, C, tri_smem, st>>>(cb.Lm, cb.Xi, C);
+  if (C == 128) {
+    const int smem = 128 * kSolveStride * static_cast<int>(sizeof(float));
+    if ((e = cudaFuncSetAttribute(bwd_tri_inv128_kernel,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+      return e;
+    bwd_tri_inv128_kernel<<<nch, 256, smem, st>>>(cb.Lm, cb.Xi);
+  } else {
+    const int tri_smem = 2 * C * C * static_cast<int>(sizeof(float));
+    if ((e = cudaFuncSetAttribute(bwd_tri_inv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  tri_smem)) != cudaSuccess)
+      return e;
+    bwd_tri_inv_kernel<<<nch, C, tri_smem, st>>>(cb.Lm, cb.Xi, C);
+  }
   bwd_chunk_elem_kernel<<<nch, 256, 0, st>>>(cb.Xi, cb.U, cb.bf, C, 1);
   if ((e = gemm(gx, nch, C, C, D, 1.f, W, D, cd, false, K, D, cd, true, cb.Nm, C, cc, false, 2)) ||
       (e = gemm(gx, nch, C, C, C, 1.f, cb.U, C, cc, false, cb.Nm, C, cc, false, cb.TK, C, cc, false, 0)) ||

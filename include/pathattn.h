@@ -284,6 +284,9 @@ int path_attn_bwd_timing_read(double* phase_ms, long* calls);
  */
 int path_attn_launches_per_call(int d, int dtype, int with_gate);
 
+/* The same for one path_attn_bwd call at sequence length T (memsets not counted). */
+int path_attn_bwd_launches_per_call(int T, int d, int dtype, int with_gate);
+
 /*
  * path_attn_debug_factors -- diagnostics: run only the chunk preparation and
  * copy its per-chunk factors (frame "Backup: fix orientation before
