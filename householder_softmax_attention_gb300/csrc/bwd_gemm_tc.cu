@@ -12,8 +12,9 @@
 // transposed, op(B) MN-major unless B is transposed, so that every global
 // read is along a stored row), one thread issues the twelve MMAs of the
 // slice, and the next slice is written once they have completed.  The
-// epilogue (alpha, accumulate, mask) runs from TMEM, one output row per
-// thread.  Three CTAs fit on an SM, so conversion, MMAs and epilogues of
+// accumulator goes from TMEM (one row per thread) through shared memory, so
+// that the epilogue (alpha, accumulate, mask) reads and writes C in coalesced
+// rows.  Three CTAs fit on an SM, so conversion, MMAs and epilogues of
 // different batch items overlap.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -44,26 +45,36 @@ __device__ __forceinline__ uint32_t swz_off(int rows, int row, int col) {
 }
 
 // Converts a stored tile (rows x cols fp32, global, leading dimension ld)
-// into bf16 hi / lo swizzled tiles.
+// into bf16 hi / lo swizzled tiles; each thread has four 8-column groups of
+// loads in flight before it converts them.
 __device__ __forceinline__ void load_split(const float* __restrict__ src, int ld, int rows, int cols,
                                            uint8_t* hi, uint8_t* lo) {
-  const int groups = rows * cols / 8;
+  const int groups = rows * cols / 8;  // a multiple of 4 * kThreads
   const int gpr = cols / 8;
-  for (int gi = threadIdx.x; gi < groups; gi += kThreads) {
-    const int r = gi / gpr, c8 = gi - r * gpr;
-    const float4* p = reinterpret_cast<const float4*>(src + static_cast<size_t>(r) * ld + c8 * 8);
-    const float4 a = __ldg(p), b = __ldg(p + 1);
-    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    uint32_t h[4], l[4];
+  for (int g0 = threadIdx.x; g0 < groups; g0 += 4 * kThreads) {
+    float4 a[4], b[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * u]), h1 = __float2bfloat16_rn(v[2 * u + 1]);
-      h[u] = pack_bf16x2(__bfloat162float(h0), __bfloat162float(h1));
-      l[u] = pack_bf16x2(v[2 * u] - __bfloat162float(h0), v[2 * u + 1] - __bfloat162float(h1));
+      const int gi = g0 + u * kThreads, r = gi / gpr, c8 = gi - r * gpr;
+      const float4* p = reinterpret_cast<const float4*>(src + static_cast<size_t>(r) * ld + c8 * 8);
+      a[u] = __ldg(p);
+      b[u] = __ldg(p + 1);
     }
-    const uint32_t off = swz_off(rows, r, c8 * 8);
-    *reinterpret_cast<uint4*>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
-    *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int gi = g0 + u * kThreads, r = gi / gpr, c8 = gi - r * gpr;
+      const float v[8] = {a[u].x, a[u].y, a[u].z, a[u].w, b[u].x, b[u].y, b[u].z, b[u].w};
+      uint32_t h[4], l[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * e]), h1 = __float2bfloat16_rn(v[2 * e + 1]);
+        h[e] = pack_bf16x2(__bfloat162float(h0), __bfloat162float(h1));
+        l[e] = pack_bf16x2(v[2 * e] - __bfloat162float(h0), v[2 * e + 1] - __bfloat162float(h1));
+      }
+      const uint32_t off = swz_off(rows, r, c8 * 8);
+      *reinterpret_cast<uint4*>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+    }
   }
 }
 
@@ -136,32 +147,45 @@ __global__ void __launch_bounds__(kThreads, 3)
     tc_fence_after_sync();
   }
   if (ok) {
+    // accumulator rows (one per thread) -> shared memory (the slice tiles are
+    // free), 16-byte units of a row rotated by the row index; then the tile
+    // goes out in row-major order, so that reads of C and writes are coalesced
     const int m = warp * 32 + lane;
     const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
-    float* crow = Cz + static_cast<size_t>(m) * ldc;
+    float4* stile = reinterpret_cast<float4*>(base);
+    constexpr int kU = N / 4;  // 16-byte units per row
 #pragma unroll
     for (int cc = 0; cc < N; cc += 32) {
       uint32_t v[32];
       tmem_ld_x32(tb + lb + cc, v);
 #pragma unroll
       for (int u4 = 0; u4 < 8; ++u4) {
-        float4 o = make_float4(alpha * __uint_as_float(v[4 * u4]), alpha * __uint_as_float(v[4 * u4 + 1]),
-                               alpha * __uint_as_float(v[4 * u4 + 2]), alpha * __uint_as_float(v[4 * u4 + 3]));
-        float4* dst = reinterpret_cast<float4*>(crow + cc + 4 * u4);
-        if (acc) {
-          const float4 c = *dst;
-          o.x += c.x; o.y += c.y; o.z += c.z; o.w += c.w;
-        }
-        const int n0 = cc + 4 * u4;
-        if (mask != 0) {
-          const int lim = mask == 1 ? m : m - 1;  // keep n <= lim
-          if (n0 > lim) o.x = 0.f;
-          if (n0 + 1 > lim) o.y = 0.f;
-          if (n0 + 2 > lim) o.z = 0.f;
-          if (n0 + 3 > lim) o.w = 0.f;
-        }
-        *dst = o;
+        const int j = cc / 4 + u4;
+        stile[m * kU + (j ^ (m & 7))] =
+            make_float4(__uint_as_float(v[4 * u4]), __uint_as_float(v[4 * u4 + 1]),
+                        __uint_as_float(v[4 * u4 + 2]), __uint_as_float(v[4 * u4 + 3]));
       }
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int idx = threadIdx.x; idx < kM * kU; idx += kThreads) {
+      const int r = idx / kU, j = idx - r * kU;
+      float4 o = stile[r * kU + (j ^ (r & 7))];
+      o.x *= alpha; o.y *= alpha; o.z *= alpha; o.w *= alpha;
+      float4* dst = reinterpret_cast<float4*>(Cz + static_cast<size_t>(r) * ldc + 4 * j);
+      if (acc) {
+        const float4 c = *dst;
+        o.x += c.x; o.y += c.y; o.z += c.z; o.w += c.w;
+      }
+      if (mask != 0) {
+        const int lim = mask == 1 ? r : r - 1;  // keep n <= lim
+        const int n0 = 4 * j;
+        if (n0 > lim) o.x = 0.f;
+        if (n0 + 1 > lim) o.y = 0.f;
+        if (n0 + 2 > lim) o.z = 0.f;
+        if (n0 + 3 > lim) o.w = 0.f;
+      }
+      *dst = o;
     }
   } else if (threadIdx.x == 0) {
     atomicExch(status, PATH_DEV_ERR_TIMEOUT);
