@@ -208,10 +208,11 @@ def path_attn_fwd_host(q, k, v, w, beta, logf=None, scale=None, out=None, lse=No
     B, H, T, d = q.shape
     if scale is None:
         scale = d ** -0.5
+    pin = q.is_pinned()  # outputs page-locked like the inputs, so copies overlap
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=pin)
     if lse is None and want_lse:
-        lse = torch.empty((B, H, T), dtype=torch.float32)
+        lse = torch.empty((B, H, T), dtype=torch.float32, pin_memory=pin)
     st = stream if stream is not None else torch.cuda.current_stream()
     rc = lib.path_attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(beta), _ptr(logf),
                                 float(scale), _ptr(out), _ptr(lse), B, H, T, d,

@@ -29,7 +29,12 @@ struct DeviceState {
   int* status = nullptr;  // device int, 0 = fine
   int cc_major = 0, cc_minor = 0;
   int num_sms = 0;
+  // copy streams of the host-buffer entry (non-blocking, created with the state)
+  cudaStream_t copy_in = nullptr, copy_out = nullptr;
 };
+
+// Slices of (b, h) problems the host-buffer entry pipelines its copies over.
+constexpr int kHostSlices = 4;
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
@@ -93,6 +98,9 @@ int device_state(DeviceState** out) {
       return set_cuda_error(e);
     if ((e = cudaMalloc(&s.status, sizeof(int))) != cudaSuccess) return set_cuda_error(e);
     if ((e = cudaMemset(s.status, 0, sizeof(int))) != cudaSuccess) return set_cuda_error(e);
+    if ((e = cudaStreamCreateWithFlags(&s.copy_in, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaStreamCreateWithFlags(&s.copy_out, cudaStreamNonBlocking)) != cudaSuccess)
+      return set_cuda_error(e);
     s.ready = true;
   }
   *out = &s;
@@ -365,40 +373,86 @@ int path_attn_fwd_host(const void* q, const void* k, const void* v, const void* 
   if ((rc = device_state(&s)) != PATH_OK) return rc;
   if ((rc = check_device(s)) != PATH_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The (b, h) problems are independent and contiguous in every array: the
+  // call runs them in slices, copies of slice i + 1 in and of slice i - 1 out
+  // on two copy streams while slice i computes on `stream`.
+  const int nsl = g.BH < kHostSlices ? g.BH : kHostSlices;
+  const int per = (g.BH + nsl - 1) / nsl;
+  Geom gs;
+  if ((rc = make_geom(1, per, T, d, dtype, logf != nullptr, &gs)) != PATH_OK) return rc;
   const size_t es = dtype == PATH_DTYPE_BF16 ? 2 : 4;
-  const size_t nx = static_cast<size_t>(g.BH) * T * d * es, nb = static_cast<size_t>(g.BH) * T * 4;
+  const size_t xrow = static_cast<size_t>(T) * d * es, brow = static_cast<size_t>(T) * 4;
+  const size_t nx = xrow * g.BH, nb = brow * g.BH;
   size_t off = 0;
   auto take = [&](size_t n) { size_t o = off; off = align_up(off + n, 256); return o; };
   const size_t oq = take(nx), ok_ = take(nx), ov = take(nx), ow = take(nx), ob = take(nb),
                olf = logf ? take(nb) : 0, oo = take(nx), ol = lse ? take(nb) : 0;
   const size_t io_bytes = off;
-  const size_t ws_bytes = workspace_layout(g, nullptr, nullptr);
+  const size_t ws_bytes = workspace_layout(gs, nullptr, nullptr);
   char* buf = nullptr;
   cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&buf), io_bytes + ws_bytes,
                                           s->pool, st);
   if (e != cudaSuccess) return set_cuda_error(e);
+  cudaEvent_t ev_start = nullptr, ev_in[kHostSlices] = {}, ev_done[kHostSlices] = {},
+              ev_out = nullptr;
+  auto mk = [](cudaEvent_t* ev) { return cudaEventCreateWithFlags(ev, cudaEventDisableTiming); };
+  bool ok = (e = mk(&ev_start)) == cudaSuccess && (e = mk(&ev_out)) == cudaSuccess;
+  for (int i = 0; ok && i < nsl; ++i)
+    ok = (e = mk(&ev_in[i])) == cudaSuccess && (e = mk(&ev_done[i])) == cudaSuccess;
+  // the buffer exists on `stream` first; both copy streams start after that
+  if (ok) ok = (e = cudaEventRecord(ev_start, st)) == cudaSuccess &&
+               (e = cudaStreamWaitEvent(s->copy_in, ev_start, 0)) == cudaSuccess &&
+               (e = cudaStreamWaitEvent(s->copy_out, ev_start, 0)) == cudaSuccess;
   auto h2d = [&](size_t o, const void* src, size_t n) {
-    return cudaMemcpyAsync(buf + o, src, n, cudaMemcpyHostToDevice, st);
+    return cudaMemcpyAsync(buf + o, src, n, cudaMemcpyHostToDevice, s->copy_in);
   };
-  if ((e = h2d(oq, q, nx)) || (e = h2d(ok_, k, nx)) || (e = h2d(ov, v, nx)) ||
-      (e = h2d(ow, w, nx)) || (e = h2d(ob, beta, nb)) || (logf && (e = h2d(olf, logf, nb)))) {
-    rc = set_cuda_error(e);
-  } else {
-    Inputs in{buf + oq, buf + ok_, buf + ov, buf + ow,
-              reinterpret_cast<float*>(buf + ob),
-              logf ? reinterpret_cast<float*>(buf + olf) : nullptr,
-              scale, buf + oo, lse ? reinterpret_cast<float*>(buf + ol) : nullptr};
-    rc = run_forward(g, in, buf + io_bytes, s, st);
-    if (rc == PATH_OK) {
-      if ((e = cudaMemcpyAsync(out, buf + oo, nx, cudaMemcpyDeviceToHost, st)) ||
-          (lse && (e = cudaMemcpyAsync(lse, buf + ol, nb, cudaMemcpyDeviceToHost, st))))
-        rc = set_cuda_error(e);
-    }
+  auto d2h = [&](void* dst, size_t o, size_t n) {
+    return cudaMemcpyAsync(dst, buf + o, n, cudaMemcpyDeviceToHost, s->copy_out);
+  };
+  auto hp = [](const void* p, size_t o) { return static_cast<const char*>(p) + o; };
+  for (int i = 0; ok && i < nsl; ++i) {
+    const int bh0 = i * per, nbh = (bh0 + per <= g.BH ? per : g.BH - bh0);
+    if (nbh <= 0) break;
+    const size_t x0 = xrow * bh0, xn = xrow * nbh, b0 = brow * bh0, bn = brow * nbh;
+    ok = (e = h2d(oq + x0, hp(q, x0), xn)) == cudaSuccess &&
+         (e = h2d(ok_ + x0, hp(k, x0), xn)) == cudaSuccess &&
+         (e = h2d(ow + x0, hp(w, x0), xn)) == cudaSuccess &&
+         (e = h2d(ob + b0, hp(beta, b0), bn)) == cudaSuccess &&
+         (!logf || (e = h2d(olf + b0, hp(logf, b0), bn)) == cudaSuccess) &&
+         (e = h2d(ov + x0, hp(v, x0), xn)) == cudaSuccess &&
+         (e = cudaEventRecord(ev_in[i], s->copy_in)) == cudaSuccess &&
+         (e = cudaStreamWaitEvent(st, ev_in[i], 0)) == cudaSuccess;
+    if (!ok) break;
+    Geom gi = gs;
+    if (nbh != per && (rc = make_geom(1, nbh, T, d, dtype, logf != nullptr, &gi)) != PATH_OK) break;
+    Inputs in{buf + oq + x0, buf + ok_ + x0, buf + ov + x0, buf + ow + x0,
+              reinterpret_cast<float*>(buf + ob + b0),
+              logf ? reinterpret_cast<float*>(buf + olf + b0) : nullptr, scale,
+              buf + oo + x0, lse ? reinterpret_cast<float*>(buf + ol + b0) : nullptr};
+    if ((rc = run_forward(gi, in, buf + io_bytes, s, st)) != PATH_OK) break;
+    ok = (e = cudaEventRecord(ev_done[i], st)) == cudaSuccess &&
+         (e = cudaStreamWaitEvent(s->copy_out, ev_done[i], 0)) == cudaSuccess &&
+         (e = d2h(static_cast<char*>(out) + x0, oo + x0, xn)) == cudaSuccess &&
+         (!lse || (e = d2h(reinterpret_cast<char*>(lse) + b0, ol + b0, bn)) == cudaSuccess);
   }
+  if (rc == PATH_OK && !ok) rc = set_cuda_error(e);
+  // whatever was queued on the copy streams finishes before the buffer is freed
+  cudaError_t e2 = cudaEventRecord(ev_out, s->copy_out);
+  if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(st, ev_out, 0);
+  cudaError_t e3 = cudaEventRecord(ev_start, s->copy_in);
+  if (e3 == cudaSuccess) e3 = cudaStreamWaitEvent(st, ev_start, 0);
+  if (rc == PATH_OK && (e2 != cudaSuccess || e3 != cudaSuccess))
+    rc = set_cuda_error(e2 != cudaSuccess ? e2 : e3);
   e = cudaFreeAsync(buf, st);
   if (rc == PATH_OK && e != cudaSuccess) rc = set_cuda_error(e);
   e = cudaStreamSynchronize(st);
   if (rc == PATH_OK && e != cudaSuccess) rc = set_cuda_error(e);
+  for (cudaEvent_t ev : {ev_start, ev_out})
+    if (ev) cudaEventDestroy(ev);
+  for (int i = 0; i < kHostSlices; ++i) {
+    if (ev_in[i]) cudaEventDestroy(ev_in[i]);
+    if (ev_done[i]) cudaEventDestroy(ev_done[i]);
+  }
   return rc;
 }
 

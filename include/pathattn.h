@@ -79,9 +79,11 @@ int path_attn_fwd(const void* q, const void* k, const void* v, const void* w,
  * path_attn_fwd_host -- the same operation on HOST buffers (same shapes and
  * dtypes as path_attn_fwd).  Copies the inputs to the current device, runs
  * path_attn_fwd on `stream`, copies out (and lse if non-NULL) back and
- * synchronises `stream` before returning.  Host buffers may be pageable;
- * page-locked buffers make the copies faster.  Device buffers come from the
- * library's pool and are returned before the call ends.
+ * synchronises `stream` before returning.  The (b, h) problems go in up to
+ * four slices: copies in and out run on two library-owned copy streams and
+ * overlap the computation of other slices.  Host buffers may be pageable;
+ * page-locked buffers make the copies faster and let them overlap.  Device
+ * buffers come from the library's pool and are returned before the call ends.
  */
 int path_attn_fwd_host(const void* q, const void* k, const void* v, const void* w,
                        const float* beta, const float* logf, float scale, void* out,

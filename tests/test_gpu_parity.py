@@ -210,6 +210,20 @@ def test_host_buffer_entry_matches_device_entry():
     assert torch.equal(o1.cpu(), o2) and torch.equal(l1.cpu(), l2)
 
 
+@pytest.mark.parametrize("B,H,dtype,pinned", [(1, 5, "bf16", True), (2, 3, "bf16", False),
+                                               (3, 3, "f32", True)])
+def test_host_buffer_entry_slices_match_device_entry(B, H, dtype, pinned):
+    """The host entry runs the (b, h) problems in slices with overlapped
+    copies; ragged slice counts and pageable buffers give the same bits."""
+    wl = Workload("host_sl", B, H, 300, 64, dtype, seed=9)
+    x = make_inputs(wl)
+    o1, l1 = _run(x)
+    h = {k: (v.pin_memory() if pinned and torch.is_tensor(v) else v) for k, v in x.items()}
+    o2, l2 = pa.path_attn_fwd_host(h["q"], h["k"], h["v"], h["w"], h["beta"], h["logf"],
+                                   h["scale"])
+    assert torch.equal(o1.cpu(), o2) and torch.equal(l1.cpu(), l2)
+
+
 def test_lse_optional_and_no_status_error():
     wl = Workload("nolse", 1, 1, 256, 128, "bf16", seed=2)
     x = make_inputs(wl)
