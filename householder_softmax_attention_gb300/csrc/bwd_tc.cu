@@ -15,8 +15,9 @@
 // Four kernels, each a tcgen05 pipeline (TMA ring -> one MMA-issuing thread
 // -> TMEM accumulators -> warps that convert or apply the softmax):
 //   xwalk   per query chunk b: X walked down c = b-1 .. 0 (X += Xw ngt_c^T,
-//           fp32 master in TMEM, its bf16 copy Xw the A operand), every
-//           X_b^(c) stored (bf16) for the later kernels
+//           fp32 master in TMEM; its bf16 copy Xw, in shared memory, is the
+//           A operand and goes out by a TMA store), every X_b^(c) stored
+//           (bf16) for the later kernels
 //   key     per key chunk c: for b = c (diagonal logits from the
 //           preparation) and b = c+1 .. N-1: S^T = Kr_c X_b^T and
 //           dP^T = V_c dO_b^T, P and dS on 8 warps, dV += P^T dO_b and
@@ -24,7 +25,8 @@
 //           G walk, the diagonal's scale dS written in fp32, row and column
 //           sums of dS for the gate
 //   gwalk   per query chunk b: G walked up c = 0 .. b-1 (G += Gw ngt_c +
-//           dS_bc Kr_c), every G_b^(c-1) stored (bf16), dQl_b written
+//           dS_bc Kr_c, Gw as Xw above), every G_b^(c-1) stored (bf16),
+//           dQl_b written
 //   dF      per chunk c: dF_c = sum_b G^T X over the stored pairs
 // Every mbarrier wait is bounded; on expiry a CTA records a timeout in the
 // status word, stops issuing, drains its copies and MMAs and frees TMEM.
@@ -96,35 +98,64 @@ __device__ __forceinline__ void st_row16(bf16* dst, const uint32_t (&pk)[16]) {
 }
 
 // ============================================================== X walk
+// The bf16 copy of the running query lives in shared memory as a
+// 128-byte-swizzled K-major tile: it is the A operand of the next crossing
+// and, through a TMA tensor store, the stored X_b^(c).
 template <int D>
 struct XwCfg {
-  static constexpr int kStages = 3;
+  static constexpr int kStages = 2;
   static constexpr uint32_t kNgBytes = D * D * 2;
-  static constexpr uint32_t kColX = 0, kColXw = D;
-  static constexpr uint32_t kTmemCols = D == 128 ? 256 : 128;
-  static constexpr size_t kSmemBytes = kStages * kNgBytes + 1024 + 256;
+  static constexpr uint32_t kXwBytes = kC * D * 2;
+  static constexpr uint32_t kOffXw = kStages * kNgBytes;
+  static constexpr uint32_t kTmemCols = D;
+  static constexpr size_t kSmemBytes = kOffXw + kXwBytes + 1024 + 256;
 };
 
 struct XwBars {
-  uint64_t full[3], empty[3];
+  uint64_t full[2], empty[2];
   uint64_t xw_ready, mma_done, final_done;
   uint32_t tmem_base;
   int abort_flag;
 };
 
+// TMA tensor store of a shared-memory box to global (bulk group of the
+// issuing thread); coordinates are never negative here.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, const void* src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_addr(src)), "r"(x), "r"(y)
+               : "memory");
+}
+
+// Barrier of the four converting warps (named barrier 3, 128 threads).
+__device__ __forceinline__ void convert_bar() { asm volatile("bar.sync 3, 128;" ::: "memory"); }
+
+// Writes 32 packed bf16 (16 words, columns col0 .. col0 + 31) of row r into a
+// swizzled K-major [128][D] tile (64-column halves of 16 KB).
+__device__ __forceinline__ void put_row32(uint8_t* tile, int r, int col0, const uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int c8 = (col0 >> 3) + q;
+    const uint32_t off = (c8 >> 3) * (kC * 128) + r * 128 + (((c8 & 7) ^ (r & 7)) << 4);
+    *reinterpret_cast<uint4*>(tile + off) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+  }
+}
+
 // 192 threads: warp 0 TMA (ngt ring), warp 1 TMEM + MMA issue, warps 2-5
-// convert the running query (TMEM lane quarter = warp % 4).
+// convert the running query (TMEM lane quarter = warp % 4; warp 2 lane 0
+// issues the stores).
 template <int D>
 __global__ void __launch_bounds__(192, 2)
-    bwd_xwalk_tc_kernel(const __grid_constant__ CUtensorMap map_ng, const float* __restrict__ ql,
-                        bf16* __restrict__ xs, int* __restrict__ status, int Np, int BH,
-                        size_t npairs) {
+    bwd_xwalk_tc_kernel(const __grid_constant__ CUtensorMap map_ng,
+                        const __grid_constant__ CUtensorMap map_xs, const float* __restrict__ ql,
+                        int* __restrict__ status, int Np, int BH, size_t npairs) {
   using Cfg = XwCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* s_ng = base;
-  XwBars* bars = reinterpret_cast<XwBars*>(base + Cfg::kStages * Cfg::kNgBytes);
+  uint8_t* s_xw = base + Cfg::kOffXw;
+  XwBars* bars = reinterpret_cast<XwBars*>(base + Cfg::kOffXw + Cfg::kXwBytes);
   volatile int* abort_flag = &bars->abort_flag;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   int b, bh;
@@ -136,13 +167,14 @@ __global__ void __launch_bounds__(192, 2)
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
     }
-    mbar_init(&bars->xw_ready, 4);
+    mbar_init(&bars->xw_ready, 1);
     mbar_init(&bars->mma_done, 1);
     mbar_init(&bars->final_done, 1);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) tma_prefetch_map(&map_ng);
+  if (warp == 2 && lane == 0) tma_prefetch_map(&map_xs);
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, Cfg::kTmemCols);
     tmem_relinquish();
@@ -176,7 +208,8 @@ __global__ void __launch_bounds__(192, 2)
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t id = idesc_bf16_f32(128, D, false, false);
-      const uint32_t tX = tb + Cfg::kColX, tXw = tb + Cfg::kColXw;
+      const uint32_t tX = tb;
+      const uint32_t a0 = smem_addr(s_xw);
       bool ok = true;
       for (int n = 0; n < ncross && ok; ++n) {
         const int s = n % Cfg::kStages;
@@ -184,11 +217,12 @@ __global__ void __launch_bounds__(192, 2)
         if (ok) ok = mbar_spin(&bars->xw_ready, n & 1, abort_flag, LIM);
         if (!ok) break;
         tc_fence_after_sync();
-        const uint32_t a = smem_addr(s_ng + s * Cfg::kNgBytes);
+        const uint32_t bb = smem_addr(s_ng + s * Cfg::kNgBytes);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * (D * 128) + (k & 3) * 32;
-          mma_bf16_ts(tX, tXw + k * 8, sdesc_sw128(a + off, 16, 1024), id, 1);
+          const uint32_t offa = (k >> 2) * (kC * 128) + (k & 3) * 32;
+          const uint32_t offb = (k >> 2) * (D * 128) + (k & 3) * 32;
+          mma_bf16_ss(tX, sdesc_sw128(a0 + offa, 16, 1024), sdesc_sw128(bb + offb, 16, 1024), id, 1);
         }
         mma_commit(&bars->mma_done);
         mma_commit(&bars->empty[s]);
@@ -200,13 +234,13 @@ __global__ void __launch_bounds__(192, 2)
   } else {
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;
+    const bool leader = warp == 2 && lane == 0;
     const uint32_t lb = static_cast<uint32_t>(q4 * 32) << 16;
-    const uint32_t tX = tb + lb + Cfg::kColX, tXw = tb + lb + Cfg::kColXw;
+    const uint32_t tX = tb + lb;
     // X_b^(b-1) = Ql_b
     {
       const float4* qrow =
           reinterpret_cast<const float4*>(ql + ((static_cast<size_t>(bh) * Np + b) * kC + r) * D);
-      bf16* xrow = xs + (pair_row(bh, npairs, b, b - 1) + r) * D;
 #pragma unroll
       for (int cc = 0; cc < D; cc += 32) {
         uint32_t m32[32];
@@ -223,12 +257,18 @@ __global__ void __launch_bounds__(192, 2)
 #pragma unroll
         for (int u = 0; u < 16; ++u)
           pk[u] = pack_bf16x2(__uint_as_float(m32[2 * u]), __uint_as_float(m32[2 * u + 1]));
-        tmem_st_x16(tXw + cc / 2, pk);
-        st_row16(xrow + cc, pk);
+        put_row32(s_xw, r, cc, pk);
       }
       tmem_st_wait();
+      fence_proxy_async_smem();
       tc_fence_before_sync();
-      warp_arrive_one(&bars->xw_ready);
+      convert_bar();
+      if (leader) {
+        const int prow = static_cast<int>(pair_row(bh, npairs, b, b - 1));
+        for (int h = 0; h < D / 64; ++h) tma_store_2d(&map_xs, h * 64, prow, s_xw + h * (kC * 128));
+        bulk_commit();
+        mbar_arrive(&bars->xw_ready);
+      }
     }
     bool ok = true;
     for (int n = 0; n < ncross; ++n) {
@@ -236,19 +276,27 @@ __global__ void __launch_bounds__(192, 2)
       ok = mbar_wait(&bars->mma_done, n & 1, abort_flag, LIM);
       if (!ok) break;
       tc_fence_after_sync();
-      bf16* xrow = xs + (pair_row(bh, npairs, b, c - 1) + r) * D;
+      uint32_t pk[D / 2];
 #pragma unroll
-      for (int cc = 0; cc < D; cc += 32) {
-        uint32_t pk[16];
-        ld_pack32(tX + cc, pk);
-        tmem_st_x16(tXw + cc / 2, pk);
-        st_row16(xrow + cc, pk);
-      }
-      tmem_st_wait();
+      for (int cc = 0; cc < D; cc += 32) ld_pack32(tX + cc, *reinterpret_cast<uint32_t(*)[16]>(&pk[cc / 2]));
+      // the previous tile has been read by its store (and by the MMA, done)
+      if (leader) bulk_wait_read<0>();
+      convert_bar();
+#pragma unroll
+      for (int cc = 0; cc < D; cc += 32) put_row32(s_xw, r, cc, *reinterpret_cast<uint32_t(*)[16]>(&pk[cc / 2]));
+      fence_proxy_async_smem();
       tc_fence_before_sync();
-      warp_arrive_one(&bars->xw_ready);
+      convert_bar();
+      if (leader) {
+        const int prow = static_cast<int>(pair_row(bh, npairs, b, c - 1));
+        for (int h = 0; h < D / 64; ++h) tma_store_2d(&map_xs, h * 64, prow, s_xw + h * (kC * 128));
+        bulk_commit();
+        mbar_arrive(&bars->xw_ready);
+      }
     }
     if (!ok) set_timeout(abort_flag, status);
+    // the stores complete before the CTA (and its shared memory) goes away
+    if (leader) bulk_wait<0>();
   }
   teardown_all<192>(warp, tb, Cfg::kTmemCols);
 }
@@ -261,9 +309,10 @@ struct GwCfg {
   static constexpr uint32_t kDsBytes = kC * kC * 2;
   static constexpr uint32_t kKrBytes = kC * D * 2;
   static constexpr uint32_t kStageBytes = kDsBytes + kKrBytes + kNgBytes;
-  static constexpr uint32_t kColG = 0, kColGw = D;
-  static constexpr uint32_t kTmemCols = D == 128 ? 256 : 128;
-  static constexpr size_t kSmemBytes = kStages * kStageBytes + 1024 + 256;
+  static constexpr uint32_t kGwBytes = kC * D * 2;  // bf16 G, swizzled K-major
+  static constexpr uint32_t kOffGw = kStages * kStageBytes;
+  static constexpr uint32_t kTmemCols = D;
+  static constexpr size_t kSmemBytes = kOffGw + kGwBytes + 1024 + 256;
 };
 
 struct GwBars {
@@ -277,8 +326,8 @@ template <int D>
 __global__ void __launch_bounds__(192, 1)
     bwd_gwalk_tc_kernel(const __grid_constant__ CUtensorMap map_ng,
                         const __grid_constant__ CUtensorMap map_ds,
-                        const __grid_constant__ CUtensorMap map_kr, bf16* __restrict__ gs,
-                        float* __restrict__ dql, int* __restrict__ status, int Np, int BH,
+                        const __grid_constant__ CUtensorMap map_kr,
+                        const __grid_constant__ CUtensorMap map_gs, float* __restrict__ dql, int* __restrict__ status, int Np, int BH,
                         size_t npairs, float scale) {
   using Cfg = GwCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -292,7 +341,8 @@ __global__ void __launch_bounds__(192, 1)
   }
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  GwBars* bars = reinterpret_cast<GwBars*>(base + Cfg::kStages * Cfg::kStageBytes);
+  uint8_t* s_gw = base + Cfg::kOffGw;
+  GwBars* bars = reinterpret_cast<GwBars*>(base + Cfg::kOffGw + Cfg::kGwBytes);
   volatile int* abort_flag = &bars->abort_flag;
   const int Tp = Np * kC;
   const uint64_t LIM = kWaitLimitNs;
@@ -302,7 +352,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
     }
-    mbar_init(&bars->gw_ready, 4);
+    mbar_init(&bars->gw_ready, 1);
     mbar_init(&bars->mma_done, 1);
     mbar_init(&bars->final_done, 1);
     bars->abort_flag = 0;
@@ -313,6 +363,7 @@ __global__ void __launch_bounds__(192, 1)
     tma_prefetch_map(&map_ds);
     tma_prefetch_map(&map_kr);
   }
+  if (warp == 2 && lane == 0) tma_prefetch_map(&map_gs);
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, Cfg::kTmemCols);
     tmem_relinquish();
@@ -355,10 +406,10 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0) {
       // G += dS_bc Kr_c: A = dS (queries x keys) read from the stored
       // [keys][queries] tile (MN-major), B = Kr_c (keys x D, MN-major).
-      // G += Gw ngt_c: A = Gw in TMEM, B = ngt_c ([k][n], MN-major).
+      // G += Gw ngt_c: A = Gw (shared memory, K-major), B = ngt_c ([k][n], MN-major).
       constexpr uint32_t idK = idesc_bf16_f32(128, D, true, true);
       constexpr uint32_t idN = idesc_bf16_f32(128, D, false, true);
-      const uint32_t tG = tb + Cfg::kColG, tGw = tb + Cfg::kColGw;
+      const uint32_t tG = tb, gw = smem_addr(s_gw);
       bool ok = true;
       for (int c = 0; c < b && ok; ++c) {
         const int s = c % Cfg::kStages;
@@ -376,7 +427,7 @@ __global__ void __launch_bounds__(192, 1)
         if (c >= 1) {
 #pragma unroll
           for (int k = 0; k < D / 16; ++k)
-            mma_bf16_ts(tG, tGw + k * 8,
+            mma_bf16_ss(tG, sdesc_sw128(gw + (k >> 2) * (kC * 128) + (k & 3) * 32, 16, 1024),
                         sdesc_sw128(sa + Cfg::kDsBytes + Cfg::kKrBytes + k * 2048, D * 128, 1024),
                         idN, 1);
         }
@@ -390,26 +441,33 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;
+    const bool leader = warp == 2 && lane == 0;
     const uint32_t lb = static_cast<uint32_t>(q4 * 32) << 16;
-    const uint32_t tG = tb + lb + Cfg::kColG, tGw = tb + lb + Cfg::kColGw;
+    const uint32_t tG = tb + lb;
     bool ok = true;
     for (int c = 0; c < b; ++c) {
       ok = mbar_wait(&bars->mma_done, c & 1, abort_flag, LIM);
       if (!ok) break;
       tc_fence_after_sync();
       if (c + 1 < b) {
-        // G_b^(c) -> Gw (next step's A operand) and the stored copy for dF
-        bf16* grow = gs + (pair_row(bh, npairs, b, c + 1) + r) * D;
+        // G_b^(c) -> Gw (next step's A operand) and, by a TMA store, the
+        // stored copy for dF; the previous Gw has been read by its store
+        uint32_t pk[D / 2];
 #pragma unroll
-        for (int cc = 0; cc < D; cc += 32) {
-          uint32_t pk[16];
-          ld_pack32(tG + cc, pk);
-          tmem_st_x16(tGw + cc / 2, pk);
-          st_row16(grow + cc, pk);
-        }
-        tmem_st_wait();
+        for (int cc = 0; cc < D; cc += 32) ld_pack32(tG + cc, *reinterpret_cast<uint32_t(*)[16]>(&pk[cc / 2]));
+        if (leader) bulk_wait_read<0>();
+        convert_bar();
+#pragma unroll
+        for (int cc = 0; cc < D; cc += 32) put_row32(s_gw, r, cc, *reinterpret_cast<uint32_t(*)[16]>(&pk[cc / 2]));
+        fence_proxy_async_smem();
         tc_fence_before_sync();
-        warp_arrive_one(&bars->gw_ready);
+        convert_bar();
+        if (leader) {
+          const int prow = static_cast<int>(pair_row(bh, npairs, b, c + 1));
+          for (int h = 0; h < D / 64; ++h) tma_store_2d(&map_gs, h * 64, prow, s_gw + h * (kC * 128));
+          bulk_commit();
+          mbar_arrive(&bars->gw_ready);
+        }
       } else {
         float4* orow = reinterpret_cast<float4*>(
             dql + ((static_cast<size_t>(bh) * Np + b) * kC + r) * D);
@@ -427,6 +485,7 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
     if (!ok) set_timeout(abort_flag, status);
+    if (leader) bulk_wait<0>();
   }
   teardown_all<192>(warp, tb, Cfg::kTmemCols);
 }
@@ -955,12 +1014,10 @@ cudaError_t launch_pairs_tc(const BwdParams& p, int* status, cudaStream_t st) {
     return cudaErrorInvalidValue;
   if (!pairs) mxs = mgs = mds = mkr;  // never dereferenced: no chunk pairs
   cudaError_t e;
-  bf16* xs = static_cast<bf16*>(p.xs);
-  bf16* gs = static_cast<bf16*>(p.gs);
   if (pairs) {
     auto kx = bwd_xwalk_tc_kernel<D>;
     if ((e = set_smem(kx, XwCfg<D>::kSmemBytes)) != cudaSuccess) return e;
-    kx<<<p.BH * (p.Np - 1), 192, XwCfg<D>::kSmemBytes, st>>>(mng, p.ql, xs, status, p.Np, p.BH,
+    kx<<<p.BH * (p.Np - 1), 192, XwCfg<D>::kSmemBytes, st>>>(mng, mxs, p.ql, status, p.Np, p.BH,
                                                               p.npairs);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
@@ -979,7 +1036,7 @@ cudaError_t launch_pairs_tc(const BwdParams& p, int* status, cudaStream_t st) {
   bwd_mark(p.ev, kBwdEvGwalk, st);
   auto kg = bwd_gwalk_tc_kernel<D>;
   if ((e = set_smem(kg, GwCfg<D>::kSmemBytes)) != cudaSuccess) return e;
-  kg<<<p.nch, 192, GwCfg<D>::kSmemBytes, st>>>(mng, mds, mkr, gs, p.dql, status, p.Np, p.BH,
+  kg<<<p.nch, 192, GwCfg<D>::kSmemBytes, st>>>(mng, mds, mkr, mgs, p.dql, status, p.Np, p.BH,
                                                 p.npairs, p.scale);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   bwd_mark(p.ev, kBwdEvDf, st);
