@@ -644,7 +644,7 @@ struct KeyCfg {
 
 struct KeyBars {
   uint64_t kv_full, full[2], empty[2];
-  uint64_t sp_full, pds_ready, p_consumed, ds_consumed, acc_done, final_done;
+  uint64_t s_full, dp_full, p_ready, ds_ready, p_consumed, ds_consumed, acc_done, final_done;
   uint32_t tmem_base;
   int abort_flag;
   float colpart[kC];
@@ -696,8 +696,10 @@ __global__ void __launch_bounds__(kKeyThreads, 1)
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
     }
-    mbar_init(&bars->sp_full, 1);
-    mbar_init(&bars->pds_ready, 8);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->p_ready, 8);
+    mbar_init(&bars->ds_ready, 8);
     mbar_init(&bars->p_consumed, 1);
     mbar_init(&bars->ds_consumed, 1);
     mbar_init(&bars->acc_done, 1);
@@ -775,6 +777,8 @@ __global__ void __launch_bounds__(kKeyThreads, 1)
         const uint32_t sX = sDO + Cfg::kTile;
         ok = mbar_spin(&bars->full[s], (n >> 1) & 1, abort_flag, LIM);
         if (!ok) break;
+        // Per step the pipe runs S^T, dP^T, dV, dKr back to back: P is made
+        // from S while dP^T is computed, dS from dP while dV accumulates.
         if (n >= 1) {
           // S^T = Kr_c X_b^T once P of the previous step has been consumed
           ok = mbar_spin(&bars->p_consumed, (n - 1) & 1, abort_flag, LIM);
@@ -786,6 +790,9 @@ __global__ void __launch_bounds__(kKeyThreads, 1)
             mma_bf16_ss(tS, sdesc_sw128(sKr + off, 16, 1024), sdesc_sw128(sX + off, 16, 1024),
                         idSS, k > 0);
           }
+        }
+        mma_commit(&bars->s_full);
+        if (n >= 1) {
           ok = mbar_spin(&bars->ds_consumed, (n - 1) & 1, abort_flag, LIM);
           if (!ok) break;
         }
@@ -797,8 +804,8 @@ __global__ void __launch_bounds__(kKeyThreads, 1)
           mma_bf16_ss(tDP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sDO + off, 16, 1024),
                       idSS, k > 0);
         }
-        mma_commit(&bars->sp_full);
-        ok = mbar_spin(&bars->pds_ready, n & 1, abort_flag, LIM);
+        mma_commit(&bars->dp_full);
+        ok = mbar_spin(&bars->p_ready, n & 1, abort_flag, LIM);
         if (!ok) break;
         tc_fence_after_sync();
         // dV += P^T dO_b (P^T in TMEM: queries 0-63 at columns 0-31, 64-127 at 64-95)
@@ -807,6 +814,9 @@ __global__ void __launch_bounds__(kKeyThreads, 1)
           mma_bf16_ts(tDV, tS + (k >> 2) * 64 + (k & 3) * 8,
                       sdesc_sw128(sDO + k * 2048, kC * 128, 1024), idAcc, (n > 0 || k > 0));
         mma_commit(&bars->p_consumed);
+        ok = mbar_spin(&bars->ds_ready, n & 1, abort_flag, LIM);
+        if (!ok) break;
+        tc_fence_after_sync();
         if (n >= 1) {
           // dKr += dS^T X_b
 #pragma unroll
@@ -854,43 +864,54 @@ __global__ void __launch_bounds__(kKeyThreads, 1)
       }
       // the stage's vectors (bulk copies) are read here: observe their barrier
       ok = mbar_wait(&bars->full[s], (n >> 1) & 1, abort_flag, LIM);
-      if (ok) ok = mbar_wait(&bars->sp_full, n & 1, abort_flag, LIM);
+      if (ok) ok = mbar_wait(&bars->s_full, n & 1, abort_flag, LIM);
       if (!ok) break;
       tc_fence_after_sync();
-      uint32_t dp[64];
       if (n >= 1) tmem_ld_x64(tS, sv);
-      tmem_ld_x64(tDP, dp);
       const int qlim = T - b * kC - 64 * g;  // columns j < qlim are real queries
-      uint32_t pk[32], dk[32];
+      // P (kept in sv as fp32 bits) and its bf16 copy over S
+      {
+        uint32_t pk[32];
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          float x;
+          if (n == 0) {
+            x = __uint_as_float(sv[j]) - vs[j];
+          } else if (kGate) {
+            x = fmaf(__uint_as_float(sv[j]), sl2, vs[2 * kC + j] - lamk - vs[j]);
+          } else {
+            x = fmaf(__uint_as_float(sv[j]), sl2, -vs[j]);
+          }
+          float p = ex2_approx(x);
+          if (j >= qlim) p = 0.f;
+          sv[j] = __float_as_uint(p);
+        }
+#pragma unroll
+        for (int u = 0; u < 32; ++u) pk[u] = pack_bf16x2(__uint_as_float(sv[2 * u]), __uint_as_float(sv[2 * u + 1]));
+        tmem_st_x32(tS, pk);
+        tmem_st_wait();
+        tc_fence_before_sync();
+        warp_arrive_one(&bars->p_ready);
+      }
+      // dS = P (dP - D) and its bf16 copy over dP
+      ok = mbar_wait(&bars->dp_full, n & 1, abort_flag, LIM);
+      if (!ok) break;
+      tc_fence_after_sync();
+      uint32_t dp[64], dk[32];
+      tmem_ld_x64(tDP, dp);
       float ds[64];
 #pragma unroll
       for (int j = 0; j < 64; ++j) {
-        float x;
-        if (n == 0) {
-          x = __uint_as_float(sv[j]) - vs[j];
-        } else if (kGate) {
-          x = fmaf(__uint_as_float(sv[j]), sl2, vs[2 * kC + j] - lamk - vs[j]);
-        } else {
-          x = fmaf(__uint_as_float(sv[j]), sl2, -vs[j]);
-        }
-        float p = ex2_approx(x);
-        if (j >= qlim) p = 0.f;
-        const float d = p * (__uint_as_float(dp[j]) - vs[kC + j]);
+        const float d = __uint_as_float(sv[j]) * (__uint_as_float(dp[j]) - vs[kC + j]);
         ds[j] = d;
         csum += d;
-        if (j & 1) {
-          pk[j >> 1] = pack_bf16x2(__uint_as_float(sv[j - 1]), p);
-        } else {
-          sv[j] = __float_as_uint(p);
-        }
       }
 #pragma unroll
       for (int u = 0; u < 32; ++u) dk[u] = pack_bf16x2(ds[2 * u], ds[2 * u + 1]);
-      tmem_st_x32(tS, pk);
       tmem_st_x32(tDP, dk);
       tmem_st_wait();
       tc_fence_before_sync();
-      warp_arrive_one(&bars->pds_ready);
+      warp_arrive_one(&bars->ds_ready);
       if (n >= 1) {
         uint4* drow = reinterpret_cast<uint4*>(
             dsbuf + (pair_row(bh, npairs, b, c) + r) * kC + 64 * g);
