@@ -34,6 +34,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <initializer_list>
 
 #include "common.cuh"
 #include "prep_solve.cuh"
@@ -605,16 +606,64 @@ struct GemmCtx {
 cudaError_t gemm(const GemmCtx& gx, int batch, int M, int N, int K, float alpha, const float* A,
                  int lda, long long sA, bool tA, const float* B, int ldb, long long sB, bool tB,
                  float* Cm, int ldc, long long sC, bool acc, int mask) {
-  if (gx.tc && gemm_tc_supported(M, N, K, lda, ldb, ldc)) {
-    TcGemm t{A, B, Cm, sA, sB, sC, lda, ldb, ldc, M, N, K, batch, mask, tA, tB, acc, alpha,
-             gx.status};
-    return launch_gemm_tc(t, gx.st);
-  }
   cudaStream_t st = gx.st;
   GemmArg g{A, B, Cm, sA, sB, sC, lda, ldb, ldc, M, N, K, batch, mask, tA, tB, acc, alpha};
   const dim3 grid(N / 64, M / 64, batch < 65535 ? batch : 65535);
   gemm_batched_kernel<<<grid, 256, 0, st>>>(g);
   return cudaGetLastError();
+}
+
+// One product alpha op(A) op(B) with K = the shared dimension.
+struct Term {
+  float alpha;
+  const float* A;
+  int lda;
+  long long sA;
+  bool tA;
+  const float* B;
+  int ldb;
+  long long sB;
+  bool tB;
+  int K;
+};
+
+// C = mask(sum of the terms + add) over the batch; add may be null or C.  The
+// tensor-core kernel does it in one launch; the fp32 path copies add into C
+// and accumulates the terms one GEMM at a time.
+cudaError_t mgemm(const GemmCtx& gx, int batch, int M, int N, std::initializer_list<Term> terms,
+                  float* Cm, int ldc, long long sC, const float* add, int mask) {
+  if (gx.tc) {
+    TcGemmN g{};
+    g.nterms = 0;
+    for (const Term& t : terms) {
+      if (g.nterms == kMaxTerms) return cudaErrorInvalidValue;
+      g.t[g.nterms++] = TcTerm{t.A, t.B, t.sA, t.sB, t.lda, t.ldb, t.K, t.tA, t.tB, t.alpha};
+    }
+    g.Cm = Cm;
+    g.Add = add;
+    g.sC = g.sAdd = sC;
+    g.ldc = g.ldadd = ldc;
+    g.M = M;
+    g.N = N;
+    g.batch = batch;
+    g.mask = mask;
+    g.status = gx.status;
+    if (gemm_tc_supported(g)) return launch_gemm_tc(g, gx.st);
+  }
+  cudaError_t e;
+  if (add && add != Cm &&
+      (e = cudaMemcpyAsync(Cm, add, static_cast<size_t>(batch) * sC * sizeof(float),
+                           cudaMemcpyDeviceToDevice, gx.st)) != cudaSuccess)
+    return e;
+  const GemmCtx simt{gx.st, false, gx.status};
+  bool acc = add != nullptr;
+  for (const Term& t : terms) {
+    if ((e = gemm(simt, batch, M, N, t.K, t.alpha, t.A, t.lda, t.sA, t.tA, t.B, t.ldb, t.sB, t.tB,
+                  Cm, ldc, sC, acc, mask)) != cudaSuccess)
+      return e;
+    acc = true;
+  }
+  return cudaSuccess;
 }
 
 template <typename ET, int D>
@@ -645,8 +694,20 @@ cudaError_t launch_bwd_t(const BwdParams& p, const ChunkBufs& cb, cudaStream_t s
                   dd = static_cast<long long>(D) * D;
   bwd_chunk_inputs_kernel<ET><<<1024, 256, 0, st>>>(p, cb);
   const float *W = cb.Wf, *K = cb.Kf, *Q = cb.Qf;
+  // Products of [C][C] (cc) and [C][D] (cd) per-chunk matrices; a Term lists
+  // alpha, A, its leading dimension and batch stride, whether it is
+  // transposed, the same for B, and the shared dimension.
+  auto CC = [&](float al, const float* A, bool tA, const float* B, bool tB) {
+    return Term{al, A, C, cc, tA, B, C, cc, tB, C};
+  };
+  auto CD_DC = [&](float al, const float* A, bool tA, const float* B, bool tB) {  // [C][D] x [D][C]
+    return Term{al, A, D, cd, tA, B, D, cd, tB, D};
+  };
+  auto CC_CD = [&](float al, const float* A, bool tA, const float* B) {  // [C][C] x [C][D]
+    return Term{al, A, C, cc, tA, B, D, cd, false, C};
+  };
   // forward factors
-  if ((e = gemm(gx, nch, C, C, D, 1.f, W, D, cd, false, W, D, cd, true, cb.GWW, C, cc, false, 0)))
+  if ((e = mgemm(gx, nch, C, C, {CD_DC(1.f, W, false, W, true)}, cb.GWW, C, cc, nullptr, 0)))
     return e;
   bwd_chunk_elem_kernel<<<nch, 256, 0, st>>>(cb.GWW, cb.Lm, cb.bf, C, 0);
   if (C == 128) {
@@ -663,59 +724,59 @@ cudaError_t launch_bwd_t(const BwdParams& p, const ChunkBufs& cb, cudaStream_t s
     bwd_tri_inv_kernel<<<nch, C, tri_smem, st>>>(cb.Lm, cb.Xi, C);
   }
   bwd_chunk_elem_kernel<<<nch, 256, 0, st>>>(cb.Xi, cb.U, cb.bf, C, 1);
-  if ((e = gemm(gx, nch, C, C, D, 1.f, W, D, cd, false, K, D, cd, true, cb.Nm, C, cc, false, 2)) ||
-      (e = gemm(gx, nch, C, C, C, 1.f, cb.U, C, cc, false, cb.Nm, C, cc, false, cb.TK, C, cc, false, 0)) ||
-      (e = gemm(gx, nch, C, D, C, 1.f, cb.U, C, cc, false, W, D, cd, false, cb.UW, D, cd, false, 0)) ||
-      (e = gemm(gx, nch, C, C, D, 1.f, Q, D, cd, false, W, D, cd, true, cb.Mm, C, cc, false, 1)))
+  if ((e = mgemm(gx, nch, C, C, {CD_DC(1.f, W, false, K, true)}, cb.Nm, C, cc, nullptr, 2)) ||
+      (e = mgemm(gx, nch, C, C, {CC(1.f, cb.U, false, cb.Nm, false)}, cb.TK, C, cc, nullptr, 0)) ||
+      (e = mgemm(gx, nch, C, D, {CC_CD(1.f, cb.U, false, W)}, cb.UW, D, cd, nullptr, 0)) ||
+      (e = mgemm(gx, nch, C, C, {CD_DC(1.f, Q, false, W, true)}, cb.Mm, C, cc, nullptr, 1)))
     return e;
   const float *dQl = p.dql, *dKr = p.dkr, *dF = p.dF, *dA = p.dad;
-  // dM = -dQl UW^T - dA TK^T, dMl = lower(dM)
-  if ((e = gemm(gx, nch, C, C, D, -1.f, dQl, D, cd, false, cb.UW, D, cd, true, cb.dM, C, cc, false, 0)) ||
-      (e = gemm(gx, nch, C, C, C, -1.f, dA, C, cc, false, cb.TK, C, cc, true, cb.dM, C, cc, true, 1)))
+  // dM = lower(-dQl UW^T - dA TK^T)
+  if ((e = mgemm(gx, nch, C, C, {CD_DC(-1.f, dQl, false, cb.UW, true), CC(-1.f, dA, false, cb.TK, true)},
+                 cb.dM, C, cc, nullptr, 1)))
     return e;
-  // dQ = dQl + dA K + dMl W
-  if ((e = cudaMemcpyAsync(cb.dQf, dQl, static_cast<size_t>(nch) * cd * 4, cudaMemcpyDeviceToDevice, st)) ||
-      (e = gemm(gx, nch, C, D, C, 1.f, dA, C, cc, false, K, D, cd, false, cb.dQf, D, cd, true, 0)) ||
-      (e = gemm(gx, nch, C, D, C, 1.f, cb.dM, C, cc, false, W, D, cd, false, cb.dQf, D, cd, true, 0)))
+  // dQ = dQl + dA K + dM W
+  if ((e = mgemm(gx, nch, C, D, {CC_CD(1.f, dA, false, K), CC_CD(1.f, cb.dM, false, W)}, cb.dQf, D,
+                 cd, dQl, 0)))
     return e;
   // dTK = -W dKr^T - M^T dA ; dUW = -M^T dQl
-  if ((e = gemm(gx, nch, C, C, D, -1.f, W, D, cd, false, dKr, D, cd, true, cb.dTK, C, cc, false, 0)) ||
-      (e = gemm(gx, nch, C, C, C, -1.f, cb.Mm, C, cc, true, dA, C, cc, false, cb.dTK, C, cc, true, 0)) ||
-      (e = gemm(gx, nch, C, D, C, -1.f, cb.Mm, C, cc, true, dQl, D, cd, false, cb.dUW, D, cd, false, 0)))
+  if ((e = mgemm(gx, nch, C, C, {CD_DC(-1.f, W, false, dKr, true), CC(-1.f, cb.Mm, true, dA, false)},
+                 cb.dTK, C, cc, nullptr, 0)) ||
+      (e = mgemm(gx, nch, C, D, {CC_CD(-1.f, cb.Mm, true, dQl)}, cb.dUW, D, cd, nullptr, 0)))
     return e;
   // dN = strictLower(U^T dTK); dK = dKr + dA^T Q + dN^T W
-  if ((e = gemm(gx, nch, C, C, C, 1.f, cb.U, C, cc, true, cb.dTK, C, cc, false, cb.dN, C, cc, false, 2)) ||
-      (e = cudaMemcpyAsync(cb.dKf, dKr, static_cast<size_t>(nch) * cd * 4, cudaMemcpyDeviceToDevice, st)) ||
-      (e = gemm(gx, nch, C, D, C, 1.f, dA, C, cc, true, Q, D, cd, false, cb.dKf, D, cd, true, 0)) ||
-      (e = gemm(gx, nch, C, D, C, 1.f, cb.dN, C, cc, true, W, D, cd, false, cb.dKf, D, cd, true, 0)))
+  if ((e = mgemm(gx, nch, C, C, {CC(1.f, cb.U, true, cb.dTK, false)}, cb.dN, C, cc, nullptr, 2)) ||
+      (e = mgemm(gx, nch, C, D, {CC_CD(1.f, dA, true, Q), CC_CD(1.f, cb.dN, true, W)}, cb.dKf, D, cd,
+                 dKr, 0)))
     return e;
-  // P1 = W dF, P2 = W dF^T
-  if ((e = gemm(gx, nch, C, D, D, 1.f, W, D, cd, false, dF, D, dd, false, cb.P1, D, cd, false, 0)) ||
-      (e = gemm(gx, nch, C, D, D, 1.f, W, D, cd, false, dF, D, dd, true, cb.P2, D, cd, false, 0)))
+  // P1 = W dF, P2 = W dF^T  ([C][D] x [D][D])
+  if ((e = mgemm(gx, nch, C, D, {Term{1.f, W, D, cd, false, dF, D, dd, false, D}}, cb.P1, D, cd,
+                 nullptr, 0)) ||
+      (e = mgemm(gx, nch, C, D, {Term{1.f, W, D, cd, false, dF, D, dd, true, D}}, cb.P2, D, cd,
+                 nullptr, 0)))
     return e;
   // dU = -P2 W^T + dTK N^T + dUW W^T
-  if ((e = gemm(gx, nch, C, C, D, -1.f, cb.P2, D, cd, false, W, D, cd, true, cb.dU, C, cc, false, 0)) ||
-      (e = gemm(gx, nch, C, C, C, 1.f, cb.dTK, C, cc, false, cb.Nm, C, cc, true, cb.dU, C, cc, true, 0)) ||
-      (e = gemm(gx, nch, C, C, D, 1.f, cb.dUW, D, cd, false, W, D, cd, true, cb.dU, C, cc, true, 0)))
+  if ((e = mgemm(gx, nch, C, C,
+                 {CD_DC(-1.f, cb.P2, false, W, true), CC(1.f, cb.dTK, false, cb.Nm, true),
+                  CD_DC(1.f, cb.dUW, false, W, true)},
+                 cb.dU, C, cc, nullptr, 0)))
     return e;
-  // dW = -TK dKr - U P1 - U^T P2 + dMl^T Q + dN K + U^T dUW  (+ the Lm terms below)
-  if ((e = gemm(gx, nch, C, D, C, -1.f, cb.TK, C, cc, false, dKr, D, cd, false, cb.dWf, D, cd, false, 0)) ||
-      (e = gemm(gx, nch, C, D, C, -1.f, cb.U, C, cc, false, cb.P1, D, cd, false, cb.dWf, D, cd, true, 0)) ||
-      (e = gemm(gx, nch, C, D, C, -1.f, cb.U, C, cc, true, cb.P2, D, cd, false, cb.dWf, D, cd, true, 0)) ||
-      (e = gemm(gx, nch, C, D, C, 1.f, cb.dM, C, cc, true, Q, D, cd, false, cb.dWf, D, cd, true, 0)) ||
-      (e = gemm(gx, nch, C, D, C, 1.f, cb.dN, C, cc, false, K, D, cd, false, cb.dWf, D, cd, true, 0)) ||
-      (e = gemm(gx, nch, C, D, C, 1.f, cb.U, C, cc, true, cb.dUW, D, cd, false, cb.dWf, D, cd, true, 0)))
+  // dW = -TK dKr - U P1 - U^T P2 + dM^T Q + dN K + U^T dUW  (+ the Lm terms below)
+  if ((e = mgemm(gx, nch, C, D,
+                 {CC_CD(-1.f, cb.TK, false, dKr), CC_CD(-1.f, cb.U, false, cb.P1),
+                  CC_CD(-1.f, cb.U, true, cb.P2), CC_CD(1.f, cb.dM, true, Q),
+                  CC_CD(1.f, cb.dN, false, K), CC_CD(1.f, cb.U, true, cb.dUW)},
+                 cb.dWf, D, cd, nullptr, 0)))
     return e;
   // dXi = dU diag(beta); T1 = Xi^T dXi; dLm = strictLower(-T1 Xi^T)
   bwd_chunk_elem_kernel<<<nch, 256, 0, st>>>(cb.dU, cb.dXi, cb.bf, C, 1);
-  if ((e = gemm(gx, nch, C, C, C, 1.f, cb.Xi, C, cc, true, cb.dXi, C, cc, false, cb.T1, C, cc, false, 0)) ||
-      (e = gemm(gx, nch, C, C, C, -1.f, cb.T1, C, cc, false, cb.Xi, C, cc, true, cb.dLm, C, cc, false, 2)))
+  if ((e = mgemm(gx, nch, C, C, {CC(1.f, cb.Xi, true, cb.dXi, false)}, cb.T1, C, cc, nullptr, 0)) ||
+      (e = mgemm(gx, nch, C, C, {CC(-1.f, cb.T1, false, cb.Xi, true)}, cb.dLm, C, cc, nullptr, 2)))
     return e;
   bwd_dbeta_kernel<<<nch, C, 0, st>>>(cb.Xi, cb.dU, cb.dLm, cb.GWW, cb.dbf, C);
   // BL = diag(beta) dLm; dW += BL W + BL^T W
   bwd_chunk_elem_kernel<<<nch, 256, 0, st>>>(cb.dLm, cb.BL, cb.bf, C, 2);
-  if ((e = gemm(gx, nch, C, D, C, 1.f, cb.BL, C, cc, false, W, D, cd, false, cb.dWf, D, cd, true, 0)) ||
-      (e = gemm(gx, nch, C, D, C, 1.f, cb.BL, C, cc, true, W, D, cd, false, cb.dWf, D, cd, true, 0)))
+  if ((e = mgemm(gx, nch, C, D, {CC_CD(1.f, cb.BL, false, W), CC_CD(1.f, cb.BL, true, W)}, cb.dWf,
+                 D, cd, cb.dWf, 0)))
     return e;
   bwd_chunk_outputs_kernel<ET><<<1024, 256, 0, st>>>(p, cb);
   if (p.dlogf) bwd_gate_kernel<<<p.BH, 1024, 0, st>>>(p);

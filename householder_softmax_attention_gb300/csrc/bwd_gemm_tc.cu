@@ -1,21 +1,23 @@
 // bwd_gemm_tc.cu -- batched small GEMMs of the backward's chunk pass on the
 // sm_103a tensor cores.
 //
-//   C[z] = mask(alpha op(A[z]) op(B[z]) + (acc ? C[z] : 0)),   z = 0 .. batch-1
+//   C[z] = mask(sum_t alpha_t op(A_t[z]) op(B_t[z]) + (Add ? Add[z] : 0)),
+//   z = 0 .. batch-1, up to kMaxTerms products t
 //
-// fp32 row-major operands (M = 128 rows, N and K in {64, 128}), one CTA of
-// four warps per batch item.  Each fp32 operand enters the MMA as
+// fp32 row-major operands (M = 128 rows, N and every K_t in {64, 128}), one
+// CTA of four warps per batch item.  Each fp32 operand enters the MMA as
 // x_hi + x_lo with x_hi = bf16(x), x_lo = bf16(x - x_hi) (about 16
-// significant bits); the three products hi*hi + hi*lo + lo*hi accumulate in
-// fp32 in TMEM.  K is consumed in slices of 64: the CTA converts a slice of A
-// and B into 128-byte-swizzled shared-memory tiles (op(A) K-major unless A is
-// transposed, op(B) MN-major unless B is transposed, so that every global
-// read is along a stored row), one thread issues the twelve MMAs of the
-// slice, and the next slice is written once they have completed.  The
-// accumulator goes from TMEM (one row per thread) through shared memory, so
-// that the epilogue (alpha, accumulate, mask) reads and writes C in coalesced
-// rows.  Three CTAs fit on an SM, so conversion, MMAs and epilogues of
-// different batch items overlap.
+// significant bits; alpha_t is applied to A_t before the split, exactly for
+// alpha = +-1); the three products hi*hi + hi*lo + lo*hi of every term
+// accumulate in fp32 in one TMEM accumulator, so a sum of products costs one
+// launch and one write of C.  Each K slice of 64 is converted into
+// 128-byte-swizzled shared-memory tiles (op(A) K-major unless A is transposed,
+// op(B) MN-major unless B is transposed, so that every global read is along
+// a stored row), one thread issues the slice's twelve MMAs, and the next
+// slice is written once they have completed.  The accumulator goes from TMEM
+// (one row per thread) through shared memory, so that the epilogue (addend,
+// mask) reads and writes in coalesced rows.  Three CTAs fit on an SM, so
+// conversion, MMAs and epilogues of different batch items overlap.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -44,11 +46,11 @@ __device__ __forceinline__ uint32_t swz_off(int rows, int row, int col) {
          ((col & 7) << 1);
 }
 
-// Converts a stored tile (rows x cols fp32, global, leading dimension ld)
-// into bf16 hi / lo swizzled tiles; each thread has four 8-column groups of
-// loads in flight before it converts them.
+// Converts a stored tile (rows x cols fp32, global, leading dimension ld),
+// times `mul`, into bf16 hi / lo swizzled tiles; each thread has four
+// 8-column groups of loads in flight before it converts them.
 __device__ __forceinline__ void load_split(const float* __restrict__ src, int ld, int rows, int cols,
-                                           uint8_t* hi, uint8_t* lo) {
+                                           float mul, uint8_t* hi, uint8_t* lo) {
   const int groups = rows * cols / 8;  // a multiple of 4 * kThreads
   const int gpr = cols / 8;
   for (int g0 = threadIdx.x; g0 < groups; g0 += 4 * kThreads) {
@@ -63,7 +65,8 @@ __device__ __forceinline__ void load_split(const float* __restrict__ src, int ld
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int gi = g0 + u * kThreads, r = gi / gpr, c8 = gi - r * gpr;
-      const float v[8] = {a[u].x, a[u].y, a[u].z, a[u].w, b[u].x, b[u].y, b[u].z, b[u].w};
+      const float v[8] = {mul * a[u].x, mul * a[u].y, mul * a[u].z, mul * a[u].w,
+                          mul * b[u].x, mul * b[u].y, mul * b[u].z, mul * b[u].w};
       uint32_t h[4], l[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -78,20 +81,14 @@ __device__ __forceinline__ void load_split(const float* __restrict__ src, int ld
   }
 }
 
-template <int N, bool kTA, bool kTB>
-__global__ void __launch_bounds__(kThreads, 3)
-    gemm_tc_kernel(const float* __restrict__ A, const float* __restrict__ B, float* __restrict__ Cm,
-                   long long sA, long long sB, long long sC, int lda, int ldb, int ldc, int K,
-                   int mask, int acc, float alpha, int* __restrict__ status) {
+template <int N>
+__global__ void __launch_bounds__(kThreads, 3) gemm_tc_kernel(const __grid_constant__ TcGemmN g) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   GemmBars* bars = reinterpret_cast<GemmBars*>(base + 2 * kSliceA + 2 * kSliceB);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const size_t z = blockIdx.x;
-  const float* Az = A + z * sA;
-  const float* Bz = B + z * sB;
-  float* Cz = Cm + z * sC;
   if (threadIdx.x == 0) {
     mbar_init(&bars->mma, 1);
     bars->abort_flag = 0;
@@ -105,51 +102,57 @@ __global__ void __launch_bounds__(kThreads, 3)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tb = bars->tmem_base;
-  constexpr uint32_t id = idesc_bf16_f32(kM, N, kTA, !kTB);
   bool ok = true;
-  const int nslices = K / kKs;
-  for (int s = 0; s < nslices && ok; ++s) {
-    const int k0 = s * kKs;
-    // op(A) slice: A[m][k0..] (K-major) or A[k0..][m] (MN-major)
-    if (kTA)
-      load_split(Az + static_cast<size_t>(k0) * lda, lda, kKs, kM, base, base + kOffAlo);
-    else
-      load_split(Az + k0, lda, kM, kKs, base, base + kOffAlo);
-    // op(B) slice: B[k0..][n] (MN-major) or B[n][k0..] (K-major)
-    if (kTB)
-      load_split(Bz + k0, ldb, N, kKs, base + kOffBhi, base + kOffBlo);
-    else
-      load_split(Bz + static_cast<size_t>(k0) * ldb, ldb, kKs, N, base + kOffBhi, base + kOffBlo);
-    fence_proxy_async_smem();
-    tc_fence_before_sync();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      tc_fence_after_sync();
-      const uint32_t a0 = smem_addr(base), b0 = smem_addr(base + kOffBhi);
+  int sl = 0;  // slices issued so far (phase of the MMA barrier)
+  for (int t = 0; t < g.nterms && ok; ++t) {
+    const TcTerm& tt = g.t[t];
+    const float* Az = tt.A + z * tt.sA;
+    const float* Bz = tt.B + z * tt.sB;
+    const uint32_t id = idesc_bf16_f32(kM, N, tt.tA, !tt.tB);
+    for (int k0 = 0; k0 < tt.K && ok; k0 += kKs, ++sl) {
+      // op(A) slice: A[m][k0..] (K-major) or A[k0..][m] (MN-major), times alpha
+      if (tt.tA)
+        load_split(Az + static_cast<size_t>(k0) * tt.lda, tt.lda, kKs, kM, tt.alpha, base,
+                   base + kOffAlo);
+      else
+        load_split(Az + k0, tt.lda, kM, kKs, tt.alpha, base, base + kOffAlo);
+      // op(B) slice: B[k0..][n] (MN-major) or B[n][k0..] (K-major)
+      if (tt.tB)
+        load_split(Bz + k0, tt.ldb, N, kKs, 1.f, base + kOffBhi, base + kOffBlo);
+      else
+        load_split(Bz + static_cast<size_t>(k0) * tt.ldb, tt.ldb, kKs, N, 1.f, base + kOffBhi,
+                   base + kOffBlo);
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        tc_fence_after_sync();
+        const uint32_t a0 = smem_addr(base), b0 = smem_addr(base + kOffBhi);
 #pragma unroll
-      for (int term = 0; term < 3; ++term) {
-        const uint32_t at = a0 + (term == 2 ? kOffAlo : 0);
-        const uint32_t bt = b0 + (term == 1 ? kSliceB : 0);
+        for (int term = 0; term < 3; ++term) {
+          const uint32_t at = a0 + (term == 2 ? kOffAlo : 0);
+          const uint32_t bt = b0 + (term == 1 ? kSliceB : 0);
 #pragma unroll
-        for (int k = 0; k < kKs / 16; ++k) {
-          const uint64_t ad = kTA ? sdesc_sw128(at + k * 2048, kKs * 128, 1024)
-                                  : sdesc_sw128(at + k * 32, 16, 1024);
-          const uint64_t bd = kTB ? sdesc_sw128(bt + k * 32, 16, 1024)
-                                  : sdesc_sw128(bt + k * 2048, kKs * 128, 1024);
-          mma_bf16_ss(tb, ad, bd, id, (s > 0 || term > 0 || k > 0));
+          for (int k = 0; k < kKs / 16; ++k) {
+            const uint64_t ad = tt.tA ? sdesc_sw128(at + k * 2048, kKs * 128, 1024)
+                                      : sdesc_sw128(at + k * 32, 16, 1024);
+            const uint64_t bd = tt.tB ? sdesc_sw128(bt + k * 32, 16, 1024)
+                                      : sdesc_sw128(bt + k * 2048, kKs * 128, 1024);
+            mma_bf16_ss(tb, ad, bd, id, (sl > 0 || term > 0 || k > 0));
+          }
         }
+        mma_commit(&bars->mma);
       }
-      mma_commit(&bars->mma);
+      // the slice's tiles are free (and, after the last, the accumulator final)
+      // once its MMAs have completed
+      ok = mbar_wait(&bars->mma, sl & 1, &bars->abort_flag, kWaitLimitNs);
+      tc_fence_after_sync();
     }
-    // the slice's tiles are free (and, after the last, the accumulator final)
-    // once its MMAs have completed
-    ok = mbar_wait(&bars->mma, s & 1, &bars->abort_flag, kWaitLimitNs);
-    tc_fence_after_sync();
   }
   if (ok) {
     // accumulator rows (one per thread) -> shared memory (the slice tiles are
     // free), 16-byte units of a row rotated by the row index; then the tile
-    // goes out in row-major order, so that reads of C and writes are coalesced
+    // goes out in row-major order, so that reads of Add and writes are coalesced
     const int m = warp * 32 + lane;
     const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
     float4* stile = reinterpret_cast<float4*>(base);
@@ -167,28 +170,28 @@ __global__ void __launch_bounds__(kThreads, 3)
       }
     }
     __syncthreads();
+    float* Cz = g.Cm + z * g.sC;
+    const float* Dz = g.Add ? g.Add + z * g.sAdd : nullptr;
 #pragma unroll 4
     for (int idx = threadIdx.x; idx < kM * kU; idx += kThreads) {
       const int r = idx / kU, j = idx - r * kU;
       float4 o = stile[r * kU + (j ^ (r & 7))];
-      o.x *= alpha; o.y *= alpha; o.z *= alpha; o.w *= alpha;
-      float4* dst = reinterpret_cast<float4*>(Cz + static_cast<size_t>(r) * ldc + 4 * j);
-      if (acc) {
-        const float4 c = *dst;
+      if (Dz) {
+        const float4 c = *reinterpret_cast<const float4*>(Dz + static_cast<size_t>(r) * g.ldadd + 4 * j);
         o.x += c.x; o.y += c.y; o.z += c.z; o.w += c.w;
       }
-      if (mask != 0) {
-        const int lim = mask == 1 ? r : r - 1;  // keep n <= lim
+      if (g.mask != 0) {
+        const int lim = g.mask == 1 ? r : r - 1;  // keep n <= lim
         const int n0 = 4 * j;
         if (n0 > lim) o.x = 0.f;
         if (n0 + 1 > lim) o.y = 0.f;
         if (n0 + 2 > lim) o.z = 0.f;
         if (n0 + 3 > lim) o.w = 0.f;
       }
-      *dst = o;
+      *reinterpret_cast<float4*>(Cz + static_cast<size_t>(r) * g.ldc + 4 * j) = o;
     }
   } else if (threadIdx.x == 0) {
-    atomicExch(status, PATH_DEV_ERR_TIMEOUT);
+    atomicExch(g.status, PATH_DEV_ERR_TIMEOUT);
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -198,34 +201,31 @@ __global__ void __launch_bounds__(kThreads, 3)
   }
 }
 
-template <int N, bool kTA, bool kTB>
-cudaError_t launch_t(const TcGemm& g, cudaStream_t st) {
-  auto kern = gemm_tc_kernel<N, kTA, kTB>;
+template <int N>
+cudaError_t launch_n(const TcGemmN& g, cudaStream_t st) {
+  auto kern = gemm_tc_kernel<N>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
-  kern<<<g.batch, kThreads, kSmemBytes, st>>>(g.A, g.B, g.Cm, g.sA, g.sB, g.sC, g.lda, g.ldb,
-                                              g.ldc, g.K, g.mask, g.acc ? 1 : 0, g.alpha,
-                                              g.status);
+  kern<<<g.batch, kThreads, kSmemBytes, st>>>(g);
   return cudaGetLastError();
-}
-
-template <int N>
-cudaError_t launch_n(const TcGemm& g, cudaStream_t st) {
-  if (g.tA) return g.tB ? launch_t<N, true, true>(g, st) : launch_t<N, true, false>(g, st);
-  return g.tB ? launch_t<N, false, true>(g, st) : launch_t<N, false, false>(g, st);
 }
 
 }  // namespace
 
-bool gemm_tc_supported(int M, int N, int K, int lda, int ldb, int ldc) {
-  return M == kM && (N == 64 || N == 128) && (K == 64 || K == 128) && lda % 8 == 0 &&
-         ldb % 8 == 0 && ldc % 4 == 0;
+bool gemm_tc_supported(const TcGemmN& g) {
+  if (g.M != kM || (g.N != 64 && g.N != 128) || g.nterms < 1 || g.nterms > kMaxTerms ||
+      g.ldc % 4 != 0 || (g.Add && g.ldadd % 4 != 0))
+    return false;
+  for (int t = 0; t < g.nterms; ++t) {
+    const TcTerm& tt = g.t[t];
+    if ((tt.K != 64 && tt.K != 128) || tt.lda % 8 != 0 || tt.ldb % 8 != 0) return false;
+  }
+  return true;
 }
 
-cudaError_t launch_gemm_tc(const TcGemm& g, cudaStream_t st) {
-  if (!gemm_tc_supported(g.M, g.N, g.K, g.lda, g.ldb, g.ldc) || g.batch < 1)
-    return cudaErrorInvalidValue;
+cudaError_t launch_gemm_tc(const TcGemmN& g, cudaStream_t st) {
+  if (!gemm_tc_supported(g) || g.batch < 1) return cudaErrorInvalidValue;
   return g.N == 128 ? launch_n<128>(g, st) : launch_n<64>(g, st);
 }
 

@@ -209,22 +209,31 @@ cudaError_t launch_bwd(const BwdParams& p, const ChunkBufs& cb, cudaStream_t st)
 // bf16, d = 64 or 128, C = 128: the chunk-pair kernels on tcgen05 (bwd_tc.cu):
 // fills xs, gs, ds, dql, dkr, dF, dad, dv, colsum, rowsum from dvec and lse2.
 cudaError_t launch_bwd_pairs_tc(const BwdParams& p, int* status, cudaStream_t st);
-// Batched C[z] = mask(alpha op(A[z]) op(B[z]) + (acc ? C[z] : 0)) for the
+// Batched C[z] = mask(sum_t alpha_t op(A_t[z]) op(B_t[z]) + Add[z]) for the
 // backward's chunk pass on tcgen05 (bwd_gemm_tc.cu): fp32 row-major operands
-// split into bf16 hi + lo, M = 128, N and K in {64, 128}.  mask 0: none,
+// split into bf16 hi + lo, M = 128, N and every K_t in {64, 128}; op(X) = X^T
+// when tX.  Add may be null (nothing added) or alias Cm.  mask 0: none,
 // 1: keep n <= m, 2: keep n < m (others written as 0).
-struct TcGemm {
+constexpr int kMaxTerms = 6;
+struct TcTerm {
   const float* A;
   const float* B;
-  float* Cm;
-  long long sA, sB, sC;
-  int lda, ldb, ldc, M, N, K, batch, mask;
-  bool tA, tB, acc;
+  long long sA, sB;
+  int lda, ldb, K;
+  bool tA, tB;
   float alpha;
+};
+struct TcGemmN {
+  TcTerm t[kMaxTerms];
+  int nterms;
+  float* Cm;
+  const float* Add;
+  long long sC, sAdd;
+  int ldc, ldadd, M, N, batch, mask;
   int* status;
 };
-bool gemm_tc_supported(int M, int N, int K, int lda, int ldb, int ldc);
-cudaError_t launch_gemm_tc(const TcGemm& g, cudaStream_t st);
+bool gemm_tc_supported(const TcGemmN& g);
+cudaError_t launch_gemm_tc(const TcGemmN& g, cudaStream_t st);
 // Diagnostics: a kernel whose bounded wait can only expire (sets *status).
 cudaError_t launch_debug_wait(int* status, unsigned long long limit_ns, cudaStream_t st);
 
