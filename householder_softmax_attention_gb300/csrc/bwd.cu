@@ -55,6 +55,11 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+__device__ __forceinline__ uint32_t pack_bf16_pair(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 __device__ __forceinline__ size_t pair_index(int b, int c) {
   return static_cast<size_t>(b) * (b - 1) / 2 + c;
 }
@@ -370,21 +375,59 @@ __global__ void __launch_bounds__(256) bwd_dF_kernel(BwdParams p) {
 }
 
 // ---------------------------------------------------------- chunk helpers
-// fp32 copies of w, k, q (zero rows past T) and beta (zero past T), per chunk
+// fp32 copies of w, k, q (zero rows past T) and beta (zero past T), per
+// chunk.  Grid (groups of a head / 256, BH); a thread converts 8 consecutive
+// elements of one row.
+__device__ __forceinline__ void ld8(const float* p, float (&v)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void ld8(const bf16* p, float (&v)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    v[2 * e] = __uint_as_float(w[e] << 16);
+    v[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+  }
+}
+__device__ __forceinline__ void st8(float* p, const float (&v)[8]) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
+}
+__device__ __forceinline__ void st8(bf16* p, const float (&v)[8]) {
+  uint4 u;
+  u.x = pack_bf16_pair(v[0], v[1]);
+  u.y = pack_bf16_pair(v[2], v[3]);
+  u.z = pack_bf16_pair(v[4], v[5]);
+  u.w = pack_bf16_pair(v[6], v[7]);
+  *reinterpret_cast<uint4*>(p) = u;
+}
+
 template <typename ET>
-__global__ void bwd_chunk_inputs_kernel(BwdParams p, ChunkBufs cb) {
-  const size_t total = static_cast<size_t>(p.BH) * p.Tp * p.d;
-  for (size_t x = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; x < total;
-       x += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const size_t row = x / p.d;
-    const int e = static_cast<int>(x % p.d);
-    const int bh = static_cast<int>(row / p.Tp), t = static_cast<int>(row % p.Tp);
-    const bool ok = t < p.T;
+__global__ void __launch_bounds__(256) bwd_chunk_inputs_kernel(BwdParams p, ChunkBufs cb) {
+  const int g8 = p.d / 8;
+  const int gi = blockIdx.x * 256 + threadIdx.x;
+  if (gi >= p.Tp * g8) return;
+  const int t = gi / g8, e = (gi - t * g8) * 8;
+  for (int bh = blockIdx.y; bh < p.BH; bh += gridDim.y) {
+  const size_t dst = (static_cast<size_t>(bh) * p.Tp + t) * p.d + e;
+  float w[8], k[8], q[8];
+  if (t < p.T) {
     const size_t src = (static_cast<size_t>(bh) * p.T + t) * p.d + e;
-    cb.Wf[x] = ok ? ldf(static_cast<const ET*>(p.w) + src) : 0.f;
-    cb.Kf[x] = ok ? ldf(static_cast<const ET*>(p.k) + src) : 0.f;
-    cb.Qf[x] = ok ? ldf(static_cast<const ET*>(p.q) + src) : 0.f;
-    if (e == 0) cb.bf[row] = ok ? p.beta[static_cast<size_t>(bh) * p.T + t] : 0.f;
+    ld8(static_cast<const ET*>(p.w) + src, w);
+    ld8(static_cast<const ET*>(p.k) + src, k);
+    ld8(static_cast<const ET*>(p.q) + src, q);
+  } else {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) w[u] = k[u] = q[u] = 0.f;
+  }
+  st8(cb.Wf + dst, w);
+  st8(cb.Kf + dst, k);
+  st8(cb.Qf + dst, q);
+  if (e == 0)
+    cb.bf[static_cast<size_t>(bh) * p.Tp + t] =
+        t < p.T ? p.beta[static_cast<size_t>(bh) * p.T + t] : 0.f;
   }
 }
 
@@ -503,50 +546,80 @@ __global__ void __launch_bounds__(256) bwd_tri_inv128_kernel(const float* Lm, fl
   }
 }
 
-// Elementwise steps of the chunk pass, one block per chunk.
+// Elementwise steps of the chunk pass, one block per chunk, 4 columns per
+// thread and step.
 //  op 0: Lm  = strictLower(beta_i GWW_ij)
-//  op 1: U   = Xi diag(beta)  (and dXi = dU diag(beta) when `in2` is dU)
+//  op 1: U   = Xi diag(beta)  (and dXi = dU diag(beta) when `in` is dU)
 //  op 2: BL  = diag(beta) dLm
-__global__ void bwd_chunk_elem_kernel(const float* in, float* out, const float* bf, int C, int op) {
+__global__ void __launch_bounds__(256) bwd_chunk_elem_kernel(const float* in, float* out,
+                                                             const float* bf, int C, int op) {
   const int ch = blockIdx.x;
-  const float* a = in + static_cast<size_t>(ch) * C * C;
-  float* o = out + static_cast<size_t>(ch) * C * C;
+  const float4* a = reinterpret_cast<const float4*>(in + static_cast<size_t>(ch) * C * C);
+  float4* o = reinterpret_cast<float4*>(out + static_cast<size_t>(ch) * C * C);
   const float* be = bf + static_cast<size_t>(ch) * C;
-  for (int x = threadIdx.x; x < C * C; x += blockDim.x) {
-    const int i = x / C, j = x % C;
-    float v;
-    if (op == 0) v = i > j ? be[i] * a[x] : 0.f;
-    else if (op == 1) v = a[x] * be[j];
-    else v = be[i] * a[x];
+  const int c4 = C / 4;
+  for (int x = threadIdx.x; x < C * c4; x += blockDim.x) {
+    const int i = x / c4, j = (x - i * c4) * 4;
+    float4 v = a[x];
+    if (op == 0) {
+      const float bi = be[i];
+      v.x = i > j ? bi * v.x : 0.f;
+      v.y = i > j + 1 ? bi * v.y : 0.f;
+      v.z = i > j + 2 ? bi * v.z : 0.f;
+      v.w = i > j + 3 ? bi * v.w : 0.f;
+    } else if (op == 1) {
+      const float4 bj = *reinterpret_cast<const float4*>(be + j);
+      v.x *= bj.x; v.y *= bj.y; v.z *= bj.z; v.w *= bj.w;
+    } else {
+      const float bi = be[i];
+      v.x *= bi; v.y *= bi; v.z *= bi; v.w *= bi;
+    }
     o[x] = v;
   }
 }
 
-// dbeta_j = sum_i Xi_ij dU_ij + sum_m dLm_jm GWW_jm
-__global__ void bwd_dbeta_kernel(const float* Xi, const float* dU, const float* dLm,
-                                 const float* GWW, float* dbf, int C) {
-  const int ch = blockIdx.x, j = threadIdx.x;
-  if (j >= C) return;
+// dbeta_j = sum_i Xi_ij dU_ij + sum_m dLm_jm GWW_jm; one block of 256 per
+// chunk: the column sums by threads j < C, the row sums by a warp per row.
+__global__ void __launch_bounds__(256) bwd_dbeta_kernel(const float* Xi, const float* dU,
+                                                        const float* dLm, const float* GWW,
+                                                        float* dbf, int C) {
+  __shared__ float rows[128];
+  const int ch = blockIdx.x, tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const size_t o = static_cast<size_t>(ch) * C * C;
-  float s = 0.f;
-  for (int i = 0; i < C; ++i) s = fmaf(Xi[o + i * C + j], dU[o + i * C + j], s);
-  for (int m = 0; m < C; ++m) s = fmaf(dLm[o + j * C + m], GWW[o + j * C + m], s);
-  dbf[static_cast<size_t>(ch) * C + j] = s;
+  for (int j = warp; j < C; j += 8) {
+    float s = 0.f;
+    for (int m = lane; m < C; m += 32) s = fmaf(dLm[o + j * C + m], GWW[o + j * C + m], s);
+    s = warp_sum(s);
+    if (lane == 0) rows[j] = s;
+  }
+  __syncthreads();
+  if (tid < C) {
+    float s = rows[tid];
+    for (int i = 0; i < C; ++i) s = fmaf(Xi[o + i * C + tid], dU[o + i * C + tid], s);
+    dbf[static_cast<size_t>(ch) * C + tid] = s;
+  }
 }
 
+// dq, dk, dw (input dtype) and dbeta from the chunk-pass buffers; grid as the
+// inputs kernel.
 template <typename ET>
-__global__ void bwd_chunk_outputs_kernel(BwdParams p, ChunkBufs cb) {
-  const size_t total = static_cast<size_t>(p.BH) * p.T * p.d;
-  for (size_t x = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; x < total;
-       x += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const size_t row = x / p.d;
-    const int e = static_cast<int>(x % p.d);
-    const int bh = static_cast<int>(row / p.T), t = static_cast<int>(row % p.T);
-    const size_t src = (static_cast<size_t>(bh) * p.Tp + t) * p.d + e;
-    stf(static_cast<ET*>(p.dq) + x, cb.dQf[src]);
-    stf(static_cast<ET*>(p.dk) + x, cb.dKf[src]);
-    stf(static_cast<ET*>(p.dw) + x, cb.dWf[src]);
-    if (e == 0) p.dbeta[row] = cb.dbf[static_cast<size_t>(bh) * p.Tp + t];
+__global__ void __launch_bounds__(256) bwd_chunk_outputs_kernel(BwdParams p, ChunkBufs cb) {
+  const int g8 = p.d / 8;
+  const int gi = blockIdx.x * 256 + threadIdx.x;
+  if (gi >= p.T * g8) return;
+  const int t = gi / g8, e = (gi - t * g8) * 8;
+  for (int bh = blockIdx.y; bh < p.BH; bh += gridDim.y) {
+  const size_t src = (static_cast<size_t>(bh) * p.Tp + t) * p.d + e;
+  const size_t dst = (static_cast<size_t>(bh) * p.T + t) * p.d + e;
+  float v[8];
+  ld8(cb.dQf + src, v);
+  st8(static_cast<ET*>(p.dq) + dst, v);
+  ld8(cb.dKf + src, v);
+  st8(static_cast<ET*>(p.dk) + dst, v);
+  ld8(cb.dWf + src, v);
+  st8(static_cast<ET*>(p.dw) + dst, v);
+  if (e == 0)
+    p.dbeta[static_cast<size_t>(bh) * p.T + t] = cb.dbf[static_cast<size_t>(bh) * p.Tp + t];
   }
 }
 
@@ -692,7 +765,7 @@ cudaError_t launch_bwd_t(const BwdParams& p, const ChunkBufs& cb, cudaStream_t s
   const GemmCtx gx{st, p.bf16, p.status};
   const long long cc = static_cast<long long>(C) * C, cd = static_cast<long long>(C) * D,
                   dd = static_cast<long long>(D) * D;
-  bwd_chunk_inputs_kernel<ET><<<1024, 256, 0, st>>>(p, cb);
+  bwd_chunk_inputs_kernel<ET><<<dim3((p.Tp * (D / 8) + 255) / 256, p.BH < 65535 ? p.BH : 65535), 256, 0, st>>>(p, cb);
   const float *W = cb.Wf, *K = cb.Kf, *Q = cb.Qf;
   // Products of [C][C] (cc) and [C][D] (cd) per-chunk matrices; a Term lists
   // alpha, A, its leading dimension and batch stride, whether it is
@@ -772,13 +845,13 @@ cudaError_t launch_bwd_t(const BwdParams& p, const ChunkBufs& cb, cudaStream_t s
   if ((e = mgemm(gx, nch, C, C, {CC(1.f, cb.Xi, true, cb.dXi, false)}, cb.T1, C, cc, nullptr, 0)) ||
       (e = mgemm(gx, nch, C, C, {CC(-1.f, cb.T1, false, cb.Xi, true)}, cb.dLm, C, cc, nullptr, 2)))
     return e;
-  bwd_dbeta_kernel<<<nch, C, 0, st>>>(cb.Xi, cb.dU, cb.dLm, cb.GWW, cb.dbf, C);
+  bwd_dbeta_kernel<<<nch, 256, 0, st>>>(cb.Xi, cb.dU, cb.dLm, cb.GWW, cb.dbf, C);
   // BL = diag(beta) dLm; dW += BL W + BL^T W
   bwd_chunk_elem_kernel<<<nch, 256, 0, st>>>(cb.dLm, cb.BL, cb.bf, C, 2);
   if ((e = mgemm(gx, nch, C, D, {CC_CD(1.f, cb.BL, false, W), CC_CD(1.f, cb.BL, true, W)}, cb.dWf,
                  D, cd, cb.dWf, 0)))
     return e;
-  bwd_chunk_outputs_kernel<ET><<<1024, 256, 0, st>>>(p, cb);
+  bwd_chunk_outputs_kernel<ET><<<dim3((p.T * (D / 8) + 255) / 256, p.BH < 65535 ? p.BH : 65535), 256, 0, st>>>(p, cb);
   if (p.dlogf) bwd_gate_kernel<<<p.BH, 1024, 0, st>>>(p);
   bwd_mark(p.ev, kBwdEvEnd, st);
   return cudaGetLastError();
