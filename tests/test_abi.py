@@ -148,3 +148,23 @@ def test_producer_validates_before_any_cuda_call(lib):
     bad = list(p)
     bad[6] = ctypes.c_void_p(0x70008)        # misaligned w
     assert prod(ptrs=bad) == INVALID
+
+
+def test_backward_launch_count(lib):
+    bf, f32 = pa.PATH_DTYPE_BF16, pa.PATH_DTYPE_F32
+    one = pa.path_attn_bwd_launches_per_call(128, 128, bf)     # one chunk: no X walk
+    many = pa.path_attn_bwd_launches_per_call(4096, 128, bf)
+    assert many == one + 1
+    # the gate adds its prefix sum and its suffix scan
+    assert pa.path_attn_bwd_launches_per_call(4096, 128, bf, True) == many + 2
+    assert pa.path_attn_bwd_launches_per_call(300, 64, f32) > many
+    assert lib.path_attn_bwd_launches_per_call(0, 128, bf, 0) == INVALID
+    assert lib.path_attn_bwd_launches_per_call(64, 96, bf, 0) == UNSUPPORTED
+
+
+def test_backward_timing_read_without_calls(lib):
+    pa.path_attn_timing_enable(True)
+    phases, calls = pa.path_attn_bwd_timing_read()
+    pa.path_attn_timing_enable(False)
+    assert calls == 0 and set(phases) == set(pa.BWD_PHASES)
+    assert all(v == 0.0 for v in phases.values())
