@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpathattn.so")
 SOURCES = ["api.cu", "prep.cu", "prep_tc.cu", "attn_f32.cu", "attn_tc.cu", "bwd.cu", "bwd_tc.cu", "bwd_gemm_tc.cu",
-           "decode.cu", "producer.cu", "producer_tc.cu"]
+           "decode.cu", "producer.cu", "producer_tc.cu", "producer_mix_tc.cu"]
 HEADERS = ["common.cuh", "ptx.cuh", "prep_solve.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

@@ -567,14 +567,13 @@ int path_producer_fwd(const void* x, const void* Wd, const void* Wu, const float
   if (rc != PATH_OK) return rc;
   if ((rc = check_device(s)) != PATH_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  float* low = nullptr;
-  cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&low),
-                                          producer_workspace_bytes(B, T, R), s->pool, st);
+  void* ws = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&ws, producer_workspace_bytes(B, T, R, H, d), s->pool, st);
   if (e != cudaSuccess) return set_cuda_error(e);
-  if ((e = launch_producer(x, Wd, Wu, cw, Ub, bb, w, beta, low, s->status, B, T, Dm, H, d, R,
+  if ((e = launch_producer(x, Wd, Wu, cw, Ub, bb, w, beta, ws, s->status, B, T, Dm, H, d, R,
                            dtype == PATH_DTYPE_BF16, st)) != cudaSuccess)
     rc = set_cuda_error(e);
-  e = cudaFreeAsync(low, st);
+  e = cudaFreeAsync(ws, st);
   if (rc == PATH_OK && e != cudaSuccess) rc = set_cuda_error(e);
   return rc;
 }

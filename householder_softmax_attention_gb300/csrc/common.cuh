@@ -139,12 +139,20 @@ cudaError_t launch_decode(const DecodeParams& p, int BH, int d, bool bf16, cudaS
 // from the chunk factors kr and ngt of a prepared workspace.
 cudaError_t launch_align_keys(const Geom& g, const Workspace& ws, float* kcache, int Tmax,
                               cudaStream_t st);
-// w / beta producer (producer.cu): two launches, `low` is [B*T][R] (fp32 at most).
-size_t producer_workspace_bytes(int B, int T, int R);
+// w / beta producer (producer.cu): the projection, then the mixing step;
+// the workspace holds `low` [B*T][R] (fp32 at most) and, for the tcgen05
+// mixing kernel, the folded weights (producer_mix_tc.cu).
+size_t producer_workspace_bytes(int B, int T, int R, int H, int d);
 cudaError_t launch_producer(const void* x, const void* Wd, const void* Wu, const float* cw,
-                            const void* Ub, const float* bb, void* w, float* beta, float* low,
+                            const void* Ub, const float* bb, void* w, float* beta, void* ws,
                             int* status, int B, int T, int Dm, int H, int d, int R, bool bf16_in,
                             cudaStream_t st);
+// bf16 mixing on tcgen05 with the convolution folded into the weights (R = 64).
+bool producer_mix_tc_supported(int B, int T, int H, int d, int R);
+size_t producer_fold_bytes(int H, int d);
+cudaError_t launch_producer_mix_tc(const void* low, const void* Wu, const float* cw, void* bf,
+                                   void* w, int* status, int B, int T, int H, int d,
+                                   cudaStream_t st);
 // bf16 producer projection on tcgen05 (producer_tc.cu); `low` is [B*T][R] bf16.
 cudaError_t launch_producer_proj_tc(const void* x, const void* Wd, const void* Ub,
                                     const float* bb, void* low, float* beta, int* status, int B,

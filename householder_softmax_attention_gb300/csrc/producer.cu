@@ -373,14 +373,17 @@ cudaError_t launch_mix(const ProdArgs& p, bool bf16_in, cudaStream_t st) {
 
 }  // namespace
 
-size_t producer_workspace_bytes(int B, int T, int R) {
-  return static_cast<size_t>(B) * T * R * sizeof(float);  // fp32 at most
+size_t producer_workspace_bytes(int B, int T, int R, int H, int d) {
+  const size_t low = align_up(static_cast<size_t>(B) * T * R * sizeof(float), 256);  // fp32 at most
+  return low + producer_fold_bytes(H, d);
 }
 
 cudaError_t launch_producer(const void* x, const void* Wd, const void* Wu, const float* cw,
-                            const void* Ub, const float* bb, void* w, float* beta, float* low,
+                            const void* Ub, const float* bb, void* w, float* beta, void* ws,
                             int* status, int B, int T, int Dm, int H, int d, int R, bool bf16_in,
                             cudaStream_t st) {
+  float* low = static_cast<float*>(ws);
+  void* fold = static_cast<char*>(ws) + align_up(static_cast<size_t>(B) * T * R * sizeof(float), 256);
   const ProdArgs p{x, Wd, Wu, Ub, cw, bb, w, beta, low, B, T, Dm, H, R};
   const int BT = B * T;
   cudaError_t e;
@@ -397,6 +400,8 @@ cudaError_t launch_producer(const void* x, const void* Wd, const void* Wu, const
     producer_proj_f32_kernel<<<BT, 128, smem, st>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
+  if (bf16_in && producer_mix_tc_supported(B, T, H, d, R))
+    return launch_producer_mix_tc(low, Wu, cw, fold, w, status, B, T, H, d, st);
   return d == 128 ? launch_mix<128>(p, bf16_in, st) : launch_mix<64>(p, bf16_in, st);
 }
 
