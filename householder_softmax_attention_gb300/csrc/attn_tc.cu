@@ -67,25 +67,13 @@ struct TcCfg {
 struct Bars {
   uint64_t kg_full[2], kg_empty[2], v_full[2], v_empty[2];
   uint64_t sq_ready, p_full, qk_done, pv_done, final_done;
+  uint64_t gate_full[2], gate_empty[2];  // FoX: the gate ring below
   uint32_t tmem_base;
   int abort_flag;
-  alignas(16) float gate[2][kC];  // FoX: log2-domain gate prefix, read as float4
+  alignas(16) float gate[2][kC];  // FoX: log2-domain gate prefix of a key chunk
 };
 
 static_assert(sizeof(Bars) <= 1280, "barrier block size");
-
-// Barrier of the softmax warpgroup (named barrier 2, 128 threads) that also
-// returns whether every thread passed `v` as true.
-__device__ __forceinline__ bool softmax_bar_and(bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 2, 128, p;\n\tselp.b32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(v ? 1u : 0u)
-      : "memory");
-  return r != 0;
-}
 
 // The warp's tcgen05 stores / loads are fenced by each thread before this;
 // the warp then arrives once.
@@ -177,6 +165,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->qk_done, 1);
     mbar_init(&bars->pv_done, 1);
     mbar_init(&bars->final_done, 2);  // one commit from each MMA-issuing thread
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->gate_full[s], 1);
+      mbar_init(&bars->gate_empty[s], 4);  // the softmax warps, once read
+    }
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -203,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int last_kg[2] = {-1, -1}, last_v[2] = {-1, -1};
+      int last_kg[2] = {-1, -1}, last_v[2] = {-1, -1}, last_g[2] = {-1, -1};
       bool ok = true;
       for (int n = 0; n <= b && ok; ++n) {
         const int s = n & 1;
@@ -218,6 +210,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(dst + kC * 128, &map_ng, h * 64, (bh * Np + c) * D, &bars->kg_full[s]);
           }
           last_kg[s] = (n >> 1) & 1;
+          if (kGate) {
+            // the key chunk's gate prefix (512 bytes) for the softmax warps
+            if (n >= 2) ok = mbar_wait(&bars->gate_empty[s], ((n >> 1) - 1) & 1, abort_flag, LIM);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&bars->gate_full[s], kC * 4);
+            bulk_load(&bars->gate[s][0], lam2 + static_cast<size_t>(bh) * Tp + c * kC, kC * 4,
+                      &bars->gate_full[s]);
+            last_g[s] = (n >> 1) & 1;
+          }
         }
         if (n >= 2) ok = mbar_wait(&bars->v_empty[s], ((n >> 1) - 1) & 1, abort_flag, LIM);
         if (!ok) break;
@@ -232,6 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < 2; ++s) {
         if (last_kg[s] >= 0) mbar_wait(&bars->kg_full[s], last_kg[s], nullptr, LIM);
         if (last_v[s] >= 0) mbar_wait(&bars->v_full[s], last_v[s], nullptr, LIM);
+        if (last_g[s] >= 0) mbar_wait(&bars->gate_full[s], last_g[s], nullptr, LIM);
       }
     }
   } else if (warp == 1) {
@@ -342,19 +344,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       warp_arrive(&bars->p_full);
     }
     bool ok = true;
+    // FoX: logits of the off-diagonal chunks are handled shifted by this row's
+    // gate prefix, y_j = scale S_j - lam2_j (log2 units), so the reference max
+    // is kept in that domain and lrow comes back for lse
     const float lrow = kGate ? lam2[static_cast<size_t>(bh) * Tp + t] : 0.f;
-    // FoX: each thread stages one gate value of the next key chunk a step ahead
-    const float* lamh = kGate ? lam2 + static_cast<size_t>(bh) * Tp : nullptr;
-    if (kGate && b > 0) {
-      bars->gate[0][r] = lamh[(b - 1) * kC + r];
-      softmax_bar_and(true);
-    }
+    if (kGate) m_used -= lrow;
     for (int n = 0; n < b; ++n) {
-      const int c = b - 1 - n;
-      const float gnext = (kGate && c >= 1) ? __ldg(lamh + (c - 1) * kC + r) : 0.f;
       ok = mbar_wait(&bars->qk_done, n & 1, abort_flag, LIM);
-      if (!ok && !kGate) break;
-      if (ok) {
+      if (!ok) break;
+      {
       tc_fence_after_sync();
       tmem_ld_x128(tS, x);
       {
@@ -369,6 +367,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       warp_arrive(&bars->sq_ready);
       float mx = -INFINITY;
       if (kGate) {
+        // the chunk's gate prefix, loaded by the producer into the ring
+        ok = mbar_wait(&bars->gate_full[n & 1], (n >> 1) & 1, abort_flag, LIM);
+        if (!ok) break;
         const float4* lg = reinterpret_cast<const float4*>(&bars->gate[n & 1][0]);
 #pragma unroll
         for (int j4 = 0; j4 < kC / 4; ++j4) {
@@ -377,9 +378,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int j = j4 * 4 + u;
-            x[j] = __float_as_uint(fmaf(__uint_as_float(x[j]), sl2, lrow - gv[u]));
+            x[j] = __float_as_uint(fmaf(__uint_as_float(x[j]), sl2, -gv[u]));
           }
         }
+        warp_arrive(&bars->gate_empty[n & 1]);
         mx = row_max(x);
       } else {
         // logits stay raw; the scale enters through the FFMA inside the exp
@@ -398,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         l *= alpha;
       }
       uint32_t pk[64];
-      // gated logits are already in the log2 domain; plain ones get the scale here
+      // gated logits are already scaled (log2 units); plain ones get the scale here
       const float mul = kGate ? 1.f : sl2;
       float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -411,8 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       l += ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
       // P buffer and O are free once O += P_{c+1} V_{c+1} has completed
       ok = mbar_wait(&bars->pv_done, n & 1, abort_flag, LIM);
-      if (!ok && !kGate) break;
-      if (ok) {
+      if (!ok) break;
+      {
       tc_fence_after_sync();
       if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
@@ -431,12 +433,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       warp_arrive(&bars->p_full);
       }  // pv_done
       }  // qk_done
-      if (kGate) {
-        // all softmax threads are past this step: the other buffer is free
-        bars->gate[(n + 1) & 1][r] = gnext;
-        ok = softmax_bar_and(ok);
-      }
-      if (!ok) break;
     }
     // epilogue: out = O / l, lse = (m + log2 l) ln 2
     if (ok) ok = mbar_wait(&bars->pv_done, b & 1, abort_flag, LIM);
@@ -459,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
         }
       }
-      if (lse && t < T) lse[static_cast<size_t>(bh) * T + t] = (m_used + log2f(l)) * kLn2;
+      if (lse && t < T) lse[static_cast<size_t>(bh) * T + t] = (m_used + lrow + log2f(l)) * kLn2;
     } else {
       record_timeout(bars, status);
     }

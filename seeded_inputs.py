@@ -61,6 +61,8 @@ WORKLOADS = {
     "fox_t8k_d128": Workload("fox_t8k_d128", 4, 16, 8192, 128, fox=True),
     "t16k_d128": Workload("t16k_d128", 2, 16, 16384, 128,
                           note="long-context headline roofline workload"),
+    "fox_t16k_d128": Workload("fox_t16k_d128", 2, 16, 16384, 128, fox=True,
+                              note="the headline shape with the FoX gate"),
     "t16k_d64": Workload("t16k_d64", 2, 32, 16384, 64),
 }
 

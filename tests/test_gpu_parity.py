@@ -188,7 +188,7 @@ def _sampled_case(wl: Workload, n_heads=2, n_rows=24):
 
 
 @pytest.mark.parametrize("name", ["t2k_d128", "t2k_d64", "t4k_d128_refl", "t4k_d64_refl",
-                                  "fox_t8k_d128", "t16k_d128", "t16k_d64"])
+                                  "fox_t8k_d128", "t16k_d128", "t16k_d64", "fox_t16k_d128"])
 def test_full_size_workloads_sampled(name):
     _sampled_case(WORKLOADS[name])
 
