@@ -156,12 +156,12 @@ __device__ __forceinline__ void invert_level_mma(float* sU, int warp, int g, int
   __syncthreads();
 }
 
-// X = (I + L)^{-1} in place (L strictly lower on entry, stride S), by
-// recursive doubling: invert the 16 x 16 diagonal blocks by substitution, then
-// combine blocks of 16 (CUDA cores), 32 and 64 (tensor cores).  Ends with a
-// block-wide barrier.
+// The 32 x 32 diagonal blocks of X = (I + L)^{-1} in place (L strictly lower
+// on entry, stride S; only those blocks are read or written): the 16 x 16
+// diagonal blocks by substitution, then one doubling level of 16 on the CUDA
+// cores.  Ends with a block-wide barrier.
 template <int S>
-__device__ __forceinline__ void invert_unit_lower(float* sU, int tid) {
+__device__ __forceinline__ void invert_diag32(float* sU, int tid) {
   {
     const int bb = tid >> 4, j = tid & 15, base = bb * 16;
     float x[16];
@@ -182,11 +182,20 @@ __device__ __forceinline__ void invert_unit_lower(float* sU, int tid) {
     __syncthreads();
   }
   invert_level<S, 16>(sU, tid);
+}
+
+// X = (I + L)^{-1} in place (L strictly lower on entry, stride S), by
+// recursive doubling: the 32 x 32 diagonal blocks as above, then levels of 32
+// and 64 on the tensor cores.  Ends with a block-wide barrier.
+template <int S>
+__device__ __forceinline__ void invert_unit_lower(float* sU, int tid) {
+  invert_diag32<S>(sU, tid);
   const int warp = tid >> 5, g = (tid & 31) >> 2, t = tid & 3;
   invert_level_mma<S, 32>(sU, warp, g, t);
   invert_level_mma<S, 64>(sU, warp, g, t);
 }
 
 }  // namespace solve
+using solve::invert_diag32;
 using solve::invert_unit_lower;
 }  // namespace pathattn

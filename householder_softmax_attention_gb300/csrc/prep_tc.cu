@@ -43,11 +43,13 @@ constexpr uint32_t kRWK = 0;        // W | K stacked per half: half h at h * 32K
 constexpr uint32_t kRQS = 65536;    // Q (P1), then S hi/lo (P2-P4), then [TK|UW] hi (P5-P6)
 constexpr uint32_t kRL = 131072;    // fp32 L/X (P2-P3, stride 132), then U hi/lo, then [TK|UW] lo
 constexpr int kSL = kC + 4;
-constexpr uint32_t kRMisc = kRL + kC * kSL * 4;   // beta, gate prefix, barriers
+constexpr uint32_t kRE = kRL + kC * kSL * 4;      // inverse levels: E tiles, hi/lo (16 KB)
+constexpr uint32_t kRMisc = kRE + 16384;          // beta, gate prefix, barriers
 constexpr size_t kSmemBytes = kRMisc + 2 * kC * 4 + 64 + 1024;
+static_assert(kRE % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 
 struct Bars {
-  uint64_t tma, mma;
+  uint64_t tma, mma, mma_q;   // mma_q: the query Gram block of P1
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -75,8 +77,9 @@ __device__ __forceinline__ void put_hilo8(uint8_t* hi_tile, uint8_t* lo_tile, in
   *reinterpret_cast<uint4*>(lo_tile + off) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
-__device__ __forceinline__ bool wait_mma(Bars* bars, uint32_t parity, int* status) {
-  if (mbar_wait(&bars->mma, parity, &bars->abort_flag, kWaitLimitNs)) return true;
+__device__ __forceinline__ bool wait_mma(Bars* bars, uint32_t parity, int* status,
+                                         uint64_t* bar = nullptr) {
+  if (mbar_wait(bar ? bar : &bars->mma, parity, &bars->abort_flag, kWaitLimitNs)) return true;
   bars->abort_flag = 1;
   atomicExch(status, PATH_DEV_ERR_TIMEOUT);
   return false;
@@ -85,7 +88,8 @@ __device__ __forceinline__ bool wait_mma(Bars* bars, uint32_t parity, int* statu
 template <int D, bool kGate>
 __global__ void __launch_bounds__(kThreads, 1)
     prep_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_k,
-                   const __grid_constant__ CUtensorMap map_q, const float* __restrict__ beta, const float* __restrict__ lam2,
+                   const __grid_constant__ CUtensorMap map_q, const uint8_t* w_raw, const uint8_t* k_raw,
+                   const uint8_t* q_raw, const float* __restrict__ beta, const float* __restrict__ lam2,
                    __nv_bfloat16* __restrict__ kr, float* __restrict__ ql,
                    __nv_bfloat16* __restrict__ ngt, float* __restrict__ sdt, int* status, int T,
                    int Np, float sl2) {
@@ -107,6 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     mbar_init(&bars->tma, 1);
     mbar_init(&bars->mma, 1);
+    mbar_init(&bars->mma_q, 1);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -134,43 +139,100 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_3d(base + kRWK + h * 2 * kHalf + kHalf, &map_k, h * 64, t0, bh, &bars->tma);
       tma_load_3d(base + kRQS + h * kHalf, &map_q, h * 64, t0, bh, &bars->tma);
     }
+    // the chunk one wave ahead (one CTA per SM, CTAs started in index order):
+    // its w, k and q rows into L2 while this chunk computes
+    const int ch2 = ch + static_cast<int>(sm_count());
+    if (ch2 < static_cast<int>(gridDim.x)) {
+      const int bh2 = ch2 / Np, t2 = (ch2 - bh2 * Np) * kC;
+      const size_t off = (static_cast<size_t>(bh2) * T + t2) * D * 2;
+      const uint32_t bytes = static_cast<uint32_t>(min(kC, T - t2)) * D * 2;
+      bulk_prefetch_l2(w_raw + off, bytes);
+      bulk_prefetch_l2(k_raw + off, bytes);
+      bulk_prefetch_l2(q_raw + off, bytes);
+    }
     ok = mbar_wait(&bars->tma, 0, &bars->abort_flag, kWaitLimitNs);
     if (ok) {
       tc_fence_after_sync();
       constexpr uint32_t id = idesc_bf16_f32(128, 256, false, false);
+      // [W W^T | W K^T], then [Q W^T | Q K^T] (it runs while the CUDA cores
+      // work on P2 and the diagonal blocks of P3; Q is overwritten by S
+      // only after its completion)
       for (int k = 0; k < D / 16; ++k) {
         const uint32_t kb = k >> 2, kk = (k & 3) * 32;
         const uint64_t bwk = sdesc_sw128(smem_addr(base + kRWK + kb * 2 * kHalf) + kk, 16, 1024);
-        const uint64_t aw = sdesc_sw128(smem_addr(base + kRWK + kb * 2 * kHalf) + kk, 16, 1024);
-        const uint64_t aq = sdesc_sw128(smem_addr(base + kRQS + kb * kHalf) + kk, 16, 1024);
-        mma_bf16_ss(tb + 0, aw, bwk, id, k > 0);    // [W W^T | W K^T]
-        mma_bf16_ss(tb + 256, aq, bwk, id, k > 0);  // [Q W^T | Q K^T]
+        mma_bf16_ss(tb + 0, bwk, bwk, id, k > 0);
       }
+      mma_commit(&bars->mma);
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t kb = k >> 2, kk = (k & 3) * 32;
+        const uint64_t bwk = sdesc_sw128(smem_addr(base + kRWK + kb * 2 * kHalf) + kk, 16, 1024);
+        const uint64_t aq = sdesc_sw128(smem_addr(base + kRQS + kb * kHalf) + kk, 16, 1024);
+        mma_bf16_ss(tb + 256, aq, bwk, id, k > 0);
+      }
+      mma_commit(&bars->mma_q);
     } else {
       bars->abort_flag = 1;
       atomicExch(status, PATH_DEV_ERR_TIMEOUT);
+      mma_commit(&bars->mma);
+      mma_commit(&bars->mma_q);
     }
-    mma_commit(&bars->mma);
   }
   ok = wait_mma(bars, mma_phase, status);
   mma_phase ^= 1;
   tc_fence_after_sync();
 
-  // ---- P2: L (fp32, smem) and S = strictLower(W K^T) (bf16 hi/lo, MN-major B)
-  {
-    uint8_t* s_hi = base + kRQS;
-    uint8_t* s_lo = base + kRQS + kTile;
+  // ---- P2: the 32 x 32 diagonal blocks of L (fp32, smem)
+  if (halfc == quarter >> 1) {   // the warps whose columns hold their rows' diagonal block
     const float bt = sBeta[row];
+    const int c0 = 32 * quarter;
+    uint32_t v[32];
+    tmem_ld_x32(tb + lb + c0, v);
+#pragma unroll
+    for (int u = 0; u < 32; u += 4) {
+      float x[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[e] = c0 + u + e < row ? __uint_as_float(v[u + e]) * bt : 0.f;
+      *reinterpret_cast<float4*>(sL + row * kSL + c0 + u) = make_float4(x[0], x[1], x[2], x[3]);
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+
+  // ---- P3: U = X D with X = (I + L)^{-1}, as bf16 hi/lo tiles (K-major A).
+  // With G = W W^T and L = strictLower(D G), every off-diagonal block of a
+  // 2 x 2 split of a diagonal block of U follows from its diagonal blocks:
+  // (I + L) X = I gives X_ba = -X_bb D_b G_ba X_aa, so U_ba = -U_bb G_ba U_aa.
+  // The 32 x 32 diagonal blocks come from the CUDA cores (fp32); the levels of
+  // 32 and 64 are two tensor-core products each, on hi/lo operands.
+  invert_diag32<kSL>(sL, tid);
+  uint8_t* const u_hi = base + kRL;
+  uint8_t* const u_lo = base + kRL + kTile;
+  {
+    // row `row`, columns [64 halfc, 64 halfc + 64): the diagonal block X D,
+    // G below it (the blocks the levels turn into U), zeros above
+    float xd[32];
+    const bool diag_here = (quarter >> 1) == halfc;
+    if (diag_here) {
+      const int c0 = 32 * quarter;
+#pragma unroll
+      for (int u = 0; u < 32; u += 4) {
+        const float4 x = *reinterpret_cast<const float4*>(sL + row * kSL + c0 + u);
+        const float4 b = *reinterpret_cast<const float4*>(sBeta + c0 + u);
+        xd[u] = c0 + u <= row ? x.x * b.x : 0.f;
+        xd[u + 1] = c0 + u + 1 <= row ? x.y * b.y : 0.f;
+        xd[u + 2] = c0 + u + 2 <= row ? x.z * b.z : 0.f;
+        xd[u + 3] = c0 + u + 3 <= row ? x.w * b.w : 0.f;
+      }
+    }
+    __syncthreads();   // the fp32 blocks are read; the tiles overwrite them
+    // S = strictLower(W K^T) -> bf16 hi/lo (MN-major B) over Q, once the query
+    // Gram product that reads Q is done
+    ok = wait_mma(bars, 0, status, &bars->mma_q) && ok;
+    tc_fence_after_sync();
 #pragma unroll
     for (int cc = 0; cc < 64; cc += 32) {
       const int c0 = halfc * 64 + cc;
       uint32_t v[32];
-      tmem_ld_x32(tb + lb + c0, v);
-#pragma unroll
-      for (int u = 0; u < 32; ++u) {
-        const int c = c0 + u;
-        sL[row * kSL + c] = c < row ? __uint_as_float(v[u]) * bt : 0.f;
-      }
       tmem_ld_x32(tb + lb + 128 + c0, v);
 #pragma unroll
       for (int g8 = 0; g8 < 4; ++g8) {
@@ -180,38 +242,145 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int c = c0 + g8 * 8 + u;
           x[u] = c < row ? __uint_as_float(v[g8 * 8 + u]) : 0.f;
         }
-        put_hilo8(s_hi, s_lo, row, (c0 >> 3) + g8, x);
+        put_hilo8(base + kRQS, base + kRQS + kTile, row, (c0 >> 3) + g8, x);
       }
     }
+#pragma unroll
+    for (int cc = 0; cc < 64; cc += 32) {
+      const int c0 = halfc * 64 + cc, cb = c0 >> 5;
+      float x[32];
+      if (cb < quarter) {
+        uint32_t v[32];
+        tmem_ld_x32(tb + lb + c0, v);
+#pragma unroll
+        for (int u = 0; u < 32; ++u) x[u] = __uint_as_float(v[u]);
+      } else if (cb == quarter) {
+#pragma unroll
+        for (int u = 0; u < 32; ++u) x[u] = xd[u];
+      } else {
+#pragma unroll
+        for (int u = 0; u < 32; ++u) x[u] = 0.f;
+      }
+#pragma unroll
+      for (int g8 = 0; g8 < 4; ++g8)
+        put_hilo8(u_hi, u_lo, row, (c0 >> 3) + g8, *reinterpret_cast<const float(*)[8]>(&x[g8 * 8]));
+    }
   }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   tc_fence_before_sync();
   __syncthreads();
-
-  // ---- P3: X = (I + L)^{-1}, then U = X diag(beta) as bf16 hi/lo (K-major A)
-  invert_unit_lower<kSL>(sL, tid);
   {
-    // 2048 groups of 8 consecutive columns of one row; 8 groups per thread,
-    // all read before the fp32 buffer is overwritten by the tiles
-    float v[8][8];
+    constexpr uint32_t id64 = idesc_bf16_f32(128, 64, false, true);
+    const uint32_t uh = smem_addr(u_hi), ul = smem_addr(u_lo), eb = smem_addr(base + kRE);
+    auto a_desc = [&](uint32_t t, int k) {   // K-major A, k-step k of 16 columns
+      return sdesc_sw128(t + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
+    };
+    auto b_desc = [&](uint32_t t) { return sdesc_sw128(t, kHalf, 1024); };
+    uint8_t* const e_tiles = base + kRE;
+    // one round of MMAs issued by thread 0, then every thread waits for it
+    auto mma_round = [&](auto&& body) {
+      if (tid == 0) {
+        if (ok) {
+          tc_fence_after_sync();
+          body();
+        }
+        mma_commit(&bars->mma);
+      }
+      ok = wait_mma(bars, mma_phase, status) && ok;
+      mma_phase ^= 1;
+      tc_fence_after_sync();
+    };
+    auto publish = [&]() {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before_sync();
+      __syncthreads();
+    };
+    // level 32, pairs p = 0, 1 (a = rows 64p.., b = rows 64p + 32..):
+    // E_p = G_ba U_aa -> TMEM cols [64p, 64p + 64) (cols 32.. are zero)
+    mma_round([&] {
+      for (int p = 0; p < 2; ++p)
+        for (int term = 0; term < 3; ++term) {
+          const uint32_t at = term == 2 ? ul : uh, bt = term == 1 ? ul : uh;
+          for (int j = 0; j < 2; ++j)
+            mma_bf16_ss(tb + 64 * p, a_desc(at, 4 * p + j),
+                        b_desc(bt + p * kHalf + (4 * p + j) * 2048), id64, term > 0 || j > 0);
+        }
+    });
+    if (quarter & 1) {   // E_p rows are lanes of quarter 2p + 1 -> MN-major B tile
+      const int p = quarter >> 1;
+      uint32_t v[32];
+      tmem_ld_x32(tb + lb + 64 * p + 32 * halfc, v);
 #pragma unroll
-    for (int gi = 0; gi < 8; ++gi) {
-      const int grp = tid + gi * kThreads, i = grp >> 4, c8 = grp & 15;
-      const float4 x0 = *reinterpret_cast<const float4*>(sL + i * kSL + c8 * 8);
-      const float4 x1 = *reinterpret_cast<const float4*>(sL + i * kSL + c8 * 8 + 4);
-      const float4 b0 = *reinterpret_cast<const float4*>(sBeta + c8 * 8);
-      const float4 b1 = *reinterpret_cast<const float4*>(sBeta + c8 * 8 + 4);
-      const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-      const float bs[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+      for (int g8 = 0; g8 < 4; ++g8) {
+        float x[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) v[gi][u] = c8 * 8 + u <= i ? xs[u] * bs[u] : 0.f;
+        for (int u = 0; u < 8; ++u) x[u] = __uint_as_float(v[g8 * 8 + u]);
+        put_hilo8(e_tiles + p * 8192, e_tiles + p * 8192 + 4096, lane, 4 * halfc + g8, x);
+      }
     }
-    __syncthreads();
-    uint8_t* u_hi = base + kRL;
-    uint8_t* u_lo = base + kRL + kTile;
+    publish();
+    // U_bb E_p -> TMEM cols [128 + 64p, ...)
+    mma_round([&] {
+      for (int p = 0; p < 2; ++p)
+        for (int term = 0; term < 3; ++term) {
+          const uint32_t at = term == 2 ? ul : uh;
+          const uint32_t bt = eb + p * 8192 + (term == 1 ? 4096 : 0);
+          for (int j = 0; j < 2; ++j)
+            mma_bf16_ss(tb + 128 + 64 * p, a_desc(at, 4 * p + 2 + j), b_desc(bt + j * 2048), id64,
+                        term > 0 || j > 0);
+        }
+    });
+    if (quarter & 1) {   // U_ba = -U_bb E_p, 16 columns per warp
+      const int p = quarter >> 1;
+      uint32_t v[16];
+      tmem_ld_x16(tb + lb + 128 + 64 * p + 16 * halfc, v);
 #pragma unroll
-    for (int gi = 0; gi < 8; ++gi) {
-      const int grp = tid + gi * kThreads, i = grp >> 4, c8 = grp & 15;
-      put_hilo8(u_hi, u_lo, i, c8, v[gi]);
+      for (int g8 = 0; g8 < 2; ++g8) {
+        float x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) x[u] = -__uint_as_float(v[g8 * 8 + u]);
+        put_hilo8(u_hi, u_lo, row, 8 * p + 2 * halfc + g8, x);
+      }
+    }
+    publish();
+    // level 64: E = G_21 U_11 -> TMEM cols [0, 64)
+    mma_round([&] {
+      for (int term = 0; term < 3; ++term) {
+        const uint32_t at = term == 2 ? ul : uh, bt = term == 1 ? ul : uh;
+        for (int j = 0; j < 4; ++j)
+          mma_bf16_ss(tb, a_desc(at, j), b_desc(bt + j * 2048), id64, term > 0 || j > 0);
+      }
+    });
+    if (quarter >= 2) {
+      uint32_t v[32];
+      tmem_ld_x32(tb + lb + 32 * halfc, v);
+#pragma unroll
+      for (int g8 = 0; g8 < 4; ++g8) {
+        float x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) x[u] = __uint_as_float(v[g8 * 8 + u]);
+        put_hilo8(e_tiles, e_tiles + 8192, row - 64, 4 * halfc + g8, x);
+      }
+    }
+    publish();
+    // U_22 E -> TMEM cols [64, 128)
+    mma_round([&] {
+      for (int term = 0; term < 3; ++term) {
+        const uint32_t at = term == 2 ? ul : uh, bt = eb + (term == 1 ? 8192 : 0);
+        for (int j = 0; j < 4; ++j)
+          mma_bf16_ss(tb + 64, a_desc(at, 4 + j), b_desc(bt + j * 2048), id64, term > 0 || j > 0);
+      }
+    });
+    if (quarter >= 2) {   // U_21 = -U_22 E
+      uint32_t v[32];
+      tmem_ld_x32(tb + lb + 64 + 32 * halfc, v);
+#pragma unroll
+      for (int g8 = 0; g8 < 4; ++g8) {
+        float x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) x[u] = -__uint_as_float(v[g8 * 8 + u]);
+        put_hilo8(u_hi, u_lo, row, 4 * halfc + g8, x);
+      }
     }
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -312,12 +481,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   ok = wait_mma(bars, mma_phase, status) && ok;
   mma_phase ^= 1;
   tc_fence_after_sync();
-  // epilogue: kr[j][:] = K[j][:] - kr'[j][:] (half 0, row j = lane), ngt[n][:] =
-  // -ngt'[n][:] (half 1, rows n < D): whole rows, 16 bytes per store
+  // epilogue, first half: this thread's output row as bf16 pairs in registers,
+  // kr[j][:] = K[j][:] - kr'[j][:] (half 0, row j = lane), ngt[n][:] =
+  // -ngt'[n][:] (half 1, rows n < D); stored while P6b runs
+  uint32_t orow[D / 2];
   if (halfc == 0) {
     const int j = row;
-    uint4* out = reinterpret_cast<uint4*>(kr + (static_cast<size_t>(ch) * kC + j) * D);
     const uint8_t* kt = base + kRWK + kHalf;  // K rows inside the W|K halves
+#pragma unroll
     for (int cc = 0; cc < D; cc += 32) {
       uint32_t v[32];
       tmem_ld_x32(tb + lb + cc, v);
@@ -328,28 +499,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             (f0 >> 6) * 2 * kHalf + j * 128 + ((((f0 & 63) >> 3) ^ (j & 7)) << 4);
         const uint4 kq = *reinterpret_cast<const uint4*>(kt + off);
         const uint32_t kw[4] = {kq.x, kq.y, kq.z, kq.w};
-        uint32_t o[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          o[e] = pack_bf16x2(__uint_as_float(kw[e] << 16) - __uint_as_float(v[u8 + 2 * e]),
-                             __uint_as_float(kw[e] & 0xffff0000u) -
-                                 __uint_as_float(v[u8 + 2 * e + 1]));
-        out[f0 / 8] = make_uint4(o[0], o[1], o[2], o[3]);
+          orow[f0 / 2 + e] = pack_bf16x2(__uint_as_float(kw[e] << 16) - __uint_as_float(v[u8 + 2 * e]),
+                                         __uint_as_float(kw[e] & 0xffff0000u) -
+                                             __uint_as_float(v[u8 + 2 * e + 1]));
       }
     }
   } else if (row < D) {
-    const int n = row;
-    uint4* out = reinterpret_cast<uint4*>(ngt + (static_cast<size_t>(ch) * D + n) * D);
+#pragma unroll
     for (int cc = 0; cc < D; cc += 32) {
       uint32_t v[32];
       tmem_ld_x32(tb + lb + 128 + cc, v);
 #pragma unroll
-      for (int u8 = 0; u8 < 32; u8 += 8)
-        out[(cc + u8) / 8] =
-            make_uint4(pack_bf16x2(-__uint_as_float(v[u8]), -__uint_as_float(v[u8 + 1])),
-                       pack_bf16x2(-__uint_as_float(v[u8 + 2]), -__uint_as_float(v[u8 + 3])),
-                       pack_bf16x2(-__uint_as_float(v[u8 + 4]), -__uint_as_float(v[u8 + 5])),
-                       pack_bf16x2(-__uint_as_float(v[u8 + 6]), -__uint_as_float(v[u8 + 7])));
+      for (int u = 0; u < 16; ++u)
+        orow[cc / 2 + u] = pack_bf16x2(-__uint_as_float(v[2 * u]), -__uint_as_float(v[2 * u + 1]));
     }
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -378,6 +542,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     mma_commit(&bars->mma);
   } else if (tid == 0) {
     mma_commit(&bars->mma);
+  }
+  // epilogue of P6a, second half: the kr / ngt rows, 32 bytes per store
+  if (halfc == 0 || row < D) {
+    uint32_t* out = halfc == 0
+                        ? reinterpret_cast<uint32_t*>(kr + (static_cast<size_t>(ch) * kC + row) * D)
+                        : reinterpret_cast<uint32_t*>(ngt + (static_cast<size_t>(ch) * D + row) * D);
+#pragma unroll
+    for (int u = 0; u < D / 2; u += 8) st_global_v8(out + u, &orow[u]);
   }
   ok = wait_mma(bars, mma_phase, status) && ok;
   mma_phase ^= 1;
@@ -491,7 +663,8 @@ cudaError_t launch_one(const Geom& g, const Inputs& in, const Workspace& ws, int
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
   kern<<<g.nch, kThreads, kSmemBytes, st>>>(
-      mw, mk, mq, in.beta, ws.lam2,
+      mw, mk, mq, static_cast<const uint8_t*>(in.w), static_cast<const uint8_t*>(in.k),
+      static_cast<const uint8_t*>(in.q), in.beta, ws.lam2,
       static_cast<__nv_bfloat16*>(ws.kr), ws.ql, static_cast<__nv_bfloat16*>(ws.ngt), ws.sdt,
       status, g.T, g.Np, in.scale * kLog2e);
   return cudaGetLastError();
