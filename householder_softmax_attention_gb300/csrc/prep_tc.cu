@@ -458,24 +458,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (tid == 0) {
     mma_commit(&bars->mma);
   }
-  // meanwhile: -lower(Q W^T) -> bf16 hi / lo A operand in TMEM columns [256, 384)
-  if (warp < 4) {
-    uint32_t v[128];
-    tmem_ld_x128(tb + lb + 256, v);
-    uint32_t ph[64], pl[64];
+  // meanwhile: -lower(Q W^T) -> bf16 hi / lo A operand in TMEM columns [256, 384),
+  // each warp 64 of its rows' 128 values; the hi / lo columns overlap the
+  // source, so both warps of a lane quarter have read before either writes
+  {
+    uint32_t v[64];
+    tmem_ld_x64(tb + lb + 256 + 64 * halfc, v);
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    uint32_t ph[32], pl[32];
 #pragma unroll
-    for (int u = 0; u < 64; ++u) {
-      const int c = 2 * u;
-      const float x0 = c <= row ? -__uint_as_float(v[c]) : 0.f;
-      const float x1 = c + 1 <= row ? -__uint_as_float(v[c + 1]) : 0.f;
+    for (int u = 0; u < 32; ++u) {
+      const int c = 64 * halfc + 2 * u;
+      const float x0 = c <= row ? -__uint_as_float(v[2 * u]) : 0.f;
+      const float x1 = c + 1 <= row ? -__uint_as_float(v[2 * u + 1]) : 0.f;
       const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
       ph[u] = pack_bf16x2(__bfloat162float(h0), __bfloat162float(h1));
       pl[u] = pack_bf16x2(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
     }
-    tmem_st_x32(tb + lb + 256, *reinterpret_cast<uint32_t(*)[32]>(&ph[0]));
-    tmem_st_x32(tb + lb + 288, *reinterpret_cast<uint32_t(*)[32]>(&ph[32]));
-    tmem_st_x32(tb + lb + 320, *reinterpret_cast<uint32_t(*)[32]>(&pl[0]));
-    tmem_st_x32(tb + lb + 352, *reinterpret_cast<uint32_t(*)[32]>(&pl[32]));
+    tmem_st_x32(tb + lb + 256 + 32 * halfc, ph);
+    tmem_st_x32(tb + lb + 320 + 32 * halfc, pl);
     tmem_st_wait();
   }
   ok = wait_mma(bars, mma_phase, status) && ok;
@@ -554,36 +557,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   ok = wait_mma(bars, mma_phase, status) && ok;
   mma_phase ^= 1;
   tc_fence_after_sync();
-  // epilogue: sdt[j][i] from Q K^T + sd' (half 0); ql[i][n] = Q[i][n] + ql' (half 1)
+  // epilogue, each warp half of its rows' columns: sdt[j][i] from Q K^T + sd'
+  // for keys j in [64 halfc, 64 halfc + 64) (coalesced over the rows i), and
+  // ql' for features [D/2 halfc, D/2 (halfc + 1)) to shared memory (the lo
+  // tiles are dead once the MMA is done)
   {
     const int i = row;
-    if (halfc == 0) {
-      float* out = sdt + static_cast<size_t>(ch) * kC * kC + i;
-      const float li = kGate ? sLam[i] : 0.f;
-      for (int cc = 0; cc < 128; cc += 32) {
-        uint32_t v[32], qk[32];
-        tmem_ld_x32(tb + lb + cc, v);
-        tmem_ld_x32(tb + lb + 384 + cc, qk);
+    float* out = sdt + static_cast<size_t>(ch) * kC * kC + i;
+    const float li = kGate ? sLam[i] : 0.f;
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-          const int j = cc + u;
-          const float gj = kGate ? sLam[j] : 0.f;
-          out[static_cast<size_t>(j) * kC] =
-              j <= i ? fmaf(__uint_as_float(qk[u]) + __uint_as_float(v[u]), sl2, li - gj) : -INFINITY;
-        }
-      }
-    } else {
-      // ql' rows to shared memory (the lo tiles are dead once the MMA is done)
-      float* sq = sL;
-      for (int cc = 0; cc < D; cc += 32) {
-        uint32_t v[32];
-        tmem_ld_x32(tb + lb + 128 + cc, v);
+    for (int cc = 64 * halfc; cc < 64 * halfc + 64; cc += 32) {
+      uint32_t v[32], qk[32];
+      tmem_ld_x32(tb + lb + cc, v);
+      tmem_ld_x32(tb + lb + 384 + cc, qk);
 #pragma unroll
-        for (int u = 0; u < 32; u += 4)
-          *reinterpret_cast<float4*>(sq + i * kSL + cc + u) =
-              make_float4(__uint_as_float(v[u]), __uint_as_float(v[u + 1]),
-                          __uint_as_float(v[u + 2]), __uint_as_float(v[u + 3]));
+      for (int u = 0; u < 32; ++u) {
+        const int j = cc + u;
+        const float gj = kGate ? sLam[j] : 0.f;
+        out[static_cast<size_t>(j) * kC] =
+            j <= i ? fmaf(__uint_as_float(qk[u]) + __uint_as_float(v[u]), sl2, li - gj) : -INFINITY;
       }
+    }
+    float* sq = sL;
+#pragma unroll
+    for (int cc = (D / 2) * halfc; cc < (D / 2) * (halfc + 1); cc += 32) {
+      uint32_t v[32];
+      tmem_ld_x32(tb + lb + 128 + cc, v);
+#pragma unroll
+      for (int u = 0; u < 32; u += 4)
+        *reinterpret_cast<float4*>(sq + i * kSL + cc + u) =
+            make_float4(__uint_as_float(v[u]), __uint_as_float(v[u + 1]),
+                        __uint_as_float(v[u + 2]), __uint_as_float(v[u + 3]));
     }
   }
   tc_fence_before_sync();
