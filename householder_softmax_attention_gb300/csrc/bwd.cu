@@ -35,6 +35,7 @@
 #include <cmath>
 #include <cstdint>
 #include <initializer_list>
+#include <type_traits>
 
 #include "common.cuh"
 #include "prep_solve.cuh"
@@ -422,9 +423,15 @@ __global__ void __launch_bounds__(256) bwd_chunk_inputs_kernel(BwdParams p, Chun
 #pragma unroll
     for (int u = 0; u < 8; ++u) w[u] = k[u] = q[u] = 0.f;
   }
-  st8(cb.Wf + dst, w);
-  st8(cb.Kf + dst, k);
-  st8(cb.Qf + dst, q);
+  if constexpr (std::is_same<ET, bf16>::value) {   // exact bf16 copies
+    st8(reinterpret_cast<bf16*>(cb.Wf) + dst, w);
+    st8(reinterpret_cast<bf16*>(cb.Kf) + dst, k);
+    st8(reinterpret_cast<bf16*>(cb.Qf) + dst, q);
+  } else {
+    st8(cb.Wf + dst, w);
+    st8(cb.Kf + dst, k);
+    st8(cb.Qf + dst, q);
+  }
   if (e == 0)
     cb.bf[static_cast<size_t>(bh) * p.Tp + t] =
         t < p.T ? p.beta[static_cast<size_t>(bh) * p.T + t] : 0.f;
@@ -674,6 +681,12 @@ struct GemmCtx {
   cudaStream_t st;
   bool tc;
   int* status;
+  // operands held as bf16 copies (exact inputs), read as such by the
+  // tensor-core products; no other path accepts them
+  const float* bf_ops[3] = {nullptr, nullptr, nullptr};
+  bool is_bf(const float* x) const {
+    return x && (x == bf_ops[0] || x == bf_ops[1] || x == bf_ops[2]);
+  }
 };
 
 cudaError_t gemm(const GemmCtx& gx, int batch, int M, int N, int K, float alpha, const float* A,
@@ -710,7 +723,11 @@ cudaError_t mgemm(const GemmCtx& gx, int batch, int M, int N, std::initializer_l
     g.nterms = 0;
     for (const Term& t : terms) {
       if (g.nterms == kMaxTerms) return cudaErrorInvalidValue;
-      g.t[g.nterms++] = TcTerm{t.A, t.B, t.sA, t.sB, t.lda, t.ldb, t.K, t.tA, t.tB, t.alpha};
+      TcTerm tt{t.A, t.B, t.sA, t.sB, t.lda, t.ldb, t.K, t.tA, t.tB, t.alpha};
+      tt.aBf = gx.is_bf(t.A);
+      tt.bBf = gx.is_bf(t.B);
+      if (tt.aBf && t.alpha != 1.f && t.alpha != -1.f) return cudaErrorInvalidValue;
+      g.t[g.nterms++] = tt;
     }
     g.Cm = Cm;
     g.Add = add;
@@ -723,6 +740,8 @@ cudaError_t mgemm(const GemmCtx& gx, int batch, int M, int N, std::initializer_l
     g.status = gx.status;
     if (gemm_tc_supported(g)) return launch_gemm_tc(g, gx.st);
   }
+  for (const Term& t : terms)
+    if (gx.is_bf(t.A) || gx.is_bf(t.B)) return cudaErrorInvalidValue;
   cudaError_t e;
   if (add && add != Cm &&
       (e = cudaMemcpyAsync(Cm, add, static_cast<size_t>(batch) * sC * sizeof(float),
@@ -762,11 +781,18 @@ cudaError_t launch_bwd_t(const BwdParams& p, const ChunkBufs& cb, cudaStream_t s
   bwd_mark(p.ev, kBwdEvChunk, st);
   // ---- chunk pass (fp32, batched over chunks)
   const int nch = p.nch;
-  const GemmCtx gx{st, p.bf16, p.status};
+  GemmCtx gx{st, p.bf16, p.status};
   const long long cc = static_cast<long long>(C) * C, cd = static_cast<long long>(C) * D,
                   dd = static_cast<long long>(D) * D;
   bwd_chunk_inputs_kernel<ET><<<dim3((p.Tp * (D / 8) + 255) / 256, p.BH < 65535 ? p.BH : 65535), 256, 0, st>>>(p, cb);
+  // bf16 inputs: W, K, Q are bf16 copies (padded to Tp), exact operands of the
+  // tensor-core products
   const float *W = cb.Wf, *K = cb.Kf, *Q = cb.Qf;
+  if (p.bf16) {
+    gx.bf_ops[0] = W;
+    gx.bf_ops[1] = K;
+    gx.bf_ops[2] = Q;
+  }
   // Products of [C][C] (cc) and [C][D] (cd) per-chunk matrices; a Term lists
   // alpha, A, its leading dimension and batch stride, whether it is
   // transposed, the same for B, and the shared dimension.

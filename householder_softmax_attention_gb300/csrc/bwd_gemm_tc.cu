@@ -5,7 +5,8 @@
 //   z = 0 .. batch-1, up to kMaxTerms products t
 //
 // fp32 row-major operands (M = 128 rows, N and every K_t in {64, 128}), one
-// CTA of four warps per batch item.  Each fp32 operand enters the MMA as
+// CTA of four warps per batch item; an operand flagged bf16 is an exact bf16
+// array (half the bytes read, its lo products skipped).  Each fp32 operand enters the MMA as
 // x_hi + x_lo with x_hi = bf16(x), x_lo = bf16(x - x_hi) (about 16
 // significant bits; alpha_t is applied to A_t before the split, exactly for
 // alpha = +-1); the three products hi*hi + hi*lo + lo*hi of every term
@@ -81,6 +82,29 @@ __device__ __forceinline__ void load_split(const float* __restrict__ src, int ld
   }
 }
 
+// An exact bf16 operand (rows x cols bf16, leading dimension ld) copied into
+// the hi tile, its sign flipped by `neg`; it needs no lo part.
+__device__ __forceinline__ void load_exact(const __nv_bfloat16* __restrict__ src, int ld, int rows,
+                                           int cols, bool neg, uint8_t* hi) {
+  const int groups = rows * cols / 8;
+  const int gpr = cols / 8;
+  const uint32_t flip = neg ? 0x80008000u : 0u;
+  for (int g0 = threadIdx.x; g0 < groups; g0 += 4 * kThreads) {
+    uint4 a[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int gi = g0 + u * kThreads, r = gi / gpr, c8 = gi - r * gpr;
+      a[u] = __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(r) * ld + c8 * 8));
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int gi = g0 + u * kThreads, r = gi / gpr, c8 = gi - r * gpr;
+      *reinterpret_cast<uint4*>(hi + swz_off(rows, r, c8 * 8)) =
+          make_uint4(a[u].x ^ flip, a[u].y ^ flip, a[u].z ^ flip, a[u].w ^ flip);
+    }
+  }
+}
+
 template <int N>
 __global__ void __launch_bounds__(kThreads, 3) gemm_tc_kernel(const __grid_constant__ TcGemmN g) {
   extern __shared__ uint8_t smem_raw[];
@@ -111,17 +135,21 @@ __global__ void __launch_bounds__(kThreads, 3) gemm_tc_kernel(const __grid_const
     const uint32_t id = idesc_bf16_f32(kM, N, tt.tA, !tt.tB);
     for (int k0 = 0; k0 < tt.K && ok; k0 += kKs, ++sl) {
       // op(A) slice: A[m][k0..] (K-major) or A[k0..][m] (MN-major), times alpha
-      if (tt.tA)
-        load_split(Az + static_cast<size_t>(k0) * tt.lda, tt.lda, kKs, kM, tt.alpha, base,
-                   base + kOffAlo);
+      const size_t aoff = tt.tA ? static_cast<size_t>(k0) * tt.lda : static_cast<size_t>(k0);
+      const int arows = tt.tA ? kKs : kM, acols = tt.tA ? kM : kKs;
+      if (tt.aBf)
+        load_exact(reinterpret_cast<const __nv_bfloat16*>(tt.A) + z * tt.sA + aoff, tt.lda, arows,
+                   acols, tt.alpha < 0.f, base);
       else
-        load_split(Az + k0, tt.lda, kM, kKs, tt.alpha, base, base + kOffAlo);
+        load_split(Az + aoff, tt.lda, arows, acols, tt.alpha, base, base + kOffAlo);
       // op(B) slice: B[k0..][n] (MN-major) or B[n][k0..] (K-major)
-      if (tt.tB)
-        load_split(Bz + k0, tt.ldb, N, kKs, 1.f, base + kOffBhi, base + kOffBlo);
+      const size_t boff = tt.tB ? static_cast<size_t>(k0) : static_cast<size_t>(k0) * tt.ldb;
+      const int brows = tt.tB ? N : kKs, bcols = tt.tB ? kKs : N;
+      if (tt.bBf)
+        load_exact(reinterpret_cast<const __nv_bfloat16*>(tt.B) + z * tt.sB + boff, tt.ldb, brows,
+                   bcols, false, base + kOffBhi);
       else
-        load_split(Bz + static_cast<size_t>(k0) * tt.ldb, tt.ldb, kKs, N, 1.f, base + kOffBhi,
-                   base + kOffBlo);
+        load_split(Bz + boff, tt.ldb, brows, bcols, 1.f, base + kOffBhi, base + kOffBlo);
       fence_proxy_async_smem();
       tc_fence_before_sync();
       __syncthreads();
@@ -130,6 +158,7 @@ __global__ void __launch_bounds__(kThreads, 3) gemm_tc_kernel(const __grid_const
         const uint32_t a0 = smem_addr(base), b0 = smem_addr(base + kOffBhi);
 #pragma unroll
         for (int term = 0; term < 3; ++term) {
+          if ((term == 1 && tt.bBf) || (term == 2 && tt.aBf)) continue;   // zero lo parts
           const uint32_t at = a0 + (term == 2 ? kOffAlo : 0);
           const uint32_t bt = b0 + (term == 1 ? kSliceB : 0);
 #pragma unroll

@@ -230,6 +230,10 @@ struct TcTerm {
   int lda, ldb, K;
   bool tA, tB;
   float alpha;
+  // operand stored as bf16 (pointer reinterpreted, leading dimension in
+  // elements): exact in one bf16 part, so its lo products are skipped; a bf16
+  // A needs alpha = +-1
+  bool aBf = false, bBf = false;
 };
 struct TcGemmN {
   TcTerm t[kMaxTerms];
