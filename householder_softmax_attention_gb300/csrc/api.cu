@@ -222,13 +222,16 @@ int path_attn_bwd_launches_per_call(int T, int d, int dtype, int with_gate) {
   if (C < 0) return C;
   if (T < 1) return PATH_ERR_INVALID_ARG;
   const int g = with_gate ? 1 : 0;
-  // chunk pass: fp32 copies, 30 GEMMs, 4 elementwise steps, inverse, dbeta,
-  // outputs, gate scan
-  const int chunk = 1 + 30 + 4 + 1 + 1 + 1 + g;
   if (dtype == PATH_DTYPE_BF16) {
+    // chunk pass: input copies, 17 tensor-core products (the scaled second
+    // outputs in their epilogues), inverse (with U), dbeta, outputs, gate scan
+    const int chunk = 1 + 17 + 1 + 1 + 1 + g;
     // preparation (+ gate prefix), rowdot, [X walk], key pass, G walk, dF
     return (1 + g) + 1 + (T > C ? 1 : 0) + 3 + chunk;
   }
+  // chunk pass: fp32 copies, 30 one-term GEMMs, 3 scaled copies, inverse,
+  // U, dbeta, outputs, gate scan
+  const int chunk = 1 + 30 + 3 + 1 + 1 + 1 + 1 + g;
   // SIMT preparation (+ gate prefix), rowdot, query walk, key pass, dF
   return (11 + g) + 1 + 3 + chunk;
 }

@@ -530,11 +530,15 @@ __global__ void bwd_tri_inv_kernel(const float* Lm, float* Xi, int C) {
 // The same inverse for C = 128 by recursive doubling (the forward
 // preparation's solver, tensor cores for the 32- and 64-blocks); 256 threads.
 constexpr int kSolveStride = 132;
-__global__ void __launch_bounds__(256) bwd_tri_inv128_kernel(const float* Lm, float* Xi) {
+// Also writes U = Xi diag(beta).
+__global__ void __launch_bounds__(256) bwd_tri_inv128_kernel(const float* Lm, float* Xi,
+                                                             const float* bf, float* Uo) {
   extern __shared__ float sl[];
   const size_t ch = blockIdx.x;
   const float* L = Lm + ch * 128 * 128;
   float* X = Xi + ch * 128 * 128;
+  float* U = Uo + ch * 128 * 128;
+  const float* be = bf + ch * 128;
   for (int x = threadIdx.x; x < 128 * 32; x += 256) {
     const int i = x >> 5, c4 = (x & 31) * 4;
     *reinterpret_cast<float4*>(sl + i * kSolveStride + c4) =
@@ -550,6 +554,8 @@ __global__ void __launch_bounds__(256) bwd_tri_inv128_kernel(const float* Lm, fl
     if (c4 + 2 > i) v.z = 0.f;
     if (c4 + 3 > i) v.w = 0.f;
     *reinterpret_cast<float4*>(X + i * 128 + c4) = v;
+    const float4 b = *reinterpret_cast<const float4*>(be + c4);
+    *reinterpret_cast<float4*>(U + i * 128 + c4) = make_float4(v.x * b.x, v.y * b.y, v.z * b.z, v.w * b.w);
   }
 }
 
@@ -716,8 +722,17 @@ struct Term {
 // C = mask(sum of the terms + add) over the batch; add may be null or C.  The
 // tensor-core kernel does it in one launch; the fp32 path copies add into C
 // and accumulates the terms one GEMM at a time.
+// A second output C2 (scaled copy of C, see TcGemmN) is written by the
+// tensor-core kernel's epilogue, else by the elementwise kernel afterwards
+// (op 0: strictLower(diag(vec) C), 1: C diag(vec), 2: diag(vec) C).
+struct Out2 {
+  float* C2 = nullptr;
+  const float* vec = nullptr;
+  int op = 0;
+};
 cudaError_t mgemm(const GemmCtx& gx, int batch, int M, int N, std::initializer_list<Term> terms,
-                  float* Cm, int ldc, long long sC, const float* add, int mask) {
+                  float* Cm, int ldc, long long sC, const float* add, int mask,
+                  Out2 o2 = Out2{}) {
   if (gx.tc) {
     TcGemmN g{};
     g.nterms = 0;
@@ -738,6 +753,12 @@ cudaError_t mgemm(const GemmCtx& gx, int batch, int M, int N, std::initializer_l
     g.batch = batch;
     g.mask = mask;
     g.status = gx.status;
+    if (o2.C2) {
+      g.C2 = o2.C2;
+      g.vec = o2.vec;
+      g.c2op = o2.op == 1 ? 2 : 1;           // C diag(vec): columns; else rows
+      g.c2mask = o2.op == 0 ? 2 : 0;         // op 0 is strictly lower
+    }
     if (gemm_tc_supported(g)) return launch_gemm_tc(g, gx.st);
   }
   for (const Term& t : terms)
@@ -754,6 +775,11 @@ cudaError_t mgemm(const GemmCtx& gx, int batch, int M, int N, std::initializer_l
                   Cm, ldc, sC, acc, mask)) != cudaSuccess)
       return e;
     acc = true;
+  }
+  if (o2.C2) {
+    if (M != N || ldc != M || sC != static_cast<long long>(M) * M) return cudaErrorInvalidValue;
+    bwd_chunk_elem_kernel<<<batch, 256, 0, gx.st>>>(Cm, o2.C2, o2.vec, M, o2.op);
+    return cudaGetLastError();
   }
   return cudaSuccess;
 }
@@ -806,23 +832,24 @@ cudaError_t launch_bwd_t(const BwdParams& p, const ChunkBufs& cb, cudaStream_t s
     return Term{al, A, C, cc, tA, B, D, cd, false, C};
   };
   // forward factors
-  if ((e = mgemm(gx, nch, C, C, {CD_DC(1.f, W, false, W, true)}, cb.GWW, C, cc, nullptr, 0)))
+  // GWW = W W^T, Lm = strictLower(diag(beta) GWW)
+  if ((e = mgemm(gx, nch, C, C, {CD_DC(1.f, W, false, W, true)}, cb.GWW, C, cc, nullptr, 0,
+                 Out2{cb.Lm, cb.bf, 0})))
     return e;
-  bwd_chunk_elem_kernel<<<nch, 256, 0, st>>>(cb.GWW, cb.Lm, cb.bf, C, 0);
   if (C == 128) {
     const int smem = 128 * kSolveStride * static_cast<int>(sizeof(float));
     if ((e = cudaFuncSetAttribute(bwd_tri_inv128_kernel,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
       return e;
-    bwd_tri_inv128_kernel<<<nch, 256, smem, st>>>(cb.Lm, cb.Xi);
+    bwd_tri_inv128_kernel<<<nch, 256, smem, st>>>(cb.Lm, cb.Xi, cb.bf, cb.U);
   } else {
     const int tri_smem = 2 * C * C * static_cast<int>(sizeof(float));
     if ((e = cudaFuncSetAttribute(bwd_tri_inv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   tri_smem)) != cudaSuccess)
       return e;
     bwd_tri_inv_kernel<<<nch, C, tri_smem, st>>>(cb.Lm, cb.Xi, C);
+    bwd_chunk_elem_kernel<<<nch, 256, 0, st>>>(cb.Xi, cb.U, cb.bf, C, 1);
   }
-  bwd_chunk_elem_kernel<<<nch, 256, 0, st>>>(cb.Xi, cb.U, cb.bf, C, 1);
   if ((e = mgemm(gx, nch, C, C, {CD_DC(1.f, W, false, K, true)}, cb.Nm, C, cc, nullptr, 2)) ||
       (e = mgemm(gx, nch, C, C, {CC(1.f, cb.U, false, cb.Nm, false)}, cb.TK, C, cc, nullptr, 0)) ||
       (e = mgemm(gx, nch, C, D, {CC_CD(1.f, cb.U, false, W)}, cb.UW, D, cd, nullptr, 0)) ||
@@ -853,29 +880,25 @@ cudaError_t launch_bwd_t(const BwdParams& p, const ChunkBufs& cb, cudaStream_t s
       (e = mgemm(gx, nch, C, D, {Term{1.f, W, D, cd, false, dF, D, dd, true, D}}, cb.P2, D, cd,
                  nullptr, 0)))
     return e;
-  // dU = -P2 W^T + dTK N^T + dUW W^T
+  // dU = -P2 W^T + dTK N^T + dUW W^T, dXi = dU diag(beta)
   if ((e = mgemm(gx, nch, C, C,
                  {CD_DC(-1.f, cb.P2, false, W, true), CC(1.f, cb.dTK, false, cb.Nm, true),
                   CD_DC(1.f, cb.dUW, false, W, true)},
-                 cb.dU, C, cc, nullptr, 0)))
+                 cb.dU, C, cc, nullptr, 0, Out2{cb.dXi, cb.bf, 1})))
     return e;
-  // dW = -TK dKr - U P1 - U^T P2 + dM^T Q + dN K + U^T dUW  (+ the Lm terms below)
+  // T1 = Xi^T dXi; dLm = strictLower(-T1 Xi^T), BL = diag(beta) dLm
+  if ((e = mgemm(gx, nch, C, C, {CC(1.f, cb.Xi, true, cb.dXi, false)}, cb.T1, C, cc, nullptr, 0)) ||
+      (e = mgemm(gx, nch, C, C, {CC(-1.f, cb.T1, false, cb.Xi, true)}, cb.dLm, C, cc, nullptr, 2,
+                 Out2{cb.BL, cb.bf, 2})))
+    return e;
+  bwd_dbeta_kernel<<<nch, 256, 0, st>>>(cb.Xi, cb.dU, cb.dLm, cb.GWW, cb.dbf, C);
+  // dW = -TK dKr - U P1 - U^T P2 + dM^T Q + dN K + U^T dUW + BL W + BL^T W
   if ((e = mgemm(gx, nch, C, D,
                  {CC_CD(-1.f, cb.TK, false, dKr), CC_CD(-1.f, cb.U, false, cb.P1),
                   CC_CD(-1.f, cb.U, true, cb.P2), CC_CD(1.f, cb.dM, true, Q),
-                  CC_CD(1.f, cb.dN, false, K), CC_CD(1.f, cb.U, true, cb.dUW)},
+                  CC_CD(1.f, cb.dN, false, K), CC_CD(1.f, cb.U, true, cb.dUW),
+                  CC_CD(1.f, cb.BL, false, W), CC_CD(1.f, cb.BL, true, W)},
                  cb.dWf, D, cd, nullptr, 0)))
-    return e;
-  // dXi = dU diag(beta); T1 = Xi^T dXi; dLm = strictLower(-T1 Xi^T)
-  bwd_chunk_elem_kernel<<<nch, 256, 0, st>>>(cb.dU, cb.dXi, cb.bf, C, 1);
-  if ((e = mgemm(gx, nch, C, C, {CC(1.f, cb.Xi, true, cb.dXi, false)}, cb.T1, C, cc, nullptr, 0)) ||
-      (e = mgemm(gx, nch, C, C, {CC(-1.f, cb.T1, false, cb.Xi, true)}, cb.dLm, C, cc, nullptr, 2)))
-    return e;
-  bwd_dbeta_kernel<<<nch, 256, 0, st>>>(cb.Xi, cb.dU, cb.dLm, cb.GWW, cb.dbf, C);
-  // BL = diag(beta) dLm; dW += BL W + BL^T W
-  bwd_chunk_elem_kernel<<<nch, 256, 0, st>>>(cb.dLm, cb.BL, cb.bf, C, 2);
-  if ((e = mgemm(gx, nch, C, D, {CC_CD(1.f, cb.BL, false, W), CC_CD(1.f, cb.BL, true, W)}, cb.dWf,
-                 D, cd, cb.dWf, 0)))
     return e;
   bwd_chunk_outputs_kernel<ET><<<dim3((p.T * (D / 8) + 255) / 256, p.BH < 65535 ? p.BH : 65535), 256, 0, st>>>(p, cb);
   if (p.dlogf) bwd_gate_kernel<<<p.BH, 1024, 0, st>>>(p);

@@ -2,7 +2,8 @@
 // sm_103a tensor cores.
 //
 //   C[z] = mask(sum_t alpha_t op(A_t[z]) op(B_t[z]) + (Add ? Add[z] : 0)),
-//   z = 0 .. batch-1, up to kMaxTerms products t
+//   z = 0 .. batch-1, up to kMaxTerms products t, and optionally
+//   C2[z] = mask2(C[z] with rows or columns scaled by a per-item vector)
 //
 // fp32 row-major operands (M = 128 rows, N and every K_t in {64, 128}), one
 // CTA of four warps per batch item; an operand flagged bf16 is an exact bf16
@@ -103,6 +104,17 @@ __device__ __forceinline__ void load_exact(const __nv_bfloat16* __restrict__ src
           make_uint4(a[u].x ^ flip, a[u].y ^ flip, a[u].z ^ flip, a[u].w ^ flip);
     }
   }
+}
+
+// Columns n0 .. n0 + 3 of row r with the triangular mask applied: mask 1
+// keeps n <= r, mask 2 keeps n < r.
+__device__ __forceinline__ float4 mask4(float4 o, int mask, int r, int n0) {
+  const int lim = mask == 1 ? r : r - 1;
+  if (n0 > lim) o.x = 0.f;
+  if (n0 + 1 > lim) o.y = 0.f;
+  if (n0 + 2 > lim) o.z = 0.f;
+  if (n0 + 3 > lim) o.w = 0.f;
+  return o;
 }
 
 template <int N>
@@ -209,15 +221,20 @@ __global__ void __launch_bounds__(kThreads, 3) gemm_tc_kernel(const __grid_const
         const float4 c = *reinterpret_cast<const float4*>(Dz + static_cast<size_t>(r) * g.ldadd + 4 * j);
         o.x += c.x; o.y += c.y; o.z += c.z; o.w += c.w;
       }
-      if (g.mask != 0) {
-        const int lim = g.mask == 1 ? r : r - 1;  // keep n <= lim
-        const int n0 = 4 * j;
-        if (n0 > lim) o.x = 0.f;
-        if (n0 + 1 > lim) o.y = 0.f;
-        if (n0 + 2 > lim) o.z = 0.f;
-        if (n0 + 3 > lim) o.w = 0.f;
-      }
+      if (g.mask != 0) o = mask4(o, g.mask, r, 4 * j);
       *reinterpret_cast<float4*>(Cz + static_cast<size_t>(r) * g.ldc + 4 * j) = o;
+      if (g.C2) {
+        const float* vz = g.vec + z * kM;
+        if (g.c2op == 1) {
+          const float b = vz[r];
+          o.x *= b; o.y *= b; o.z *= b; o.w *= b;
+        } else {
+          const float4 b = *reinterpret_cast<const float4*>(vz + 4 * j);
+          o.x *= b.x; o.y *= b.y; o.z *= b.z; o.w *= b.w;
+        }
+        if (g.c2mask != 0) o = mask4(o, g.c2mask, r, 4 * j);
+        *reinterpret_cast<float4*>(g.C2 + z * g.sC + static_cast<size_t>(r) * g.ldc + 4 * j) = o;
+      }
     }
   } else if (threadIdx.x == 0) {
     atomicExch(g.status, PATH_DEV_ERR_TIMEOUT);
@@ -245,6 +262,8 @@ cudaError_t launch_n(const TcGemmN& g, cudaStream_t st) {
 bool gemm_tc_supported(const TcGemmN& g) {
   if (g.M != kM || (g.N != 64 && g.N != 128) || g.nterms < 1 || g.nterms > kMaxTerms ||
       g.ldc % 4 != 0 || (g.Add && g.ldadd % 4 != 0))
+    return false;
+  if (g.C2 && (!g.vec || (g.c2op != 1 && g.c2op != 2) || (g.c2op == 2 && g.N != kM)))
     return false;
   for (int t = 0; t < g.nterms; ++t) {
     const TcTerm& tt = g.t[t];

@@ -222,7 +222,7 @@ cudaError_t launch_bwd_pairs_tc(const BwdParams& p, int* status, cudaStream_t st
 // split into bf16 hi + lo, M = 128, N and every K_t in {64, 128}; op(X) = X^T
 // when tX.  Add may be null (nothing added) or alias Cm.  mask 0: none,
 // 1: keep n <= m, 2: keep n < m (others written as 0).
-constexpr int kMaxTerms = 6;
+constexpr int kMaxTerms = 8;
 struct TcTerm {
   const float* A;
   const float* B;
@@ -243,6 +243,12 @@ struct TcGemmN {
   long long sC, sAdd;
   int ldc, ldadd, M, N, batch, mask;
   int* status;
+  // optional second output, same layout as C: C2 = mask2(C scaled by the
+  // batch item's vector: op 1 rows (vec[r]), op 2 columns (vec[n])), vec
+  // holding M values per batch item
+  float* C2 = nullptr;
+  const float* vec = nullptr;
+  int c2op = 0, c2mask = 0;
 };
 bool gemm_tc_supported(const TcGemmN& g);
 cudaError_t launch_gemm_tc(const TcGemmN& g, cudaStream_t st);
