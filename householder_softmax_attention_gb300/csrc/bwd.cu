@@ -591,24 +591,38 @@ __global__ void __launch_bounds__(256) bwd_chunk_elem_kernel(const float* in, fl
   }
 }
 
-// dbeta_j = sum_i Xi_ij dU_ij + sum_m dLm_jm GWW_jm; one block of 256 per
-// chunk: the column sums by threads j < C, the row sums by a warp per row.
+// dbeta_j = sum_i Xi_ij dU_ij + sum_m dLm_jm GWW_jm (Xi lower, dLm strictly
+// lower triangular); one block of 256 per chunk: the row sums by a warp per
+// row, the column sums by all threads.
 __global__ void __launch_bounds__(256) bwd_dbeta_kernel(const float* Xi, const float* dU,
                                                         const float* dLm, const float* GWW,
                                                         float* dbf, int C) {
-  __shared__ float rows[128];
+  __shared__ float rows[128], cols[256];
   const int ch = blockIdx.x, tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const size_t o = static_cast<size_t>(ch) * C * C;
   for (int j = warp; j < C; j += 8) {
     float s = 0.f;
-    for (int m = lane; m < C; m += 32) s = fmaf(dLm[o + j * C + m], GWW[o + j * C + m], s);
+    for (int m = lane; m < j; m += 32) s = fmaf(dLm[o + j * C + m], GWW[o + j * C + m], s);
     s = warp_sum(s);
     if (lane == 0) rows[j] = s;
   }
+  // column sums (Xi is lower triangular: rows r >= c): 256 / C threads per
+  // column, each over every (256 / C)-th row, with independent partial sums
+  // so that several loads are in flight
+  const int nh = 256 / C, c = tid % C, h = tid / C;
+  float a[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int i = h; i < C; i += 4 * nh) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int r = i + u * nh;
+      if (r < C && r >= c) a[u] = fmaf(Xi[o + r * C + c], dU[o + r * C + c], a[u]);
+    }
+  }
+  cols[tid] = (a[0] + a[1]) + (a[2] + a[3]);
   __syncthreads();
   if (tid < C) {
     float s = rows[tid];
-    for (int i = 0; i < C; ++i) s = fmaf(Xi[o + i * C + tid], dU[o + i * C + tid], s);
+    for (int q = 0; q < nh; ++q) s += cols[q * C + tid];
     dbf[static_cast<size_t>(ch) * C + tid] = s;
   }
 }
