@@ -103,6 +103,27 @@ def test_near_reflection_mix_and_batches():
     _full_case(Workload("refl_mix", 2, 3, 520, 64, "bf16", near_reflection=True, seed=3))
 
 
+@pytest.mark.parametrize("dtype,d,spread", [("bf16", 128, 0.1), ("bf16", 64, 0.1),
+                                            ("bf16", 128, 0.02), ("f32", 64, 0.1)])
+def test_correlated_directions_near_reflections(dtype, d, spread):
+    """Nearly equal directions w_t (per head a common unit vector plus noise of
+    norm about `spread`) with beta in [1.9, 2): every Gram block of a chunk is
+    close to all-ones, the hardest input for the chunk's triangular inverse
+    U = (I + strictLower(D W W^T))^{-1} D and its doubling levels."""
+    wl = Workload("corr_w", 1, 2, 400, d, dtype, beta_range=(1.9, 2.0), seed=17)
+    x = make_inputs(wl)
+    g = np.random.default_rng(17)
+    base = g.standard_normal((1, 2, 1, d))
+    base /= np.linalg.norm(base, axis=-1, keepdims=True)
+    w = base + spread * g.standard_normal((1, 2, wl.T, d)) / math.sqrt(d)
+    w /= np.linalg.norm(w, axis=-1, keepdims=True)
+    x["w"] = torch.tensor(w, dtype=x["w"].dtype)
+    out, lse = _run(x)
+    ro, rl = path_oracle_fwd(_np(x["q"]), _np(x["k"]), _np(x["v"]), _np(x["w"]),
+                             _np(x["beta"]), _np(x["logf"]), x["scale"])
+    _check(_np(out), _np(lse), ro, rl, dtype == "bf16", f"corr_w {dtype} d={d} {spread}")
+
+
 def test_beta_zero_matches_sdpa_on_device():
     """beta = 0: PaTH is plain causal softmax attention."""
     wl = Workload("beta0", 1, 4, 777, 128, "bf16", beta_range=(0.0, 0.0), seed=9)
