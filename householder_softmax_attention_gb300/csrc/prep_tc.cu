@@ -6,16 +6,19 @@
 // representation makes paths computable" and "Backup: fix orientation before
 // implementing UT products").  Phases:
 //
-//   P1  [W W^T | W K^T] = W [W; K]^T and [Q W^T | Q K^T] = Q [W; K]^T:
-//       two MMAs of width 256 per k-step (exact fp32 products of bf16 inputs)
-//   P2  L = strictLower(D W W^T) -> fp32 shared memory;
-//       S = strictLower(W K^T) -> bf16 hi / lo tiles
-//   P3  X = (I + L)^{-1} (prep_solve.cuh), U = X D -> bf16 hi / lo
+//   P1  [W W^T | W K^T] = W [W; K]^T, then [Q W^T | Q K^T] = Q [W; K]^T:
+//       MMAs of width 256 (exact fp32 products of bf16 inputs), committed
+//       separately so that the second runs during P2 and P3
+//   P2  the 32 x 32 diagonal blocks of L = strictLower(D W W^T) -> fp32
+//   P3  U = X D, X = (I + L)^{-1}, as bf16 hi / lo tiles: the diagonal
+//       blocks of X on the CUDA cores (prep_solve.cuh), the doubling levels
+//       of 32 and 64 on tcgen05 through U_ba = -U_bb (W W^T)_ba U_aa;
+//       S = strictLower(W K^T) -> bf16 hi / lo tiles over Q
 //   P4  TK = U S (three hi/lo products), UW = U W (two)
 //   P5  TK, UW -> bf16 hi / lo tiles, laid out as [TK | UW]
 //   P6a kr' = TK^T W, ngt' = UW^T W   (two terms each; at d = 64 the
 //       accumulator rows of ngt' past d are never read)
-//       kr = K - kr', ngt = -ngt'
+//       kr = K - kr', ngt = -ngt' (rows stored while P6b runs)
 //   P6b [sd' | ql'] = -lower(Q W^T) [TK | UW]   (A from TMEM, three terms)
 //       sdt = log2(e) (scale (Q K^T + sd') + gate) transposed, ql = Q + ql'
 //
