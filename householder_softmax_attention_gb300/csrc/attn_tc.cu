@@ -87,23 +87,47 @@ __device__ __forceinline__ void record_timeout(Bars* bars, int* status) {
   atomicExch(status, PATH_DEV_ERR_TIMEOUT);
 }
 
-// Row max / min of 128 values held as bit patterns, as eight independent
-// chains (a single chain would put 128 dependent operations on the path).
+// Row max / min of 128 values held as bit patterns: three-input max / min in
+// four independent chains (a single chain would put every operation on the
+// path).
 __device__ __forceinline__ float row_max(const uint32_t (&x)[128]) {
-  float m[8];
+  float m[4];
 #pragma unroll
-  for (int u = 0; u < 8; ++u) m[u] = __uint_as_float(x[u]);
+  for (int u = 0; u < 4; ++u) m[u] = __uint_as_float(x[u]);
 #pragma unroll
-  for (int j = 8; j < 128; ++j) m[j & 7] = fmaxf(m[j & 7], __uint_as_float(x[j]));
-  return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
+  for (int j = 4; j < 128; j += 2)
+    m[(j >> 1) & 3] = max3f(m[(j >> 1) & 3], __uint_as_float(x[j]), __uint_as_float(x[j + 1]));
+  return max3f(m[0], m[1], fmaxf(m[2], m[3]));
 }
 __device__ __forceinline__ float row_min(const uint32_t (&x)[128]) {
-  float m[8];
+  float m[4];
 #pragma unroll
-  for (int u = 0; u < 8; ++u) m[u] = __uint_as_float(x[u]);
+  for (int u = 0; u < 4; ++u) m[u] = __uint_as_float(x[u]);
 #pragma unroll
-  for (int j = 8; j < 128; ++j) m[j & 7] = fminf(m[j & 7], __uint_as_float(x[j]));
-  return fminf(fminf(fminf(m[0], m[1]), fminf(m[2], m[3])), fminf(fminf(m[4], m[5]), fminf(m[6], m[7])));
+  for (int j = 4; j < 128; j += 2)
+    m[(j >> 1) & 3] = min3f(m[(j >> 1) & 3], __uint_as_float(x[j]), __uint_as_float(x[j + 1]));
+  return min3f(m[0], m[1], fminf(m[2], m[3]));
+}
+
+// p_j = 2^(mul x_j - m) for 128 values held as bit patterns, as bf16 pairs
+// in pk, returning their sum; the argument and the running sums go two values
+// per instruction (four packed partial sums).
+__device__ __forceinline__ float exp_row(const uint32_t (&x)[128], float mul, float m,
+                                         uint32_t (&pk)[64]) {
+  const uint64_t mulv = f2(mul, mul), negm = f2(-m, -m);
+  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+  for (int j = 0; j < 128; j += 2) {
+    float a0, a1;
+    f2_split(f2_fma(f2(__uint_as_float(x[j]), __uint_as_float(x[j + 1])), mulv, negm), a0, a1);
+    const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+    acc[(j >> 1) & 3] = f2_add(acc[(j >> 1) & 3], f2(p0, p1));
+    pk[j >> 1] = pack_bf16x2(p0, p1);
+  }
+  float s[8];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) f2_split(acc[u], s[2 * u], s[2 * u + 1]);
+  return ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
 }
 
 // End of every role: all 384 threads meet on named barrier 1, then warp 1
@@ -328,15 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < kC; ++j) x[j] = __float_as_uint(__ldg(sd + j * kC));
       m_used = row_max(x);
       uint32_t pk[64];
-      float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int j = 0; j < kC; j += 2) {
-        const float p0 = ex2_approx(__uint_as_float(x[j]) - m_used);
-        const float p1 = ex2_approx(__uint_as_float(x[j + 1]) - m_used);
-        part[(j / 2) & 7] += p0 + p1;
-        pk[j / 2] = pack_bf16x2(p0, p1);
-      }
-      l = ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
+      l = exp_row(x, 1.f, m_used, pk);
       tmem_st_x32(tP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
       tmem_st_x32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
       tmem_st_wait();
@@ -370,19 +386,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the chunk's gate prefix, loaded by the producer into the ring
         ok = mbar_wait(&bars->gate_full[n & 1], (n >> 1) & 1, abort_flag, LIM);
         if (!ok) break;
-        const float4* lg = reinterpret_cast<const float4*>(&bars->gate[n & 1][0]);
+        // z_j = lam2_j - scale S_j = -y_j, two per instruction; max y = -min z
+        const uint64_t* lg = reinterpret_cast<const uint64_t*>(&bars->gate[n & 1][0]);
+        const uint64_t nsl = f2(-sl2, -sl2);
 #pragma unroll
-        for (int j4 = 0; j4 < kC / 4; ++j4) {
-          const float4 g4 = lg[j4];
-          const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int j = j4 * 4 + u;
-            x[j] = __float_as_uint(fmaf(__uint_as_float(x[j]), sl2, -gv[u]));
-          }
+        for (int j = 0; j < kC; j += 2) {
+          float z0, z1;
+          f2_split(f2_fma(f2(__uint_as_float(x[j]), __uint_as_float(x[j + 1])), nsl, lg[j >> 1]),
+                   z0, z1);
+          x[j] = __float_as_uint(z0);
+          x[j + 1] = __float_as_uint(z1);
         }
         warp_arrive(&bars->gate_empty[n & 1]);
-        mx = row_max(x);
+        mx = -row_min(x);
       } else {
         // logits stay raw; the scale enters through the FFMA inside the exp
         if (sl2 >= 0.f) {
@@ -400,17 +416,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         l *= alpha;
       }
       uint32_t pk[64];
-      // gated logits are already scaled (log2 units); plain ones get the scale here
-      const float mul = kGate ? 1.f : sl2;
-      float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int j = 0; j < kC; j += 2) {
-        const float p0 = ex2_approx(fmaf(__uint_as_float(x[j]), mul, -m_used));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(x[j + 1]), mul, -m_used));
-        part[(j / 2) & 7] += p0 + p1;
-        pk[j / 2] = pack_bf16x2(p0, p1);
-      }
-      l += ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
+      // gated: x holds z = -y (scaled, log2 units); plain logits get the scale here
+      l += exp_row(x, kGate ? -1.f : sl2, m_used, pk);
       // P buffer and O are free once O += P_{c+1} V_{c+1} has completed
       ok = mbar_wait(&bars->pv_done, n & 1, abort_flag, LIM);
       if (!ok) break;
