@@ -71,11 +71,7 @@ __device__ __forceinline__ void load_split(const float* __restrict__ src, int ld
                           mul * b[u].x, mul * b[u].y, mul * b[u].z, mul * b[u].w};
       uint32_t h[4], l[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * e]), h1 = __float2bfloat16_rn(v[2 * e + 1]);
-        h[e] = pack_bf16x2(__bfloat162float(h0), __bfloat162float(h1));
-        l[e] = pack_bf16x2(v[2 * e] - __bfloat162float(h0), v[2 * e + 1] - __bfloat162float(h1));
-      }
+      for (int e = 0; e < 4; ++e) split_hilo2(v[2 * e], v[2 * e + 1], h[e], l[e]);
       const uint32_t off = swz_off(rows, r, c8 * 8);
       *reinterpret_cast<uint4*>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
       *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);

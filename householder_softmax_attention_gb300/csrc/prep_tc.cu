@@ -70,11 +70,7 @@ __device__ __forceinline__ void put_hilo8(uint8_t* hi_tile, uint8_t* lo_tile, in
                                           const float (&v)[8]) {
   uint32_t h[4], l[4];
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * u]), h1 = __float2bfloat16_rn(v[2 * u + 1]);
-    h[u] = pack_bf16x2(__bfloat162float(h0), __bfloat162float(h1));
-    l[u] = pack_bf16x2(v[2 * u] - __bfloat162float(h0), v[2 * u + 1] - __bfloat162float(h1));
-  }
+  for (int u = 0; u < 4; ++u) split_hilo2(v[2 * u], v[2 * u + 1], h[u], l[u]);
   const uint32_t off = tile_off(row, c8 * 8);
   *reinterpret_cast<uint4*>(hi_tile + off) = make_uint4(h[0], h[1], h[2], h[3]);
   *reinterpret_cast<uint4*>(lo_tile + off) = make_uint4(l[0], l[1], l[2], l[3]);
@@ -476,9 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int c = 64 * halfc + 2 * u;
       const float x0 = c <= row ? -__uint_as_float(v[2 * u]) : 0.f;
       const float x1 = c + 1 <= row ? -__uint_as_float(v[2 * u + 1]) : 0.f;
-      const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
-      ph[u] = pack_bf16x2(__bfloat162float(h0), __bfloat162float(h1));
-      pl[u] = pack_bf16x2(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+      split_hilo2(x0, x1, ph[u], pl[u]);
     }
     tmem_st_x32(tb + lb + 256 + 32 * halfc, ph);
     tmem_st_x32(tb + lb + 320 + 32 * halfc, pl);
