@@ -142,7 +142,26 @@ def test_beta_zero_matches_sdpa_on_device():
                                          ("bf16", 128, False), ("bf16", 64, True)])
 def test_chunk_factors_match_blockwise_oracle(dtype, d, fox):
     wl = Workload("factors", 1, 2, 300, d, dtype, fox=fox, seed=21)
+    _factor_case(wl, make_inputs(wl), dtype, fox)
+
+
+@pytest.mark.parametrize("d", [128, 64])
+def test_chunk_factors_correlated_directions(d):
+    """The chunk factors for nearly equal directions w_t with beta in [1.9, 2)
+    (every Gram block close to all-ones), against the blockwise oracle."""
+    wl = Workload("factors_corr", 1, 2, 300, d, "bf16", beta_range=(1.9, 2.0), seed=23)
     x = make_inputs(wl)
+    g = np.random.default_rng(23)
+    base = g.standard_normal((1, 2, 1, d))
+    base /= np.linalg.norm(base, axis=-1, keepdims=True)
+    w = base + 0.05 * g.standard_normal((1, 2, wl.T, d)) / math.sqrt(d)
+    w /= np.linalg.norm(w, axis=-1, keepdims=True)
+    x["w"] = torch.tensor(w, dtype=x["w"].dtype)
+    _factor_case(wl, x, "bf16", False)
+
+
+def _factor_case(wl, x, dtype, fox):
+    d = wl.d
     dev = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in x.items()}
     f = pa.path_attn_debug_factors(dev["q"], dev["k"], dev["w"], dev["beta"], dev["logf"],
                                    x["scale"])
@@ -168,8 +187,9 @@ def test_chunk_factors_match_blockwise_oracle(dtype, d, fox):
             tol_in = (2 ** -8) if bf else 2e-6
             np.testing.assert_allclose(kr, fc["Kr"], atol=2e-4 + tol_in * np.abs(fc["Kr"]).max())
             np.testing.assert_allclose(ngt, -fc["G"].T, atol=2e-4 + tol_in * np.abs(fc["G"]).max())
-            # bf16 inputs: the fused preparation rounds computed operands to tf32
-            # (2^-11) before its tensor-core products; sums of up to C such terms
+            # bf16 inputs: the fused preparation splits computed operands into
+            # bf16 hi + lo (about 16 bits) before its tensor-core products;
+            # sums of up to C such terms
             tol_tf32 = 5e-3 if bf else 2e-4
             np.testing.assert_allclose(ql, fc["Ql"], atol=tol_tf32)
             S = log2e * x["scale"] * fc["Adiag"]
