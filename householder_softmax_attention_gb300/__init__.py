@@ -21,7 +21,8 @@ import threading
 
 __all__ = [
     "PathAttnError", "load_library", "path_attn_fwd", "path_attn_fwd_host",
-    "path_attn_fwd_noalloc", "path_attn_debug_wait_timeout", "path_attn_prefill",
+    "path_attn_fwd_noalloc", "path_attn_noalloc_status", "path_attn_debug_wait_timeout",
+    "path_attn_prefill",
     "path_attn_decode_step", "DecodeCache", "path_attn_fwd_partial", "path_producer_fwd",
     "path_attn_bwd", "path_attn_bwd_workspace_bytes", "path_attn_bwd_launches_per_call",
     "path_attn_debug_factors", "path_attn_device_status", "path_attn_workspace_bytes",
@@ -105,6 +106,8 @@ def load_library(path: str | None = None):
         lib.path_attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, fp, fp, f, vp, fp, vp,
                                               i, i, i, i, i, vp]
         lib.path_attn_fwd_noalloc.restype = i
+        lib.path_attn_noalloc_status.argtypes = [i, i]
+        lib.path_attn_noalloc_status.restype = i
         lib.path_attn_fwd_partial.argtypes = [vp, vp, vp, vp, fp, fp, f, vp, fp, i, i, i, i, i,
                                               i, vp]
         lib.path_attn_fwd_partial.restype = i
@@ -245,6 +248,14 @@ def path_attn_fwd_noalloc(q, k, v, w, beta, logf=None, scale=None, out=None, lse
                                        B, H, T, d, _dtype_code(q), ctypes.c_void_p(st.cuda_stream))
     _check(rc, "path_attn_fwd_noalloc")
     return out, lse
+
+
+def path_attn_noalloc_status(device: int = 0, clear: bool = True) -> int:
+    """0 if no bounded wait of ``path_attn_fwd_noalloc``'s kernels expired
+    while they reported into the library's static status word (calls made
+    with ``status=None``), else PATH_ERR_TIMEOUT.  Synchronises the device;
+    allocates nothing."""
+    return load_library().path_attn_noalloc_status(device, 1 if clear else 0)
 
 
 def path_attn_fwd_partial(q, k, v, u, beta, logf=None, scale=None, out=None, lse=None,

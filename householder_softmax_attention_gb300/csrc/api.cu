@@ -717,26 +717,39 @@ struct NoAllocState {
 };
 NoAllocState g_noalloc[kMaxDevices];
 
-// Once per device, with that device current: look up the arrays' device
-// addresses (host code may not use the symbols themselves as pointers).
+// Once per device, with that device current: check that the device is the
+// one the library is built for (before anything loads the module holding the
+// arrays), then look up the arrays' device addresses (host code may not use
+// the symbols themselves as pointers).
 int noalloc_setup(NoAllocState** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return set_cuda_error(e);
-  if (dev < 0 || dev >= kMaxDevices) return PATH_ERR_UNSUPPORTED;
+  if (dev < 0 || dev >= kMaxDevices) {
+    std::snprintf(g_last_error, sizeof(g_last_error),
+                  "libpathattn keeps state for devices 0 .. %d; the current device is %d",
+                  kMaxDevices - 1, dev);
+    return PATH_ERR_UNSUPPORTED;
+  }
   std::lock_guard<std::mutex> lk(g_mu);
   NoAllocState& s = g_noalloc[dev];
   if (!s.ready) {
-    void* p = nullptr;
-    if ((e = cudaGetSymbolAddress(&p, g_noalloc_scratch)) != cudaSuccess) return set_cuda_error(e);
-    s.scratch = static_cast<char*>(p);
-    if ((e = cudaGetSymbolAddress(&p, g_noalloc_status)) != cudaSuccess) return set_cuda_error(e);
-    s.status = static_cast<int*>(p);
     if ((e = cudaDeviceGetAttribute(&s.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) !=
             cudaSuccess ||
         (e = cudaDeviceGetAttribute(&s.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) !=
             cudaSuccess)
       return set_cuda_error(e);
+    if (s.cc_major != 10 || s.cc_minor != 3) {
+      std::snprintf(g_last_error, sizeof(g_last_error),
+                    "libpathattn is built for sm_103a; this device is sm_%d%d", s.cc_major,
+                    s.cc_minor);
+      return PATH_ERR_UNSUPPORTED;
+    }
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, g_noalloc_scratch)) != cudaSuccess) return set_cuda_error(e);
+    s.scratch = static_cast<char*>(p);
+    if ((e = cudaGetSymbolAddress(&p, g_noalloc_status)) != cudaSuccess) return set_cuda_error(e);
+    s.status = static_cast<int*>(p);
     s.ready = true;
   }
   *out = &s;
@@ -768,12 +781,6 @@ extern "C" int path_attn_fwd_noalloc(const void* q, const void* k, const void* v
   }
   NoAllocState* s = nullptr;
   if ((rc = noalloc_setup(&s)) != PATH_OK) return rc;
-  if (s->cc_major != 10 || s->cc_minor != 3) {
-    std::snprintf(g_last_error, sizeof(g_last_error),
-                  "libpathattn is built for sm_103a; this device is sm_%d%d", s->cc_major,
-                  s->cc_minor);
-    return PATH_ERR_UNSUPPORTED;
-  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int* word = status ? status : s->status;
   cudaError_t e = cudaMemsetAsync(word, 0, sizeof(int), st);
@@ -785,4 +792,23 @@ extern "C" int path_attn_fwd_noalloc(const void* q, const void* k, const void* v
   e = g.bf16 ? launch_attn_tc(g, in, ws, word, st, nullptr) : launch_attn_f32(g, in, ws, st, nullptr);
   if (e != cudaSuccess) return set_cuda_error(e);
   return PATH_OK;
+}
+
+extern "C" int path_attn_noalloc_status(int device, int clear) {
+  int prev = 0;
+  cudaError_t e = cudaGetDevice(&prev);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  if ((e = cudaSetDevice(device)) != cudaSuccess) return set_cuda_error(e);
+  NoAllocState* s = nullptr;
+  int rc = noalloc_setup(&s);
+  int word = 0;
+  // a synchronous copy to a host int and a memset: nothing is allocated
+  if (rc == PATH_OK &&
+      ((e = cudaDeviceSynchronize()) != cudaSuccess ||
+       (e = cudaMemcpy(&word, s->status, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess ||
+       (clear && (e = cudaMemset(s->status, 0, sizeof(int))) != cudaSuccess)))
+    rc = set_cuda_error(e);
+  cudaSetDevice(prev);
+  if (rc != PATH_OK) return rc;
+  return word == PATH_DEV_OK ? PATH_OK : PATH_ERR_TIMEOUT;
 }

@@ -331,13 +331,18 @@ int path_attn_debug_wait_timeout(unsigned long long limit_ns, void* stream);
  * a steady-state serving loop with a fixed memory budget.  This entry runs
  * the same kernels as path_attn_fwd but takes its workspace from a static
  * device array of PATH_NOALLOC_SCRATCH_BYTES (64 MiB) inside the library, so
- * it allocates nothing.  Every GPU on which this entry has been called holds
- * that array until the process exits.
+ * it allocates nothing.  The array belongs to the library's host-API module:
+ * with lazy module loading (the CUDA default) only GPUs on which this entry
+ * (or path_attn_noalloc_status) has been called hold it; under eager module
+ * loading (CUDA_MODULE_LOADING=EAGER) every device on which the library
+ * creates or uses a context holds it, whatever entry is called.  A GPU that
+ * holds it keeps it until the process exits.
  *
  *   Arguments as path_attn_fwd, plus
  *   status  device int, or NULL: set to 0 at the start of the call, and to a
- *           non-zero value by a kernel whose bounded wait expired (NULL = a
- *           second static word in the library).
+ *           non-zero value by a kernel whose bounded wait expired.  With
+ *           NULL the kernels report into a second static word of the
+ *           library, which path_attn_noalloc_status() reads.
  *
  * Problems whose workspace (path_attn_workspace_bytes) exceeds the array are
  * rejected with PATH_ERR_UNSUPPORTED before any launch; the message says how
@@ -353,6 +358,21 @@ int path_attn_fwd_noalloc(const void* q, const void* k, const void* v, const voi
                           const float* beta, const float* logf, float scale, void* out,
                           float* lse, int* status, int B, int H, int T, int d, int dtype,
                           void* stream);
+
+/*
+ * path_attn_noalloc_status -- reads the static status word that
+ * path_attn_fwd_noalloc's kernels write when it was called with status NULL.
+ * The paper has no counterpart; this is a library interface.
+ *
+ * Selects `device` for the call (the previous device is restored),
+ * synchronises it, copies the word to the host and, if `clear` is non-zero,
+ * resets it to 0.  Allocates nothing.  Returns PATH_OK when no bounded wait
+ * expired since the word was last reset (every path_attn_fwd_noalloc call
+ * with status NULL resets it at its start), PATH_ERR_TIMEOUT when one did,
+ * PATH_ERR_UNSUPPORTED on a device other than sm_103a, PATH_ERR_CUDA on a
+ * CUDA error.
+ */
+int path_attn_noalloc_status(int device, int clear);
 
 #ifdef __cplusplus
 }

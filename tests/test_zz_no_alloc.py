@@ -89,3 +89,18 @@ def test_noalloc_rejects_problems_beyond_the_static_scratch(lib):
                                    wl.B, wl.H, wl.T, wl.d, pa.PATH_DTYPE_BF16, None)
     assert rc == UNSUPPORTED
     assert b"workspace" in lib.path_attn_last_error()
+
+
+@pytest.mark.gpu
+def test_noalloc_null_status_is_readable(lib):
+    """With status NULL the kernels report into the library's static word;
+    path_attn_noalloc_status reads it (0 after a call whose waits all ended)
+    and clears it, allocating nothing."""
+    wl = Workload("noalloc_null", 1, 2, 300, 128, "bf16", seed=35)
+    x = {n: (t.cuda() if torch.is_tensor(t) else t) for n, t in make_inputs(wl).items()}
+    ref_out, _ = pa.path_attn_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], None, x["scale"])
+    for _ in range(2):
+        out, _ = _noalloc(lib, x, None)
+        assert lib.path_attn_noalloc_status(0, 1) == 0
+        _close(out, ref_out, True)
+    assert pa.path_attn_noalloc_status(0, False) == 0
