@@ -252,16 +252,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// The driver's tensor-map encoder, looked up once: a function-local static
+// is initialised exactly once even when host threads make their first call
+// at the same time.
 PFN_cuTensorMapEncodeTiled_v12000 mix_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+    cudaDriverEntryPointQueryResult qr;
+    const bool found = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                        cudaEnableDefault, &qr) == cudaSuccess &&
+                       qr == cudaDriverEntryPointSuccess;
+    return found ? reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p) : nullptr;
+  }();
   return fn;
 }
 
