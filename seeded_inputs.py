@@ -12,6 +12,9 @@ Options:
   near_reflection -- a seeded 10% of tokens get beta ~ U[1.9, 2.0)
   fox             -- log f_t = log(sigmoid(N(2, 1))) in fp32 (PaTH-FoX gate)
   beta_range      -- draw every beta ~ U[lo, hi) instead (stress cases)
+  w_spread        -- nearly equal directions: per (b, h) one unit vector u,
+                     then w_t = u + w_spread * N(0, I) / sqrt(d), L2-normalised
+                     (every Gram entry of a chunk close to 1; stress case)
 The shapes follow the B x T x d grid of the PaTH authors' kernel-latency table
 (OpenReview rebuttal, "Efficiency Evaluation"), with H = 16 heads at d = 128
 and H = 32 at d = 64.  No dataset is involved.
@@ -39,6 +42,7 @@ class Workload:
     near_reflection: bool = False
     fox: bool = False
     beta_range: tuple | None = None
+    w_spread: float | None = None
     seed: int = 0
     note: str = field(default="", compare=False)
 
@@ -85,6 +89,11 @@ def make_inputs(wl: Workload, device="cpu"):
     v = normal(shape)
     w = normal(shape)
     w = w / w.norm(dim=-1, keepdim=True).clamp_min(1e-30)
+    if wl.w_spread is not None:
+        u = normal((wl.B, wl.H, 1, wl.d))
+        u = u / u.norm(dim=-1, keepdim=True).clamp_min(1e-30)
+        w = u + (wl.w_spread / math.sqrt(wl.d)) * normal(shape)
+        w = w / w.norm(dim=-1, keepdim=True).clamp_min(1e-30)
     bshape = shape[:-1]
     if wl.beta_range is not None:
         lo, hi = wl.beta_range

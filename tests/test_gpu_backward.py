@@ -123,3 +123,22 @@ def test_backward_identities_at_size(T, d, H, fox):
         assert float(dlogf[..., 0].abs().max()) <= 1e-2 * float(dlogf.abs().max())
     for g in (dq, dk, dv, dw, dbeta):
         assert bool(torch.isfinite(g).all())
+
+
+@pytest.mark.parametrize("dtype,d,fox,T", [("f32", 64, True, 70), ("f32", 128, False, 40),
+                                           ("bf16", 64, True, 100), ("bf16", 128, False, 64)])
+def test_backward_matches_literal_autograd_oracle(dtype, d, fox, T):
+    """The GPU gradients directly against autograd of the literal fp64
+    forward (oracle/backward.py: every logit k_j^T H_{j+1} ... H_i q_i formed
+    token by token), not only against the blockwise backward: one head,
+    ragged against the chunk at T = 70 and 100."""
+    from oracle.backward import path_oracle_bwd
+    wl = Workload("bwd_literal", 1, 1, T, d, dtype, fox=fox, seed=57 + T)
+    x, gi, _, _, grads = _run(wl, with_dlse=True)
+    sel = lambda t: None if t is None else _np(t[0, 0])
+    ref = path_oracle_bwd(sel(x["q"]), sel(x["k"]), sel(x["v"]), sel(x["w"]), sel(x["beta"]),
+                          sel(gi["dout"]), logf=sel(x["logf"]), scale=x["scale"],
+                          dlse=sel(gi["dlse"]))
+    names = ["q", "k", "v", "w", "beta"] + (["logf"] if fox else [])
+    for n, g in zip(names, grads):
+        _compare(dtype, _np(g[0, 0]), ref[n].numpy(), "d" + n)
