@@ -10,9 +10,13 @@ one decoding step of every (b, h) at the last position of a full key/value
 cache (keys rewritten in place); that line reports GB/s of algorithmic HBM
 traffic against the measured copy bandwidth.  With ``--workload bwd_<name>``
 one step is the forward and the backward of workload <name> (the pages time
-PaTH forward + backward together) and the line reports ms per step.  The JSON line reports issued TFLOP/s (formulas in ``step_flops``),
-ms per step, the roofline of the attention kernel, an end-to-end number
-through the host-buffer C-ABI entry, sampled SM clocks and a CPU-oracle
+PaTH forward + backward together) and the line reports ms per step.  The
+JSON line reports issued TFLOP/s (formulas in ``step_flops``), ms per step,
+the roofline of the attention kernel (against the measured bf16 burst peak,
+the stated spec peak and, for a second-long back-to-back loop, the measured
+sustained peak), an end-to-end number through the host-buffer C-ABI entry
+with the host link's own copy bandwidth beside it, sampled SM clocks, the
+d = 64 (H = 32) and FoX variants of the headline shape, and a CPU-oracle
 baseline.  ``--impl reference`` times the fp64 CPU oracle instead, on a
 bounded sample of the same workload.  Under torchrun (N > 1) every rank runs
 the full workload on its own GPU (independent replicas; weak scaling).
@@ -801,68 +805,165 @@ def run_reference(args, wl, flops):
     return 0
 
 
+# Dense BF16 tensor peak of one GB300 as NVIDIA states it (the stricter
+# denominator of the two spec figures in circulation; the other is 2250).
+SPEC_BF16_TFLOPS = 2500.0
+NOMINAL_BF16_TFLOPS = 2250.0
+# Workloads timed beside the headline one in the default run: the d = 64
+# variant of the long-context shape (H = 32) and the same shape with the FoX gate.
+VARIANTS = ("t16k_d64", "fox_t16k_d128")
+
+
+def _sustained_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f).get("bf16_tflops_sustained")
+    except Exception:
+        return None
+
+
+def _host_placement():
+    """Where pinned host buffers can live: this process's CPU set and the
+    host's NUMA nodes (read from sysfs; empty where absent)."""
+    info = {"cpus": len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else None}
+    try:
+        nodes = sorted(n for n in os.listdir("/sys/devices/system/node") if n.startswith("node"))
+        info["numa_nodes"] = len(nodes)
+        with open("/proc/self/status") as fh:
+            for line in fh:
+                if line.startswith("Mems_allowed_list"):
+                    info["mems_allowed"] = line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return info
+
+
+class ForwardRun:
+    """Inputs of one workload resident on the device and the timed forward."""
+
+    def __init__(self, pa, wl, dev, st):
+        import torch
+        from seeded_inputs import make_inputs
+        self.pa, self.wl, self.dev, self.st = pa, wl, dev, st
+        self.x = make_inputs(wl, device=dev)
+        x = self.x
+        self.q = x["q"]
+        self.out = torch.empty_like(x["q"])
+        self.lse = torch.empty(x["beta"].shape, device=dev, dtype=torch.float32)
+        self.flops = step_flops(wl.B, wl.H, wl.T, wl.d)
+
+    def step(self):
+        x = self.x
+        self.pa.path_attn_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["logf"], x["scale"],
+                              out=self.out, lse=self.lse, stream=self.st)
+
+    def timed(self, steps, warmup, world=1, local=0):
+        """Device time of `steps` forwards after `warmup`; per-kernel times
+        from the library's own events.  Returns a dict."""
+        import torch
+        pa = self.pa
+        for _ in range(warmup):
+            self.step()
+        torch.cuda.synchronize(self.dev)
+        assert pa.path_attn_device_status(local, True) == 0, "a kernel wait expired"
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        pa.path_attn_timing_enable(True)
+        barrier(world)
+        torch.cuda.synchronize(self.dev)
+        with ClockSampler(local) as clk:
+            e0.record(self.st)
+            for _ in range(steps):
+                self.step()
+            e1.record(self.st)
+            torch.cuda.synchronize(self.dev)
+        barrier(world)
+        ms = e0.elapsed_time(e1) / steps
+        prep_ms, attn_ms, calls = pa.path_attn_timing_read()
+        pa.path_attn_timing_enable(False)
+        assert calls == steps
+        assert pa.path_attn_device_status(local, True) == 0, "a kernel wait expired"
+        return {"ms": ms, "prep_ms": prep_ms / calls, "attn_ms": attn_ms / calls,
+                "clocks": clk.summary(), "steps": steps}
+
+    def summary(self, t, peak):
+        f = self.flops
+        total = f["attn"] + f["prep"]
+        attn_tf = f["attn"] / (t["attn_ms"] * 1e-3) / 1e12
+        return {"workload": self.wl.name, "B": self.wl.B, "H": self.wl.H, "T": self.wl.T,
+                "d": self.wl.d, "fox": self.wl.fox, "ms_per_step": t["ms"],
+                "tflops": total / (t["ms"] * 1e-3) / 1e12,
+                "attn_ms": t["attn_ms"], "attn_tflops": attn_tf,
+                "attn_frac_measured": attn_tf / peak, "attn_frac_spec": attn_tf / SPEC_BF16_TFLOPS,
+                "prep_ms": t["prep_ms"], "steps": t["steps"], "clocks": t["clocks"]}
+
+
 def run_gpu(args, wl, flops):
     import torch
 
     import householder_softmax_attention_gb300 as pa
-    from seeded_inputs import make_inputs
 
     rank, world, local = dist_setup()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     pa.load_library()
-    x = make_inputs(wl, device=dev)
-    q, k, v, w, beta, logf, scale = (x[n] for n in ("q", "k", "v", "w", "beta", "logf", "scale"))
-    out = torch.empty_like(q)
-    lse = torch.empty(beta.shape, device=dev, dtype=torch.float32)
     st = torch.cuda.current_stream(dev)
-
-    def step():
-        pa.path_attn_fwd(q, k, v, w, beta, logf, scale, out=out, lse=lse, stream=st)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
-    assert pa.path_attn_device_status(local, True) == 0, "a kernel wait expired"
-
-    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, w, beta) if t is not None)
-    ws_bytes = pa.path_attn_workspace_bytes(wl.B, wl.H, wl.T, wl.d, 1, logf is not None)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    pa.path_attn_timing_enable(True)
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clk:
-        e0.record(st)
-        for _ in range(args.steps):
-            step()
-        e1.record(st)
-        torch.cuda.synchronize(dev)
-    barrier(world)
-    ms = e0.elapsed_time(e1) / args.steps
-    prep_ms, attn_ms, calls = pa.path_attn_timing_read()
-    pa.path_attn_timing_enable(False)
-    assert calls == args.steps
-    assert pa.path_attn_device_status(local, True) == 0, "a kernel wait expired"
-    ms_max = reduce_max(ms, world)
+    run = ForwardRun(pa, wl, dev, st)
+    x = run.x
+    q, beta, logf, scale = x["q"], x["beta"], x["logf"], x["scale"]
+    t = run.timed(args.steps, args.warmup, world, local)
+    ms_max = reduce_max(t["ms"], world)
     total = flops["attn"] + flops["prep"]
     value = world * total / (ms_max * 1e-3) / 1e12
+    in_bytes = sum(a.numel() * a.element_size() for a in (x["q"], x["k"], x["v"], x["w"], beta,
+                                                          logf) if a is not None)
+    ws_bytes = pa.path_attn_workspace_bytes(wl.B, wl.H, wl.T, wl.d, 1, logf is not None)
 
     # roofline of the dominant kernel (the attention scan)
-    attn_avg_ms = attn_ms / calls
     peak, _, peak_src = _peaks()
-    achieved = flops["attn"] / (attn_avg_ms * 1e-3) / 1e12
+    sustained = _sustained_peak()
+    achieved = flops["attn"] / (t["attn_ms"] * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak,
                 "traffic": args.traffic if args.traffic is not None else (
                     traffic_record() if wl.name == DEFAULT_WORKLOAD else None),
                 "kernel": "attn_tc_kernel", "peak_source": f"{peak_src} bf16 burst",
-                "avg_launch_ms": attn_avg_ms, "prep_avg_ms": prep_ms / calls}
+                "frac_spec": achieved / SPEC_BF16_TFLOPS, "spec_peak": SPEC_BF16_TFLOPS,
+                "frac_nominal": achieved / NOMINAL_BF16_TFLOPS,
+                "nominal_peak": NOMINAL_BF16_TFLOPS,
+                "step_frac": value / world / peak, "step_frac_spec": value / world / SPEC_BF16_TFLOPS,
+                "avg_launch_ms": t["attn_ms"], "prep_avg_ms": t["prep_ms"]}
+
+    # the same step back to back for about a second: the sustained regime
+    n_sus = max(args.steps, int(math.ceil(args.sustain_s * 1e3 / max(t["ms"], 1e-3))))
+    ts = run.timed(n_sus, 1, world, local)
+    sus = {"ms_per_step": ts["ms"], "steps": n_sus, "seconds": ts["ms"] * n_sus * 1e-3,
+           "value": total / (ts["ms"] * 1e-3) / 1e12, "attn_ms": ts["attn_ms"],
+           "prep_ms": ts["prep_ms"], "clocks": ts["clocks"]}
+    if sustained:
+        sus["step_frac_sustained_peak"] = sus["value"] / sustained
+        sus["attn_frac_sustained_peak"] = flops["attn"] / (ts["attn_ms"] * 1e-3) / 1e12 / sustained
+        sus["sustained_peak"] = sustained
 
     # end to end through the host-buffer entry: H2D of the inputs from pinned
     # memory, the forward, D2H of out and lse, every step
-    hx = {n: (t.cpu().pin_memory() if torch.is_tensor(t) else t) for n, t in x.items()}
+    hx = {n: (a.cpu().pin_memory() if torch.is_tensor(a) else a) for n, a in x.items()}
     hout = torch.empty(q.shape, dtype=q.dtype).pin_memory()
     hlse = torch.empty(beta.shape, dtype=torch.float32).pin_memory()
+
+    # the host link on its own: one copy of q in and of out back, best of three
+    def copy_gbs(dst, src):
+        best = float("inf")
+        for _ in range(3):
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            c0.record(st)
+            dst.copy_(src, non_blocking=True)
+            c1.record(st)
+            torch.cuda.synchronize(dev)
+            best = min(best, c0.elapsed_time(c1))
+        return src.numel() * src.element_size() / (best * 1e-3) / 1e9
+
+    h2d_gbs = copy_gbs(run.out, hx["q"])
+    d2h_gbs = copy_gbs(hout, run.out)
 
     def e2e_step():
         pa.path_attn_fwd_host(hx["q"], hx["k"], hx["v"], hx["w"], hx["beta"], hx["logf"],
@@ -877,6 +978,7 @@ def run_gpu(args, wl, flops):
         e2e_step()
     e2e_ms = reduce_max((time.perf_counter() - t0) * 1e3 / n_e2e, world)
     d2h = hout.numel() * hout.element_size() + hlse.numel() * 4
+    del hx, hout, hlse
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -890,13 +992,29 @@ def run_gpu(args, wl, flops):
         "flops_per_step": {"attn": flops["attn"], "prep": flops["prep"]},
         "flash_equiv_tflops": world * flops["flash_equiv"] / (ms_max * 1e-3) / 1e12,
         "roofline": roofline,
+        "sustained": sus,
         "e2e": {"value": world * total / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": in_bytes,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "link": {"h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs,
+                         "copy_floor_ms": (in_bytes / h2d_gbs + d2h / d2h_gbs) * 1e-6,
+                         "host": _host_placement()}},
         "gpu_launches": args.steps * pa.path_attn_launches_per_call(
             wl.d, 1 if wl.dtype == "bf16" else 0, logf is not None),
-        "clocks": clk.summary(),
+        "clocks": t["clocks"],
     }
+    if wl.name == DEFAULT_WORKLOAD and not args.no_variants:
+        from seeded_inputs import WORKLOADS
+        del run
+        torch.cuda.empty_cache()
+        variants = {}
+        for name in VARIANTS:
+            vr = ForwardRun(pa, WORKLOADS[name], dev, st)
+            variants[name] = vr.summary(vr.timed(max(10, min(args.steps, 20)), 3, world, local),
+                                        peak)
+            del vr
+            torch.cuda.empty_cache()
+        line["variants"] = variants
     if rank == 0 and not args.no_cpu_baseline:
         threads = os.cpu_count() or 1
         sec_per_unit, desc = oracle_sample(wl, args.cpu_budget_s, threads)
@@ -919,6 +1037,10 @@ def main(argv=None):
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--ref-step-s", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the d = 64 and FoX workloads timed beside the headline one")
+    ap.add_argument("--sustain-s", type=float, default=1.0,
+                    help="seconds of back-to-back steps for the sustained figure")
     ap.add_argument("--no-graph", action="store_true", help="decoding: time the eager loop only")
     ap.add_argument("--B", type=int, default=None, help="override the workload's batch")
     ap.add_argument("--H", type=int, default=None, help="override the workload's heads")
