@@ -39,7 +39,12 @@ namespace {
 
 constexpr int kC = 128;       // chunk length = query tile = key tile
 constexpr int kThreads = 384;
-constexpr int kHeadGroup = 8;
+// Tiles launch in groups of 4 heads: the group's kr, ngt and V chunks (12 MB
+// per head at T = 16384, d = 128) then stay in L2 until its last tile has
+// read them.  Measured at B = 2, H = 16, T = 16384, d = 128 (DRAM bytes per
+// launch, ncu; floor 1.05 GB): groups of 16 heads 3.34 GB, 8 heads 1.83 GB,
+// 4 heads 1.09 GB, 2 heads 1.06 GB; attention 1.986 / 1.914 / 1.891 / 1.891 ms.
+constexpr int kHeadGroup = 4;
 constexpr int kRegsLow = 56, kRegsSoftmax = 240, kRegsQuery = 112;
 static_assert(128 * (kRegsLow + kRegsSoftmax + kRegsQuery) <= kThreads * 168, "register split");
 
