@@ -10,7 +10,10 @@ one decoding step of every (b, h) at the last position of a full key/value
 cache (keys rewritten in place); that line reports GB/s of algorithmic HBM
 traffic against the measured copy bandwidth.  With ``--workload bwd_<name>``
 one step is the forward and the backward of workload <name> (the pages time
-PaTH forward + backward together) and the line reports ms per step.  The
+PaTH forward + backward together) and the line reports ms per step;
+``--workload bwd_grid`` times forward + backward on every B x T x d row of
+the pages' latency table; ``--workload partial_<name>`` times partial PaTH
+(r = d/2) beside full PaTH.  The
 JSON line reports issued TFLOP/s (formulas in ``step_flops``), ms per step,
 the roofline of the attention kernel (against the measured bf16 burst peak,
 the stated spec peak and, for a second-long back-to-back loop, the measured
@@ -753,6 +756,142 @@ def run_bwd(args, wl):
     return 0
 
 
+def run_partial(args, wl):
+    """Partial PaTH (transitions on the first r = d/2 coordinates, plain dot
+    products on the rest) against full PaTH on the same inputs, timed in one
+    process; value = partial ms per step."""
+    import torch
+
+    import householder_softmax_attention_gb300 as pa
+    from seeded_inputs import make_inputs
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    pa.load_library()
+    st = torch.cuda.current_stream(dev)
+    x = make_inputs(wl, device=dev)
+    r = wl.d // 2
+    g = torch.Generator(device=dev).manual_seed(wl.seed + 5)
+    u = torch.randn((wl.B, wl.H, wl.T, r), generator=g, device=dev)
+    u = (u / u.norm(dim=-1, keepdim=True).clamp_min(1e-30)).to(x["q"].dtype).contiguous()
+    out = torch.empty_like(x["q"])
+    lse = torch.empty(x["beta"].shape, device=dev, dtype=torch.float32)
+
+    def full():
+        pa.path_attn_fwd(x["q"], x["k"], x["v"], x["w"], x["beta"], x["logf"], x["scale"],
+                         out=out, lse=lse, stream=st)
+
+    def partial():
+        pa.path_attn_fwd_partial(x["q"], x["k"], x["v"], u, x["beta"], x["logf"], x["scale"],
+                                 out=out, lse=lse, stream=st)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        assert pa.path_attn_device_status(0, True) == 0, "a kernel wait expired"
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        pa.path_attn_timing_enable(True)
+        with ClockSampler(0) as clk:
+            e0.record(st)
+            for _ in range(args.steps):
+                fn()
+            e1.record(st)
+            torch.cuda.synchronize(dev)
+        p, a, n = pa.path_attn_timing_read()
+        pa.path_attn_timing_enable(False)
+        assert pa.path_attn_device_status(0, True) == 0, "a kernel wait expired"
+        return {"ms_per_step": e0.elapsed_time(e1) / args.steps, "prep_ms": p / n,
+                "attn_ms": a / n, "clocks": clk.summary()}
+
+    tf, tp = timed(full), timed(partial)
+    line = {"metric": f"partial PaTH (r = d/2) fwd ms, {wl.name}", "value": tp["ms_per_step"],
+            "unit": "ms", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": tp["ms_per_step"], "higher_is_better": False, "dtype": wl.dtype,
+            "data": "synthetic",
+            "config": {"workload": "partial_" + wl.name, "B": wl.B, "H": wl.H, "T": wl.T,
+                       "d": wl.d, "r": r, "fox": wl.fox},
+            "partial": tp, "full": tf, "speedup_vs_full": tf["ms_per_step"] / tp["ms_per_step"],
+            "gpu_launches": args.steps * pa.path_attn_launches_per_call(
+                wl.d, 1 if wl.dtype == "bf16" else 0, wl.fox)}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# The pages' latency grid (rebuttal, "Efficiency Evaluation": PaTH Triton
+# forward + backward, hardware unstated), B x T x d with H = 16 at d = 128 and
+# H = 32 at d = 64; plain PaTH (the table's PaTH column).
+BWD_GRID = [(16, 2048, 128, 17.59), (16, 2048, 64, 11.95), (8, 4096, 128, 21.88),
+            (8, 4096, 64, 16.64), (4, 8192, 128, 30.90), (4, 8192, 64, 26.06),
+            (2, 16384, 128, 48.49), (2, 16384, 64, 43.89)]
+
+
+def run_bwd_grid(args):
+    """Forward + backward of every row of the pages' grid, one JSON line with
+    a row per configuration (ms per fwd+bwd step, the pages' Triton figure
+    beside it as context)."""
+    import torch
+
+    import householder_softmax_attention_gb300 as pa
+    from seeded_inputs import Workload, make_grad_inputs, make_inputs
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    pa.load_library()
+    st = torch.cuda.current_stream(dev)
+    rows = []
+    for B, T, d, pages in BWD_GRID:
+        H = 16 if d == 128 else 32
+        wl = Workload(f"t{T // 1024}k_d{d}", B, H, T, d)
+        x = make_inputs(wl, device=dev)
+        gi = make_grad_inputs(wl, device=dev)
+        q, k, v, w, beta, scale = (x[n] for n in ("q", "k", "v", "w", "beta", "scale"))
+        out = torch.empty_like(q)
+        lse = torch.empty(beta.shape, device=dev, dtype=torch.float32)
+        grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v),
+                 torch.empty_like(w), torch.empty_like(beta), None)
+
+        def fwd():
+            pa.path_attn_fwd(q, k, v, w, beta, None, scale, out=out, lse=lse, stream=st)
+
+        def bwd():
+            pa.path_attn_bwd(q, k, v, w, beta, out, lse, gi["dout"], scale=scale,
+                             dlse=gi["dlse"], grads=grads, stream=st)
+
+        for _ in range(max(args.warmup, 3)):
+            fwd()
+            bwd()
+        torch.cuda.synchronize(dev)
+        assert pa.path_attn_device_status(0, True) == 0, "a kernel wait expired"
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        fms, bms = [], []
+        for _ in range(args.steps):
+            ev[0].record(st)
+            fwd()
+            ev[1].record(st)
+            bwd()
+            ev[2].record(st)
+            torch.cuda.synchronize(dev)
+            fms.append(ev[0].elapsed_time(ev[1]))
+            bms.append(ev[1].elapsed_time(ev[2]))
+        assert pa.path_attn_device_status(0, True) == 0, "a kernel wait expired"
+        fm, bm = statistics.median(fms), statistics.median(bms)
+        rows.append({"B": B, "H": H, "T": T, "d": d, "fwd_ms": fm, "bwd_ms": bm,
+                     "fwd_bwd_ms": fm + bm, "pages_triton_fwd_bwd_ms": pages,
+                     "ratio_to_pages": (fm + bm) / pages})
+        print(f"B={B} T={T} d={d} H={H}: fwd {fm:.3f} ms + bwd {bm:.3f} ms = {fm + bm:.3f} ms "
+              f"(pages {pages} ms)", file=sys.stderr, flush=True)
+        del x, gi, q, k, v, w, beta, out, lse, grads
+        torch.cuda.empty_cache()
+    line = {"metric": "PaTH-attn fwd+bwd ms over the pages' B x T x d grid", "unit": "ms",
+            "value": sum(r["fwd_bwd_ms"] for r in rows), "n_gpus": 1, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "higher_is_better": False, "dtype": "bf16",
+            "data": "synthetic", "config": {"workload": "bwd_grid"}, "rows": rows,
+            "note": "value = sum over the rows; the pages' figures are Triton on unstated hardware"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_bwd_reference(args, wl):
     rank, world, _ = dist_setup()
     if rank != 0:
@@ -1058,6 +1197,18 @@ def main(argv=None):
         if args.B or args.H:
             wl = wl.with_(B=args.B or wl.B, H=args.H or wl.H)
         return run_decode_reference(args, wl) if args.impl == "reference" else run_decode(args, wl)
+    if args.workload.startswith("partial_") and args.workload[8:] in WORKLOADS:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "partial PaTH is timed against full PaTH on the GPU only"}))
+            return 0
+        return run_partial(args, WORKLOADS[args.workload[8:]])
+    if args.workload == "bwd_grid":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the grid is a GPU timing table; use bwd_<workload> for the oracle"}))
+            return 0
+        return run_bwd_grid(args)
     if args.workload.startswith("bwd_") and args.workload[4:] in WORKLOADS:
         wl = WORKLOADS[args.workload[4:]]
         if args.B or args.H:

@@ -342,6 +342,20 @@ int path_attn_fwd_partial(const void* q, const void* k, const void* v, const voi
   if ((rc = device_state(&s)) != PATH_OK) return rc;
   if ((rc = check_device(s)) != PATH_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (g.bf16 && d == 128 && r == 64 && aligned16(w)) {
+    // rank-64 transitions at d = 128: the preparation reads u through a
+    // tensor map of width r (zeros past it) and the attention carries only
+    // the first r coordinates of the running query through the transitions
+    void* ws = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, workspace_layout(g, nullptr, nullptr), s->pool, st);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    Inputs in{q, k, v, w, beta, logf, scale, out, lse};
+    in.wr = r;
+    rc = run_forward(g, in, static_cast<char*>(ws), s, st);
+    e = cudaFreeAsync(ws, st);
+    if (rc == PATH_OK && e != cudaSuccess) rc = set_cuda_error(e);
+    return rc;
+  }
   const size_t es = g.bf16 ? 2 : 4;
   const size_t rows = static_cast<size_t>(g.BH) * T;
   const size_t wbytes = align_up(rows * d * es, 256);

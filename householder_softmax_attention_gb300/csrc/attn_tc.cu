@@ -48,21 +48,26 @@ constexpr int kHeadGroup = 4;
 constexpr int kRegsLow = 56, kRegsSoftmax = 240, kRegsQuery = 112;
 static_assert(128 * (kRegsLow + kRegsSoftmax + kRegsQuery) <= kThreads * 168, "register split");
 
-template <int D>
+// D: head dimension; R: the coordinates the transitions act on (R = D for
+// PaTH; R < D for partial PaTH, whose running query changes only in its
+// first R coordinates and whose ngt_c vanishes outside its first R rows).
+template <int D, int R>
 struct TcCfg {
+  static_assert(R <= D && R % 64 == 0, "transition rank");
   static constexpr int kHalves = D / 64;           // 64-column (128-byte) halves
-  // One B tile per step stacks kr_c (kC rows) over ngt_c (D rows), so that
-  // S = Qw kr^T and the transition Qm += Qw ngt^T are a single MMA of width
-  // N = kC + D; tcgen05.mma pays a fixed cost per instruction below N = 256.
-  static constexpr int kKgRows = kC + D;
+  // One B tile per step stacks kr_c (kC rows) over the first R rows of ngt_c,
+  // so that S = Qw kr^T and the transition Qm += Qw ngt^T are a single MMA
+  // of width N = kC + R; tcgen05.mma pays a fixed cost per instruction below
+  // N = 256.
+  static constexpr int kKgRows = kC + R;
   static constexpr uint32_t kKgHalf = kKgRows * 128;  // one 64-column half
   static constexpr uint32_t kKgBytes = kHalves * kKgHalf;
   static constexpr uint32_t kVBytes = kC * D * 2;
   static constexpr uint32_t kColS = 0;             // S and Qm are adjacent: one
-  static constexpr uint32_t kColQm = 128;          // accumulator of width kC + D
-  static constexpr uint32_t kColO = 128 + D;
-  static constexpr uint32_t kColQw = 128 + 2 * D;
-  static constexpr uint32_t kColP = 128 + 2 * D + D / 2;
+  static constexpr uint32_t kColQm = 128;          // accumulator of width kC + R
+  static constexpr uint32_t kColO = 128 + R;
+  static constexpr uint32_t kColQw = 128 + R + D;
+  static constexpr uint32_t kColP = 128 + R + D + D / 2;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr size_t kTileBytes = 2 * (kKgBytes + kVBytes);
   static constexpr size_t kSmemBytes = kTileBytes + 1024 /*align*/ + 1280 /*barriers, gate*/;
@@ -155,7 +160,7 @@ __device__ __forceinline__ void teardown(int warp, uint32_t tb, uint32_t ncols) 
   }
 }
 
-template <int D, bool kGate>
+template <int D, bool kGate, int R>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap map_kr,
                    const __grid_constant__ CUtensorMap map_ng,
@@ -163,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const float* __restrict__ sdt, const float* __restrict__ lam2,
                    __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
                    int* __restrict__ status, int T, int Np, int BH, float sl2) {
-  using Cfg = TcCfg<D>;
+  using Cfg = TcCfg<D, R>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -283,8 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t tS = tb + Cfg::kColS, tQw = tb + Cfg::kColQw;
       constexpr uint32_t idS = idesc_bf16_f32(128, kC, false, false);       // S only
-      constexpr uint32_t idSQ = idesc_bf16_f32(128, kC + D, false, false);  // [S | Qm]
-      constexpr uint32_t idQ = idesc_bf16_f32(128, D, false, false);        // Qm only
+      constexpr uint32_t idSQ = idesc_bf16_f32(128, kC + R, false, false);  // [S | Qm]
+      constexpr uint32_t idQ = idesc_bf16_f32(128, R, false, false);        // Qm only
       bool ok = true;
       for (int n = 0; n < b && ok; ++n) {
         const int c = b - 1 - n, s = n & 1;
@@ -296,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         const uint32_t kg_a = smem_addr(s_kg + s * Cfg::kKgBytes);
         // the logits and the backward crossing of chunk c in one MMA of width
-        // kC + D; the last chunk needs no crossing.  S starts from zero:
+        // kC + R; the last chunk needs no crossing.  S starts from zero:
         // either the first k-step writes it alone (the crossing part
         // accumulating into Qm) or the softmax warps cleared it
         const uint32_t id = c > 0 ? idSQ : idS;
@@ -512,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           m32[4 * u + 2] = __float_as_uint(f.z);
           m32[4 * u + 3] = __float_as_uint(f.w);
         }
-        tmem_st_x32(tQm + cc, m32);
+        if (cc < R) tmem_st_x32(tQm + cc, m32);   // the rest never changes
 #pragma unroll
         for (int u = 0; u < 16; ++u)
           qw[cc / 2 + u] = pack_bf16x2(__uint_as_float(m32[2 * u]), __uint_as_float(m32[2 * u + 1]));
@@ -530,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after_sync();
 #pragma unroll
-        for (int cc = 0; cc < D; cc += 64) {
+        for (int cc = 0; cc < R; cc += 64) {
           uint32_t m64[64];
           tmem_ld_x64(tQm + cc, m64);
 #pragma unroll
@@ -538,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             qw[cc / 2 + u] = pack_bf16x2(__uint_as_float(m64[2 * u]), __uint_as_float(m64[2 * u + 1]));
         }
 #pragma unroll
-        for (int cc = 0; cc < D / 2; cc += 32)
+        for (int cc = 0; cc < R / 2; cc += 32)
           tmem_st_x32(tQw + cc, *reinterpret_cast<uint32_t(*)[32]>(&qw[cc]));
         tmem_st_wait();
         tc_fence_before_sync();
@@ -581,16 +586,17 @@ bool make_map(CUtensorMap* m, const void* ptr, int rank, uint64_t cols, uint64_t
          CUDA_SUCCESS;
 }
 
-template <int D, bool kGate>
+template <int D, bool kGate, int R = D>
 cudaError_t launch_tc(const Geom& g, const Inputs& in, const Workspace& ws, int* status,
                       cudaStream_t st) {
-  using Cfg = TcCfg<D>;
+  using Cfg = TcCfg<D, R>;
   CUtensorMap mkr, mng, mv;
+  // ngt_c is read as its first R rows (all D columns)
   if (!make_map(&mkr, ws.kr, 2, D, static_cast<uint64_t>(g.BH) * g.Tp, 1, kC) ||
-      !make_map(&mng, ws.ngt, 2, D, static_cast<uint64_t>(g.nch) * D, 1, D) ||
+      !make_map(&mng, ws.ngt, 2, D, static_cast<uint64_t>(g.nch) * D, 1, R) ||
       !make_map(&mv, in.v, 3, D, g.T, g.BH, kC))
     return cudaErrorInvalidValue;
-  auto kern = attn_tc_kernel<D, kGate>;
+  auto kern = attn_tc_kernel<D, kGate, R>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(Cfg::kSmemBytes));
   if (e != cudaSuccess) return e;
@@ -623,6 +629,11 @@ cudaError_t launch_attn_tc(const Geom& g, const Inputs& in, const Workspace& ws,
                            cudaStream_t st, int* launches) {
   if (launches) *launches = 1;
   if (g.C != kC) return cudaErrorInvalidValue;
+  if (in.wr > 0 && in.wr < g.d) {   // partial PaTH: transitions of rank 64 at d = 128
+    if (g.d != 128 || in.wr != 64) return cudaErrorInvalidValue;
+    return g.gate ? launch_tc<128, true, 64>(g, in, ws, status, st)
+                  : launch_tc<128, false, 64>(g, in, ws, status, st);
+  }
   if (g.d == 128) return g.gate ? launch_tc<128, true>(g, in, ws, status, st)
                                 : launch_tc<128, false>(g, in, ws, status, st);
   if (g.d == 64) return g.gate ? launch_tc<64, true>(g, in, ws, status, st)

@@ -93,6 +93,10 @@ struct Inputs {
   float scale;
   void* out;
   float* lse;
+  // columns of w: 0 = d.  Partial PaTH (bf16) passes its u [B,H,T,r] as w
+  // with wr = r; the preparation reads it with zeros in columns r .. d-1 and
+  // the attention carries only the first r coordinates through transitions.
+  int wr = 0;
 };
 
 // Kernel-family launchers (each returns the first launch error, if any).

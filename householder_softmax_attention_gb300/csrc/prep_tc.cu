@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const uint8_t* q_raw, const float* __restrict__ beta, const float* __restrict__ lam2,
                    __nv_bfloat16* __restrict__ kr, float* __restrict__ ql,
                    __nv_bfloat16* __restrict__ ngt, float* __restrict__ sdt, int* status, int T,
-                   int Np, float sl2) {
+                   int Np, float sl2, int wr) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -145,7 +145,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int bh2 = ch2 / Np, t2 = (ch2 - bh2 * Np) * kC;
       const size_t off = (static_cast<size_t>(bh2) * T + t2) * D * 2;
       const uint32_t bytes = static_cast<uint32_t>(min(kC, T - t2)) * D * 2;
-      bulk_prefetch_l2(w_raw + off, bytes);
+      // w has wr columns (wr = D, or r for partial PaTH)
+      const size_t off_w = (static_cast<size_t>(bh2) * T + t2) * wr * 2;
+      const uint32_t bytes_w = static_cast<uint32_t>(min(kC, T - t2)) * wr * 2;
+      bulk_prefetch_l2(w_raw + off_w, bytes_w);
       bulk_prefetch_l2(k_raw + off, bytes);
       bulk_prefetch_l2(q_raw + off, bytes);
     }
@@ -658,7 +661,11 @@ template <int D, bool kGate>
 cudaError_t launch_one(const Geom& g, const Inputs& in, const Workspace& ws, int* status,
                        cudaStream_t st) {
   CUtensorMap mw, mk, mq;
-  if (!make_input_map(&mw, in.w, D, g.T, g.BH) || !make_input_map(&mk, in.k, D, g.T, g.BH) ||
+  // w may have fewer columns than D (partial PaTH): its boxes then read zeros
+  // past column wr, which makes every transition the identity there
+  const int wr = in.wr > 0 ? in.wr : D;
+  if (wr > D || wr % 64 != 0) return cudaErrorInvalidValue;
+  if (!make_input_map(&mw, in.w, wr, g.T, g.BH) || !make_input_map(&mk, in.k, D, g.T, g.BH) ||
       !make_input_map(&mq, in.q, D, g.T, g.BH))
     return cudaErrorInvalidValue;
   auto kern = prep_tc_kernel<D, kGate>;
@@ -669,7 +676,7 @@ cudaError_t launch_one(const Geom& g, const Inputs& in, const Workspace& ws, int
       mw, mk, mq, static_cast<const uint8_t*>(in.w), static_cast<const uint8_t*>(in.k),
       static_cast<const uint8_t*>(in.q), in.beta, ws.lam2,
       static_cast<__nv_bfloat16*>(ws.kr), ws.ql, static_cast<__nv_bfloat16*>(ws.ngt), ws.sdt,
-      status, g.T, g.Np, in.scale * kLog2e);
+      status, g.T, g.Np, in.scale * kLog2e, wr);
   return cudaGetLastError();
 }
 
