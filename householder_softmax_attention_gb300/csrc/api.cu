@@ -33,8 +33,31 @@ struct DeviceState {
   cudaStream_t copy_in = nullptr, copy_out = nullptr;
 };
 
-// Slices of (b, h) problems the host-buffer entry pipelines its copies over.
-constexpr int kHostSlices = 4;
+// Slices of (b, h) problems the host-buffer entry pipelines its copies over
+// (at most this many).
+constexpr int kHostSlices = 8;
+
+// Heads per slice of the host-buffer entry, in order; returns the count.
+// Fewer than 16 problems: up to four equal slices.  Otherwise a first and a
+// last slice of BH/8 problems around middle slices of about BH/4: the copy
+// of the first slice and the compute and copy-out of the last one are the
+// parts of the call nothing overlaps, so they are kept small, while the
+// middle slices stay large enough to fill the GPU.
+int host_slice_plan(int BH, int* heads) {
+  if (BH < 16) {
+    const int nsl = BH < 4 ? BH : 4, per = (BH + nsl - 1) / nsl;
+    int n = 0;
+    for (int b0 = 0; b0 < BH; b0 += per) heads[n++] = std::min(per, BH - b0);
+    return n;
+  }
+  const int edge = BH / 8, mid = BH - 2 * edge;
+  const int n_mid = std::min(kHostSlices - 2, (mid + BH / 4 - 1) / (BH / 4));
+  int n = 0;
+  heads[n++] = edge;
+  for (int i = 0; i < n_mid; ++i) heads[n++] = mid / n_mid + (i < mid % n_mid ? 1 : 0);
+  heads[n++] = edge;
+  return n;
+}
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
@@ -145,6 +168,23 @@ int check_device(const DeviceState* s) {
     return PATH_ERR_UNSUPPORTED;
   }
   return PATH_OK;
+}
+
+// Prep, then (once `ev_v` has completed: the copy of v) attention, for the
+// host-buffer entry's slices.
+int run_forward_after(const Geom& g, const Inputs& in, char* ws_base, DeviceState* s,
+                      cudaStream_t st, cudaEvent_t ev_v) {
+  Workspace ws;
+  workspace_layout(g, ws_base, &ws);
+  cudaError_t e;
+  if ((e = launch_prep(g, in, ws, s->status, st, nullptr)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(st, ev_v, 0)) != cudaSuccess)
+    return set_cuda_error(e);
+  if (g.bf16)
+    e = launch_attn_tc(g, in, ws, s->status, st, nullptr);
+  else
+    e = launch_attn_f32(g, in, ws, st, nullptr);
+  return e == cudaSuccess ? PATH_OK : set_cuda_error(e);
 }
 
 // Runs prep + attention for device pointers; `ws_base` must hold the layout.
@@ -392,9 +432,13 @@ int path_attn_fwd_host(const void* q, const void* k, const void* v, const void* 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // The (b, h) problems are independent and contiguous in every array: the
   // call runs them in slices, copies of slice i + 1 in and of slice i - 1 out
-  // on two copy streams while slice i computes on `stream`.
-  const int nsl = g.BH < kHostSlices ? g.BH : kHostSlices;
-  const int per = (g.BH + nsl - 1) / nsl;
+  // on two copy streams while slice i computes on `stream`.  Within a slice,
+  // q, k, w, beta (and log f) go first: the preparation starts once they have
+  // landed, while v is still copying.
+  int heads[kHostSlices];
+  const int nsl = host_slice_plan(g.BH, heads);
+  int per = 0;
+  for (int i = 0; i < nsl; ++i) per = std::max(per, heads[i]);
   Geom gs;
   if ((rc = make_geom(1, per, T, d, dtype, logf != nullptr, &gs)) != PATH_OK) return rc;
   const size_t es = dtype == PATH_DTYPE_BF16 ? 2 : 4;
@@ -410,12 +454,13 @@ int path_attn_fwd_host(const void* q, const void* k, const void* v, const void* 
   cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&buf), io_bytes + ws_bytes,
                                           s->pool, st);
   if (e != cudaSuccess) return set_cuda_error(e);
-  cudaEvent_t ev_start = nullptr, ev_in[kHostSlices] = {}, ev_done[kHostSlices] = {},
-              ev_out = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_in[kHostSlices] = {}, ev_qkw[kHostSlices] = {},
+              ev_done[kHostSlices] = {}, ev_out = nullptr;
   auto mk = [](cudaEvent_t* ev) { return cudaEventCreateWithFlags(ev, cudaEventDisableTiming); };
   bool ok = (e = mk(&ev_start)) == cudaSuccess && (e = mk(&ev_out)) == cudaSuccess;
   for (int i = 0; ok && i < nsl; ++i)
-    ok = (e = mk(&ev_in[i])) == cudaSuccess && (e = mk(&ev_done[i])) == cudaSuccess;
+    ok = (e = mk(&ev_in[i])) == cudaSuccess && (e = mk(&ev_qkw[i])) == cudaSuccess &&
+         (e = mk(&ev_done[i])) == cudaSuccess;
   // the buffer exists on `stream` first; both copy streams start after that
   if (ok) ok = (e = cudaEventRecord(ev_start, st)) == cudaSuccess &&
                (e = cudaStreamWaitEvent(s->copy_in, ev_start, 0)) == cudaSuccess &&
@@ -427,18 +472,18 @@ int path_attn_fwd_host(const void* q, const void* k, const void* v, const void* 
     return cudaMemcpyAsync(dst, buf + o, n, cudaMemcpyDeviceToHost, s->copy_out);
   };
   auto hp = [](const void* p, size_t o) { return static_cast<const char*>(p) + o; };
-  for (int i = 0; ok && i < nsl; ++i) {
-    const int bh0 = i * per, nbh = (bh0 + per <= g.BH ? per : g.BH - bh0);
-    if (nbh <= 0) break;
+  for (int i = 0, bh0 = 0; ok && i < nsl; bh0 += heads[i], ++i) {
+    const int nbh = heads[i];
     const size_t x0 = xrow * bh0, xn = xrow * nbh, b0 = brow * bh0, bn = brow * nbh;
     ok = (e = h2d(oq + x0, hp(q, x0), xn)) == cudaSuccess &&
          (e = h2d(ok_ + x0, hp(k, x0), xn)) == cudaSuccess &&
          (e = h2d(ow + x0, hp(w, x0), xn)) == cudaSuccess &&
          (e = h2d(ob + b0, hp(beta, b0), bn)) == cudaSuccess &&
          (!logf || (e = h2d(olf + b0, hp(logf, b0), bn)) == cudaSuccess) &&
+         (e = cudaEventRecord(ev_qkw[i], s->copy_in)) == cudaSuccess &&
          (e = h2d(ov + x0, hp(v, x0), xn)) == cudaSuccess &&
          (e = cudaEventRecord(ev_in[i], s->copy_in)) == cudaSuccess &&
-         (e = cudaStreamWaitEvent(st, ev_in[i], 0)) == cudaSuccess;
+         (e = cudaStreamWaitEvent(st, ev_qkw[i], 0)) == cudaSuccess;
     if (!ok) break;
     Geom gi = gs;
     if (nbh != per && (rc = make_geom(1, nbh, T, d, dtype, logf != nullptr, &gi)) != PATH_OK) break;
@@ -446,7 +491,7 @@ int path_attn_fwd_host(const void* q, const void* k, const void* v, const void* 
               reinterpret_cast<float*>(buf + ob + b0),
               logf ? reinterpret_cast<float*>(buf + olf + b0) : nullptr, scale,
               buf + oo + x0, lse ? reinterpret_cast<float*>(buf + ol + b0) : nullptr};
-    if ((rc = run_forward(gi, in, buf + io_bytes, s, st)) != PATH_OK) break;
+    if ((rc = run_forward_after(gi, in, buf + io_bytes, s, st, ev_in[i])) != PATH_OK) break;
     ok = (e = cudaEventRecord(ev_done[i], st)) == cudaSuccess &&
          (e = cudaStreamWaitEvent(s->copy_out, ev_done[i], 0)) == cudaSuccess &&
          (e = d2h(static_cast<char*>(out) + x0, oo + x0, xn)) == cudaSuccess &&
@@ -468,6 +513,7 @@ int path_attn_fwd_host(const void* q, const void* k, const void* v, const void* 
     if (ev) cudaEventDestroy(ev);
   for (int i = 0; i < kHostSlices; ++i) {
     if (ev_in[i]) cudaEventDestroy(ev_in[i]);
+    if (ev_qkw[i]) cudaEventDestroy(ev_qkw[i]);
     if (ev_done[i]) cudaEventDestroy(ev_done[i]);
   }
   return rc;

@@ -318,10 +318,12 @@ def test_host_buffer_entry_matches_device_entry():
 
 
 @pytest.mark.parametrize("B,H,dtype,pinned", [(1, 5, "bf16", True), (2, 3, "bf16", False),
-                                               (3, 3, "f32", True)])
+                                               (3, 3, "f32", True), (2, 9, "bf16", True),
+                                               (1, 17, "bf16", False), (2, 8, "f32", True)])
 def test_host_buffer_entry_slices_match_device_entry(B, H, dtype, pinned):
     """The host entry runs the (b, h) problems in slices with overlapped
-    copies; ragged slice counts and pageable buffers give the same bits."""
+    copies (equal slices below 16 problems, small first and last slices from
+    16 on); ragged slice counts and pageable buffers give the same bits."""
     wl = Workload("host_sl", B, H, 300, 64, dtype, seed=9)
     x = make_inputs(wl)
     o1, l1 = _run(x)
