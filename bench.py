@@ -13,7 +13,8 @@ one step is the forward and the backward of workload <name> (the pages time
 PaTH forward + backward together) and the line reports ms per step;
 ``--workload bwd_grid`` times forward + backward on every B x T x d row of
 the pages' latency table; ``--workload partial_<name>`` times partial PaTH
-(r = d/2) beside full PaTH.  The
+(r = d/2) beside full PaTH; ``--workload forms_<name>`` times the dense and
+the low-rank transition forms (d = 64).  The
 JSON line reports issued TFLOP/s (formulas in ``step_flops``), ms per step,
 the roofline of the attention kernel (against the measured bf16 burst peak,
 the stated spec peak and, for a second-long back-to-back loop, the measured
@@ -818,6 +819,39 @@ def run_partial(args, wl):
     return 0
 
 
+def run_transition_forms(args, wl):
+    """The dense and the low-rank transition forms (d = 64) on the same inputs,
+    timed in one process; value = low-rank ms per step."""
+    import torch
+
+    import householder_softmax_attention_gb300 as pa
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    pa.load_library()
+    run = ForwardRun(pa, wl, dev, torch.cuda.current_stream(dev))
+    peak, _, _ = _peaks()
+    res = {}
+    try:
+        for name, form in (("dense", 0), ("low_rank", 1), ("dense_again", 0)):
+            pa.path_attn_set_transition_form(form)
+            res[name] = run.summary(run.timed(args.steps, args.warmup), peak)
+    finally:
+        pa.path_attn_set_transition_form(0)
+    N, C, d = -(-wl.T // 128), 128, wl.d
+    X = (N - 1) * (N - 2) // 2
+    line = {"metric": f"transition forms, PaTH fwd ms, {wl.name}",
+            "value": res["low_rank"]["ms_per_step"], "unit": "ms", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": False,
+            "dtype": wl.dtype, "data": "synthetic", "config": {"workload": "forms_" + wl.name},
+            "dense": res["dense"], "low_rank": res["low_rank"], "dense_again": res["dense_again"],
+            "transition_flops_per_head": {"dense": 2 * C * d * d * X,
+                                          "low_rank": 2 * (2 * C * C * d) * X},
+            "attn_ratio_low_rank_over_dense": res["low_rank"]["attn_ms"] / res["dense"]["attn_ms"]}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 # The pages' latency grid (rebuttal, "Efficiency Evaluation": PaTH Triton
 # forward + backward, hardware unstated), B x T x d with H = 16 at d = 128 and
 # H = 32 at d = 64; plain PaTH (the table's PaTH column).
@@ -1203,6 +1237,12 @@ def main(argv=None):
                               "partial PaTH is timed against full PaTH on the GPU only"}))
             return 0
         return run_partial(args, WORKLOADS[args.workload[8:]])
+    if args.workload.startswith("forms_") and args.workload[6:] in WORKLOADS:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the transition forms are compared on the GPU only"}))
+            return 0
+        return run_transition_forms(args, WORKLOADS[args.workload[6:]])
     if args.workload == "bwd_grid":
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable":

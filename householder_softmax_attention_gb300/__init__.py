@@ -26,7 +26,8 @@ __all__ = [
     "path_attn_decode_step", "DecodeCache", "path_attn_fwd_partial", "path_producer_fwd",
     "path_attn_bwd", "path_attn_bwd_workspace_bytes", "path_attn_bwd_launches_per_call",
     "path_attn_debug_factors", "path_attn_device_status", "path_attn_workspace_bytes",
-    "path_attn_chunk_size", "path_attn_launches_per_call", "path_attn_timing_enable",
+    "path_attn_chunk_size", "path_attn_launches_per_call", "path_attn_set_transition_form",
+    "path_attn_timing_enable",
     "path_attn_timing_read", "path_attn_bwd_timing_read", "BWD_PHASES", "path_attn_version",
     "path_attn_status_string",
     "LIBRARY_PATH", "HEADER_PATH", "PATH_DTYPE_F32", "PATH_DTYPE_BF16",
@@ -94,6 +95,8 @@ def load_library(path: str | None = None):
         lib.path_attn_bwd_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double),
                                                   ctypes.POINTER(ctypes.c_long)]
         lib.path_attn_bwd_timing_read.restype = i
+        lib.path_attn_set_transition_form.argtypes = [i]
+        lib.path_attn_set_transition_form.restype = i
         lib.path_attn_launches_per_call.argtypes = [i, i, i]
         lib.path_attn_launches_per_call.restype = i
         lib.path_attn_bwd_launches_per_call.argtypes = [i, i, i, i]
@@ -537,6 +540,13 @@ def path_attn_launches_per_call(d, dtype_code, with_gate=False) -> int:
     if n < 0:
         raise PathAttnError(n, "path_attn_launches_per_call")
     return n
+
+
+def path_attn_set_transition_form(form: int = 0):
+    """0: dense transitions (default); 1: the low-rank form q <- q - (q W^T)(U W)
+    for bf16 problems at d = 64 (others keep the dense form)."""
+    _check(load_library().path_attn_set_transition_form(int(form)),
+           "path_attn_set_transition_form")
 
 
 def path_attn_timing_enable(enable: bool = True):

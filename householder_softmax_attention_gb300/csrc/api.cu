@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <climits>
 #include <cstdio>
 #include <cstdint>
@@ -32,6 +33,15 @@ struct DeviceState {
   // copy streams of the host-buffer entry (non-blocking, created with the state)
   cudaStream_t copy_in = nullptr, copy_out = nullptr;
 };
+
+// Form of the transition in the bf16 d = 64 forward (path_attn_set_transition_form):
+// 0 dense (q <- q + q ngt^T), 1 low-rank (q <- q + (q W^T)(-(U W))).
+std::atomic<int> g_transition_form{0};
+
+// The low-rank form applies to bf16 problems at d = 64 when selected.
+void apply_transition_form(Geom* g) {
+  g->lowrank = g_transition_form.load() == 1 && g->bf16 && g->d == 64;
+}
 
 // Slices of (b, h) problems the host-buffer entry pipelines its copies over
 // (at most this many).
@@ -287,6 +297,7 @@ int path_attn_fwd(const void* q, const void* k, const void* v, const void* w,
   Geom g;
   int rc = make_geom(B, H, T, d, dtype, logf != nullptr, &g);
   if (rc != PATH_OK) return rc;
+  apply_transition_form(&g);
   DeviceState* s = nullptr;
   if ((rc = device_state(&s)) != PATH_OK) return rc;
   if ((rc = check_device(s)) != PATH_OK) return rc;
@@ -300,6 +311,12 @@ int path_attn_fwd(const void* q, const void* k, const void* v, const void* w,
   e = cudaFreeAsync(ws, st);
   if (rc == PATH_OK && e != cudaSuccess) rc = set_cuda_error(e);
   return rc;
+}
+
+int path_attn_set_transition_form(int form) {
+  if (form != 0 && form != 1) return PATH_ERR_INVALID_ARG;
+  g_transition_form = form;
+  return PATH_OK;
 }
 
 int path_attn_bwd_workspace_bytes(int B, int H, int T, int d, int dtype, int with_gate,
@@ -441,6 +458,7 @@ int path_attn_fwd_host(const void* q, const void* k, const void* v, const void* 
   for (int i = 0; i < nsl; ++i) per = std::max(per, heads[i]);
   Geom gs;
   if ((rc = make_geom(1, per, T, d, dtype, logf != nullptr, &gs)) != PATH_OK) return rc;
+  apply_transition_form(&gs);
   const size_t es = dtype == PATH_DTYPE_BF16 ? 2 : 4;
   const size_t xrow = static_cast<size_t>(T) * d * es, brow = static_cast<size_t>(T) * 4;
   const size_t nx = xrow * g.BH, nb = brow * g.BH;
@@ -487,6 +505,7 @@ int path_attn_fwd_host(const void* q, const void* k, const void* v, const void* 
     if (!ok) break;
     Geom gi = gs;
     if (nbh != per && (rc = make_geom(1, nbh, T, d, dtype, logf != nullptr, &gi)) != PATH_OK) break;
+    apply_transition_form(&gi);
     Inputs in{buf + oq + x0, buf + ok_ + x0, buf + ov + x0, buf + ow + x0,
               reinterpret_cast<float*>(buf + ob + b0),
               logf ? reinterpret_cast<float*>(buf + olf + b0) : nullptr, scale,

@@ -51,25 +51,34 @@ static_assert(128 * (kRegsLow + kRegsSoftmax + kRegsQuery) <= kThreads * 168, "r
 // D: head dimension; R: the coordinates the transitions act on (R = D for
 // PaTH; R < D for partial PaTH, whose running query changes only in its
 // first R coordinates and whose ngt_c vanishes outside its first R rows).
-template <int D, int R>
+// kLR: the low-rank form of the transition (d = 64 only), see below.
+template <int D, int R, bool kLR = false>
 struct TcCfg {
   static_assert(R <= D && R % 64 == 0, "transition rank");
+  static_assert(!kLR || (D == 64 && R == 64), "the low-rank form is built at d = 64");
   static constexpr int kHalves = D / 64;           // 64-column (128-byte) halves
   // One B tile per step stacks kr_c (kC rows) over the first R rows of ngt_c,
   // so that S = Qw kr^T and the transition Qm += Qw ngt^T are a single MMA
   // of width N = kC + R; tcgen05.mma pays a fixed cost per instruction below
-  // N = 256.
-  static constexpr int kKgRows = kC + R;
+  // N = 256.  Low-rank form: kr_c over W_c ([S | Y] = Qw [kr_c ; W_c]^T),
+  // and -(U W)_c beside them, the B operand of Qm += Y (-(U W)_c).
+  static constexpr int kKgRows = kLR ? 2 * kC : kC + R;
   static constexpr uint32_t kKgHalf = kKgRows * 128;  // one 64-column half
   static constexpr uint32_t kKgBytes = kHalves * kKgHalf;
+  static constexpr uint32_t kUwBytes = kLR ? kC * D * 2 : 0;
+  static constexpr uint32_t kStageBytes = kKgBytes + kUwBytes;
   static constexpr uint32_t kVBytes = kC * D * 2;
+  // low-rank form: the bf16 copy of Y, A operand of the second product
+  // (K-major, two 64-column halves)
+  static constexpr uint32_t kYwBytes = kLR ? kC * kC * 2 : 0;
   static constexpr uint32_t kColS = 0;             // S and Qm are adjacent: one
-  static constexpr uint32_t kColQm = 128;          // accumulator of width kC + R
-  static constexpr uint32_t kColO = 128 + R;
-  static constexpr uint32_t kColQw = 128 + R + D;
-  static constexpr uint32_t kColP = 128 + R + D + D / 2;
+  static constexpr uint32_t kColY = 128;           // (low-rank: S and Y)
+  static constexpr uint32_t kColQm = kLR ? 256 : 128;  // accumulator of width kC + R
+  static constexpr uint32_t kColO = kColQm + R;
+  static constexpr uint32_t kColQw = kColO + D;
+  static constexpr uint32_t kColP = kColQw + D / 2;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr size_t kTileBytes = 2 * (kKgBytes + kVBytes);
+  static constexpr size_t kTileBytes = 2 * (kStageBytes + kVBytes) + kYwBytes;
   static constexpr size_t kSmemBytes = kTileBytes + 1024 /*align*/ + 1280 /*barriers, gate*/;
   static_assert(kColP + 64 <= kTmemCols, "TMEM budget");
 };
@@ -86,6 +95,7 @@ constexpr bool kSplitFirst = D == 64 || kGate;
 struct Bars {
   uint64_t kg_full[2], kg_empty[2], v_full[2], v_empty[2];
   uint64_t sq_ready, p_full, qk_done, pv_done, final_done;
+  uint64_t yw_ready, q_done;  // low-rank form: Y converted; Qm += Y (-UW) done
   uint64_t gate_full[2], gate_empty[2];  // FoX: the gate ring below
   uint32_t tmem_base;
   int abort_flag;
@@ -160,20 +170,22 @@ __device__ __forceinline__ void teardown(int warp, uint32_t tb, uint32_t ncols) 
   }
 }
 
-template <int D, bool kGate, int R>
+template <int D, bool kGate, int R, bool kLR>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap map_kr,
                    const __grid_constant__ CUtensorMap map_ng,
-                   const __grid_constant__ CUtensorMap map_v, const float* __restrict__ ql,
+                   const __grid_constant__ CUtensorMap map_v,
+                   const __grid_constant__ CUtensorMap map_uw, const float* __restrict__ ql,
                    const float* __restrict__ sdt, const float* __restrict__ lam2,
                    __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
                    int* __restrict__ status, int T, int Np, int BH, float sl2) {
-  using Cfg = TcCfg<D, R>;
+  using Cfg = TcCfg<D, R, kLR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* s_kg = base;                                   // [2][kKgBytes]
-  uint8_t* s_v = base + 2 * Cfg::kKgBytes;                // [2][kVBytes]
+  uint8_t* s_kg = base;                                   // [2][kStageBytes]
+  uint8_t* s_v = base + 2 * Cfg::kStageBytes;             // [2][kVBytes]
+  uint8_t* s_yw = s_v + 2 * Cfg::kVBytes;                 // low-rank: [kYwBytes]
   Bars* bars = reinterpret_cast<Bars*>(base + Cfg::kTileBytes);
   volatile int* abort_flag = &bars->abort_flag;
 
@@ -208,6 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->qk_done, 1);
     mbar_init(&bars->pv_done, 1);
     mbar_init(&bars->final_done, 2);  // one commit from each MMA-issuing thread
+    mbar_init(&bars->yw_ready, 4);    // low-rank: the 4 running-query warps
+    mbar_init(&bars->q_done, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->gate_full[s], 1);
       mbar_init(&bars->gate_empty[s], 4);  // the softmax warps, once read
@@ -219,6 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_map(&map_kr);
     tma_prefetch_map(&map_ng);
     tma_prefetch_map(&map_v);
+    if (kLR) tma_prefetch_map(&map_uw);
   }
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, Cfg::kTmemCols);
@@ -246,12 +261,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int c = b - 1 - n;
           if (n >= 2) ok = mbar_wait(&bars->kg_empty[s], ((n >> 1) - 1) & 1, abort_flag, LIM);
           if (!ok) break;
-          mbar_arrive_expect_tx(&bars->kg_full[s], Cfg::kKgBytes);
+          mbar_arrive_expect_tx(&bars->kg_full[s], Cfg::kStageBytes);
+          uint8_t* stage = s_kg + s * Cfg::kStageBytes;
           for (int h = 0; h < Cfg::kHalves; ++h) {
-            uint8_t* dst = s_kg + s * Cfg::kKgBytes + h * Cfg::kKgHalf;
+            uint8_t* dst = stage + h * Cfg::kKgHalf;
             tma_load_2d(dst, &map_kr, h * 64, bh * Tp + c * kC, &bars->kg_full[s]);
-            tma_load_2d(dst + kC * 128, &map_ng, h * 64, (bh * Np + c) * D, &bars->kg_full[s]);
+            if constexpr (kLR)   // W_c, the input directions (rows past T read as zero)
+              tma_load_3d(dst + kC * 128, &map_ng, h * 64, c * kC, bh, &bars->kg_full[s]);
+            else
+              tma_load_2d(dst + kC * 128, &map_ng, h * 64, (bh * Np + c) * D, &bars->kg_full[s]);
           }
+          if constexpr (kLR)     // -(U W)_c, kC rows of D
+            for (int h = 0; h < Cfg::kHalves; ++h)
+              tma_load_2d(stage + Cfg::kKgBytes + h * (kC * 128), &map_uw, h * 64,
+                          (bh * Np + c) * kC, &bars->kg_full[s]);
           last_kg[s] = (n >> 1) & 1;
           if (kGate) {
             // the key chunk's gate prefix (512 bytes) for the softmax warps
@@ -299,7 +322,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) ok = mbar_spin(&bars->sq_ready, n & 1, abort_flag, LIM);
         if (!ok) break;
         tc_fence_after_sync();
-        const uint32_t kg_a = smem_addr(s_kg + s * Cfg::kKgBytes);
+        const uint32_t kg_a = smem_addr(s_kg + s * Cfg::kStageBytes);
+        if constexpr (kLR) {
+          // low-rank form: [S | Y] = Qw [kr_c ; W_c]^T from zero (width 2 kC;
+          // S alone for the last chunk), then, once the running-query warps
+          // have turned Y into bf16 in shared memory, Qm += Y (-(U W)_c)
+          constexpr uint32_t idSY = idesc_bf16_f32(128, 2 * kC, false, false);
+          constexpr uint32_t idQ2 = idesc_bf16_f32(128, D, false, true);
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k >> 2) * Cfg::kKgHalf + (k & 3) * 32;
+            mma_bf16_ts(tS, tQw + k * 8, sdesc_sw128(kg_a + off, 16, 1024), c > 0 ? idSY : idS,
+                        k > 0);
+          }
+          mma_commit(&bars->qk_done);
+          if (c > 0) {
+            ok = mbar_spin(&bars->yw_ready, n & 1, abort_flag, LIM);
+            if (!ok) break;
+            tc_fence_after_sync();
+            const uint32_t yw = smem_addr(s_yw), uw = kg_a + Cfg::kKgBytes;
+#pragma unroll
+            for (int k = 0; k < kC / 16; ++k)
+              mma_bf16_ss(tb + Cfg::kColQm,
+                          sdesc_sw128(yw + (k >> 2) * (kC * 128) + (k & 3) * 32, 16, 1024),
+                          sdesc_sw128(uw + k * 2048, kC * 128, 1024), idQ2, 1);
+            mma_commit(&bars->q_done);
+          }
+          mma_commit(&bars->kg_empty[s]);
+          continue;
+        }
         // the logits and the backward crossing of chunk c in one MMA of width
         // kC + R; the last chunk needs no crossing.  S starts from zero:
         // either the first k-step writes it alone (the crossing part
@@ -534,6 +585,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(&bars->qk_done, n & 1, abort_flag, LIM);
         if (!ok) break;
         tc_fence_after_sync();
+        if constexpr (kLR) {
+          // Y (kC fp32 columns of this row) -> bf16 into the K-major,
+          // 128-byte-swizzled A tile of the second product, 64 columns at a
+          // time; then wait for Qm += Y (-UW) before refreshing Qw below
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t y64[64];
+            tmem_ld_x64(tb + lb + Cfg::kColY + 64 * hh, y64);
+            uint8_t* rowp = s_yw + hh * (kC * 128) + r * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(y64[8 * j]), __uint_as_float(y64[8 * j + 1]));
+              v.y = pack_bf16x2(__uint_as_float(y64[8 * j + 2]), __uint_as_float(y64[8 * j + 3]));
+              v.z = pack_bf16x2(__uint_as_float(y64[8 * j + 4]), __uint_as_float(y64[8 * j + 5]));
+              v.w = pack_bf16x2(__uint_as_float(y64[8 * j + 6]), __uint_as_float(y64[8 * j + 7]));
+              *reinterpret_cast<uint4*>(rowp + ((j ^ (r & 7)) << 4)) = v;
+            }
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          tc_fence_before_sync();
+          warp_arrive(&bars->yw_ready);
+          ok = mbar_wait(&bars->q_done, n & 1, abort_flag, LIM);
+          if (!ok) break;
+          tc_fence_after_sync();
+        }
 #pragma unroll
         for (int cc = 0; cc < R; cc += 64) {
           uint32_t m64[64];
@@ -586,22 +663,32 @@ bool make_map(CUtensorMap* m, const void* ptr, int rank, uint64_t cols, uint64_t
          CUDA_SUCCESS;
 }
 
-template <int D, bool kGate, int R = D>
+template <int D, bool kGate, int R = D, bool kLR = false>
 cudaError_t launch_tc(const Geom& g, const Inputs& in, const Workspace& ws, int* status,
                       cudaStream_t st) {
-  using Cfg = TcCfg<D, R>;
-  CUtensorMap mkr, mng, mv;
-  // ngt_c is read as its first R rows (all D columns)
+  using Cfg = TcCfg<D, R, kLR>;
+  CUtensorMap mkr, mng, mv, muw;
   if (!make_map(&mkr, ws.kr, 2, D, static_cast<uint64_t>(g.BH) * g.Tp, 1, kC) ||
-      !make_map(&mng, ws.ngt, 2, D, static_cast<uint64_t>(g.nch) * D, 1, R) ||
       !make_map(&mv, in.v, 3, D, g.T, g.BH, kC))
     return cudaErrorInvalidValue;
-  auto kern = attn_tc_kernel<D, kGate, R>;
+  if constexpr (kLR) {
+    // the input directions W ([BH][T][D], rows past T read as zero) and
+    // -(U W) per chunk ([nch * kC][D]) from the preparation
+    if (!ws.uwn || !make_map(&mng, in.w, 3, D, g.T, g.BH, kC) ||
+        !make_map(&muw, ws.uwn, 2, D, static_cast<uint64_t>(g.nch) * kC, 1, kC))
+      return cudaErrorInvalidValue;
+  } else {
+    // ngt_c is read as its first R rows (all D columns); no fourth operand
+    if (!make_map(&mng, ws.ngt, 2, D, static_cast<uint64_t>(g.nch) * D, 1, R))
+      return cudaErrorInvalidValue;
+    muw = mv;
+  }
+  auto kern = attn_tc_kernel<D, kGate, R, kLR>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(Cfg::kSmemBytes));
   if (e != cudaSuccess) return e;
   kern<<<g.nch, kThreads, Cfg::kSmemBytes, st>>>(
-      mkr, mng, mv, ws.ql, ws.sdt, kGate ? ws.lam2 : nullptr,
+      mkr, mng, mv, muw, ws.ql, ws.sdt, kGate ? ws.lam2 : nullptr,
       static_cast<__nv_bfloat16*>(in.out), in.lse, status, g.T, g.Np, g.BH, in.scale * kLog2e);
   return cudaGetLastError();
 }
@@ -633,6 +720,11 @@ cudaError_t launch_attn_tc(const Geom& g, const Inputs& in, const Workspace& ws,
     if (g.d != 128 || in.wr != 64) return cudaErrorInvalidValue;
     return g.gate ? launch_tc<128, true, 64>(g, in, ws, status, st)
                   : launch_tc<128, false, 64>(g, in, ws, status, st);
+  }
+  if (g.lowrank) {   // the low-rank transition form, d = 64 only
+    if (g.d != 64 || !ws.uwn) return cudaErrorInvalidValue;
+    return g.gate ? launch_tc<64, true, 64, true>(g, in, ws, status, st)
+                  : launch_tc<64, false, 64, true>(g, in, ws, status, st);
   }
   if (g.d == 128) return g.gate ? launch_tc<128, true>(g, in, ws, status, st)
                                 : launch_tc<128, false>(g, in, ws, status, st);

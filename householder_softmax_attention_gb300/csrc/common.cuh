@@ -29,6 +29,9 @@ struct Geom {
   int nch;      // BH * Np
   bool bf16;    // element type of q, k, v, w, out (else fp32)
   bool gate;    // PaTH-FoX gate present
+  // the low-rank transition form (bf16, d = 64): crossing chunk c as
+  // q <- q + (q W_c^T)(-(U W)_c) instead of q <- q + q ngt_c^T
+  bool lowrank = false;
 };
 
 // Workspace: every region 256-byte aligned.  Per chunk ch = bh * Np + n:
@@ -37,6 +40,7 @@ struct Geom {
 //   ngt  [ch][d][d]   elem  -(W^T U W)^T, so q_next = q + q ngt^T
 //   sdt  [ch][C][C]   f32   intra-chunk log2-domain logits, [j][i], -inf for j > i
 //   lam2 [bh][Tp]     f32   log2(e) * inclusive cumsum of log f (gate only)
+//   uwn  [ch][C][d]   elem  -(U W), the low-rank transition form only
 // and, for fp32 inputs only, the scratch of the SIMT preparation kernels:
 //   lmat [ch][C][C] f32   strictLower(diag(beta) W W^T), then U
 //   awk  [ch][C][C] f32   strictLower(W K^T)
@@ -50,6 +54,7 @@ struct Workspace {
   void* ngt;
   float* sdt;
   float* lam2;
+  void* uwn;
   float *lmat, *awk, *aqw, *aqk, *tk, *uw;
 };
 
@@ -72,6 +77,7 @@ inline size_t workspace_layout(const Geom& g, char* base, Workspace* ws) {
   w.ngt = take(nch * d * d * es);
   w.sdt = reinterpret_cast<float*>(take(nch * C * C * 4));
   w.lam2 = g.gate ? reinterpret_cast<float*>(take(static_cast<size_t>(g.BH) * g.Tp * 4)) : nullptr;
+  w.uwn = g.lowrank ? take(nch * C * d * es) : nullptr;
   if (g.bf16) {  // the fused tensor-core preparation keeps its intermediates on chip
     w.lmat = w.awk = w.aqw = w.aqk = w.tk = w.uw = nullptr;
     if (ws) *ws = w;

@@ -90,8 +90,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap map_q, const uint8_t* w_raw, const uint8_t* k_raw,
                    const uint8_t* q_raw, const float* __restrict__ beta, const float* __restrict__ lam2,
                    __nv_bfloat16* __restrict__ kr, float* __restrict__ ql,
-                   __nv_bfloat16* __restrict__ ngt, float* __restrict__ sdt, int* status, int T,
-                   int Np, float sl2, int wr) {
+                   __nv_bfloat16* __restrict__ ngt, float* __restrict__ sdt,
+                   __nv_bfloat16* __restrict__ uwn, int* status, int T, int Np, float sl2,
+                   int wr) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -436,6 +437,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = 0; u < 8; ++u) x[u] = __uint_as_float(v[g8 * 8 + u]);
         put_hilo8(hi + halfc * kTile, lo + halfc * kTile, row, (cc >> 3) + g8, x);
       }
+      if (uwn != nullptr && halfc == 1) {
+        // the low-rank transition form reads -(U W) as a bf16 operand
+        uint32_t pk[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          pk[u] = pack_bf16x2(-__uint_as_float(v[2 * u]), -__uint_as_float(v[2 * u + 1]));
+        uint4* dst = reinterpret_cast<uint4*>(uwn + (static_cast<size_t>(ch) * kC + row) * D + cc);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+      }
     }
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -676,7 +687,7 @@ cudaError_t launch_one(const Geom& g, const Inputs& in, const Workspace& ws, int
       mw, mk, mq, static_cast<const uint8_t*>(in.w), static_cast<const uint8_t*>(in.k),
       static_cast<const uint8_t*>(in.q), in.beta, ws.lam2,
       static_cast<__nv_bfloat16*>(ws.kr), ws.ql, static_cast<__nv_bfloat16*>(ws.ngt), ws.sdt,
-      status, g.T, g.Np, in.scale * kLog2e, wr);
+      static_cast<__nv_bfloat16*>(ws.uwn), status, g.T, g.Np, in.scale * kLog2e, wr);
   return cudaGetLastError();
 }
 

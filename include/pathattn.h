@@ -327,6 +327,27 @@ int path_attn_debug_factors(const void* q, const void* k, const void* w, const f
 int path_attn_debug_wait_timeout(unsigned long long limit_ns, void* stream);
 
 /*
+ * path_attn_set_transition_form -- how the bf16 forward at d = 64 carries
+ * the running query across a key chunk ("PaTH Attention ..." slides, frames
+ * "A triangular representation makes paths computable" and "A right-to-left
+ * scan accumulates cross-block paths": crossing chunk c multiplies the query
+ * by I - W_c^T U_c W_c).  A library switch for measuring the two forms; they
+ * compute the same values up to rounding.
+ *   form 0 (default)  dense: q <- q + q ngt_c^T with the d x d matrix
+ *                     ngt_c = -(W_c^T U_c W_c)^T from the preparation, fused
+ *                     with the logits into one MMA of width C + d.
+ *   form 1            low-rank, as the slides write it: q <- q - (q W_c^T)(U_c W_c):
+ *                     [S | Y] = Qw [kr_c ; W_c]^T in one MMA of width 2C, Y
+ *                     rounded to bf16 in shared memory, then Qm += Y (-(U W)_c)
+ *                     (K = C); the preparation also stores -(U W)_c in bf16.
+ * Other dtypes, d = 128 (where the low-rank form's TMEM accumulators, S, Y,
+ * Qm, O, Qw and P, would need 704 of the 512 columns), partial PaTH, prefill
+ * and path_attn_fwd_noalloc always use the dense form.  Process-wide; returns
+ * PATH_ERR_INVALID_ARG for any other value.
+ */
+int path_attn_set_transition_form(int form);
+
+/*
  * path_attn_fwd_noalloc -- path_attn_fwd for callers that cannot allocate
  * device memory.  The paper has no counterpart; this is a library interface.
  *

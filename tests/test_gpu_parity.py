@@ -343,3 +343,47 @@ def test_lse_optional_and_no_status_error():
     torch.cuda.synchronize()
     assert l2 is None and torch.equal(o1, o2)
     assert pa.path_attn_device_status(0) == 0
+
+
+# ------------------------------------------------------------ low-rank transition form
+@pytest.fixture
+def _low_rank_form():
+    """Selects the low-rank transition form (bf16, d = 64) for one test."""
+    pa.path_attn_set_transition_form(1)
+    yield
+    pa.path_attn_set_transition_form(0)
+
+
+@pytest.mark.parametrize("T,fox,rng", [(1, False, None), (200, False, None), (1000, True, None),
+                                       (700, False, (1.98, 2.0)), (520, True, (0.0, 0.05))])
+def test_low_rank_form_against_oracle(_low_rank_form, T, fox, rng):
+    """Crossing chunk c as q <- q - (q W_c^T)(U_c W_c) ("A right-to-left scan
+    accumulates cross-block paths"), every output against the oracle."""
+    _full_case(Workload("lowrank", 1, 2, T, 64, "bf16", fox=fox, beta_range=rng, seed=61 + T))
+
+
+@pytest.mark.parametrize("name,kw", [("t16k_d64", {}), ("t2k_d64", {}),
+                                     ("t16k_d64", {"beta_range": (1.98, 2.0)}),
+                                     ("t16k_d64", {"fox": True})])
+def test_low_rank_form_full_size_sampled(_low_rank_form, name, kw):
+    wl = WORKLOADS[name]
+    if kw:
+        wl = wl.with_(name=f"{name}_lowrank_{'_'.join(kw)}", seed=63, **kw)
+    _sampled_case(wl, n_heads=2, n_rows=12)
+
+
+def test_low_rank_form_host_entry_and_other_shapes(_low_rank_form):
+    """The host-buffer entry runs the same form (same bits as the device
+    entry); d = 128 keeps the dense form (same bits as with the switch off)."""
+    wl = Workload("lowrank_host", 2, 9, 300, 64, "bf16", seed=65)
+    x = make_inputs(wl)
+    o1, l1 = _run(x)
+    o2, l2 = pa.path_attn_fwd_host(x["q"], x["k"], x["v"], x["w"], x["beta"], x["logf"],
+                                   x["scale"])
+    assert torch.equal(o1.cpu(), o2) and torch.equal(l1.cpu(), l2)
+    wl = Workload("lowrank_d128", 1, 2, 300, 128, "bf16", seed=66)
+    x = make_inputs(wl)
+    o1, l1 = _run(x)
+    pa.path_attn_set_transition_form(0)
+    o2, l2 = _run(x)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
