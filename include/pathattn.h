@@ -340,8 +340,8 @@ int path_attn_debug_wait_timeout(unsigned long long limit_ns, void* stream);
  *                     [S | Y] = Qw [kr_c ; W_c]^T in one MMA of width 2C, Y
  *                     rounded to bf16 in shared memory, then Qm += Y (-(U W)_c)
  *                     (K = C); the preparation also stores -(U W)_c in bf16.
- * Other dtypes, d = 128 (where the low-rank form's TMEM accumulators, S, Y,
- * Qm, O, Qw and P, would need 704 of the 512 columns), partial PaTH, prefill
+ * Other dtypes, d = 128 (where the low-rank form's tensor-memory operands, S,
+ * Y, Qm, O, Qw and P, would need 640 of the 512 columns), partial PaTH, prefill
  * and path_attn_fwd_noalloc always use the dense form.  Process-wide; returns
  * PATH_ERR_INVALID_ARG for any other value.
  */
