@@ -969,13 +969,27 @@ def run_reference(args, wl, flops):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": est * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "T": wl.T, "d": wl.d},
+        "config": _config(wl, world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def _config(wl, world):
+    """The workload description both arms print (the reference arm's line
+    carries the same config)."""
+    es = 2 if wl.dtype == "bf16" else 4
+    C = 128 if wl.dtype == "bf16" else 64
+    BH, N = wl.B * wl.H, -(-wl.T // C)
+    in_bytes = 4 * BH * wl.T * wl.d * es + BH * wl.T * 4 * (2 if wl.fox else 1)
+    ws_bytes = BH * N * (C * wl.d * es + C * wl.d * 4 + wl.d * wl.d * es + C * C * 4)
+    return {"workload": wl.name, "B": wl.B, "H": wl.H, "T": wl.T, "d": wl.d,
+            "fox": wl.fox, "parallelism": f"replicas x{world}",
+            "l2": f"inputs larger than L2: {in_bytes / 2**20:.0f} MiB inputs + "
+                  f"{ws_bytes / 2**20:.0f} MiB workspace per step"}
 
 
 # Dense BF16 tensor peak of one GB300 as NVIDIA states it (the stricter
@@ -1089,7 +1103,6 @@ def run_gpu(args, wl, flops):
     value = world * total / (ms_max * 1e-3) / 1e12
     in_bytes = sum(a.numel() * a.element_size() for a in (x["q"], x["k"], x["v"], x["w"], beta,
                                                           logf) if a is not None)
-    ws_bytes = pa.path_attn_workspace_bytes(wl.B, wl.H, wl.T, wl.d, 1, logf is not None)
 
     # roofline of the dominant kernel (the attention scan)
     peak, _, peak_src = _peaks()
@@ -1158,10 +1171,7 @@ def run_gpu(args, wl, flops):
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
         "data": "synthetic",
-        "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "T": wl.T, "d": wl.d,
-                   "fox": wl.fox, "parallelism": f"replicas x{world}",
-                   "l2": f"inputs larger than L2: {in_bytes / 2**20:.0f} MiB inputs + "
-                         f"{ws_bytes / 2**20:.0f} MiB workspace per step"},
+        "config": _config(wl, world),
         "flops_per_step": {"attn": flops["attn"], "prep": flops["prep"]},
         "flash_equiv_tflops": world * flops["flash_equiv"] / (ms_max * 1e-3) / 1e12,
         "roofline": roofline,

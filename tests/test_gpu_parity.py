@@ -387,3 +387,27 @@ def test_low_rank_form_host_entry_and_other_shapes(_low_rank_form):
     pa.path_attn_set_transition_form(0)
     o2, l2 = _run(x)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+# ------------------------------------------------------------ seeded random shapes
+def _random_cases(n, seed):
+    g = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        d = int(g.choice([64, 128]))
+        dtype = str(g.choice(["bf16", "bf16", "f32"]))
+        T = int(g.integers(1, 900))
+        B, H = int(g.integers(1, 3)), int(g.integers(1, 4))
+        fox = bool(g.random() < 0.4)
+        lo = float(g.choice([0.0, 0.0, 1.0, 1.9]))
+        rng = None if g.random() < 0.5 else (lo, float(min(2.0, lo + g.choice([0.05, 0.1, 1.0]))))
+        cases.append((f"rand{i}", B, H, T, d, dtype, fox, rng, 1000 + i))
+    return cases
+
+
+@pytest.mark.parametrize("name,B,H,T,d,dtype,fox,rng,seed", _random_cases(24, 2027))
+def test_seeded_random_shapes_against_oracle(name, B, H, T, d, dtype, fox, rng, seed):
+    """Random (seeded) batch, heads, length (ragged against the chunk in
+    general), head size, dtype, gate and beta range: every output against
+    the oracle, at the bars of the fixed cases."""
+    _full_case(Workload(name, B, H, T, d, dtype, fox=fox, beta_range=rng, seed=seed))
