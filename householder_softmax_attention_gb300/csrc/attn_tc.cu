@@ -477,26 +477,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           x[j + 1] = __float_as_uint(z1);
         }
         warp_arrive(&bars->gate_empty[n & 1]);
-        mx = -row_min(x);
-      } else {
-        // logits stay raw; the scale enters through the FFMA inside the exp
-        if (sl2 >= 0.f) {
+      }
+      // The step's exponentials against the current reference max (gated: x
+      // holds z = -y, scaled, log2 units; plain logits get the scale here).
+      // Only when their sum shows that the logits grew past it (a term above
+      // 2^9) is the row max taken and the reference moved (lazy rescaling);
+      // otherwise the step needs no max at all.  NaN sums take that path too.
+      const float mul = kGate ? -1.f : sl2;
+      uint32_t pk[64];
+      float ls = exp_row(x, mul, m_used, pk);
+      bool need = false;
+      float alpha = 1.f;
+      if (!(ls <= 65536.f)) {
+        if (kGate) {
+          mx = -row_min(x);
+        } else if (sl2 >= 0.f) {
           mx = row_max(x) * sl2;
         } else {
           mx = row_min(x) * sl2;
         }
+        need = mx > m_used + 8.f;
+        if (need) {
+          alpha = ex2_approx(m_used - mx);
+          m_used = mx;
+          l *= alpha;
+          ls = exp_row(x, mul, m_used, pk);
+        }
       }
-      // lazy rescaling: move the reference max only when it grows by > 8 (log2)
-      const bool need = mx > m_used + 8.f;
-      float alpha = 1.f;
-      if (need) {
-        alpha = ex2_approx(m_used - mx);
-        m_used = mx;
-        l *= alpha;
-      }
-      uint32_t pk[64];
-      // gated: x holds z = -y (scaled, log2 units); plain logits get the scale here
-      l += exp_row(x, kGate ? -1.f : sl2, m_used, pk);
+      l += ls;
       // P buffer and O are free once O += P_{c+1} V_{c+1} has completed
       ok = mbar_wait(&bars->pv_done, n & 1, abort_flag, LIM);
       if (!ok) break;
