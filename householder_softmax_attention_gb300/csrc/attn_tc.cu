@@ -17,11 +17,12 @@
 // Qw is its bf16 copy, the A operand of the next step.  The transition is the
 // dense d x d form of F_c^T = I - W^T U W from the chunk preparation.
 //
-// Warp roles (384 threads):
+// Warp roles (384 threads; 512 at d = 64):
 //   warp 0      TMA producer: kr_c over ngt_c (one B tile), V (own ring)
 //   warp 1      TMEM allocation; one thread issues the [S | Qm] MMAs
 //   warp 2      one thread issues the O += P V MMAs
-//   warps 4-7   softmax: one query row per thread (TMEM lane = row)
+//   warps 4-7   softmax: one query row per thread (TMEM lane = row); at
+//               d = 64 keys 0-63 of each step, warps 12-15 keys 64-127
 //   warps 8-11  running-query conversion Qm -> Qw (and its initial load)
 // TMEM columns: S [0,128), Qm (d), O (d), Qw (d/2, packed bf16x2), P (64).
 // Every wait is bounded; on expiry the CTA records PATH_DEV_ERR_TIMEOUT in the
@@ -38,15 +39,22 @@ namespace pathattn {
 namespace {
 
 constexpr int kC = 128;       // chunk length = query tile = key tile
-constexpr int kThreads = 384;
+// 384 threads; at d = 64 (dense form) 512: each query row's logits are then
+// split between two softmax warpgroups, 64 keys each (see below).
+template <int D, bool kLR>
+constexpr bool kSplitRows = D == 64 && !kLR;
+template <int D, bool kLR>
+constexpr int kThreadsOf = kSplitRows<D, kLR> ? 512 : 384;
 // Tiles launch in groups of 4 heads: the group's kr, ngt and V chunks (12 MB
 // per head at T = 16384, d = 128) then stay in L2 until its last tile has
 // read them.  Measured at B = 2, H = 16, T = 16384, d = 128 (DRAM bytes per
 // launch, ncu; floor 1.05 GB): groups of 16 heads 3.34 GB, 8 heads 1.83 GB,
 // 4 heads 1.09 GB, 2 heads 1.06 GB; attention 1.986 / 1.914 / 1.891 / 1.891 ms.
 constexpr int kHeadGroup = 4;
-constexpr int kRegsLow = 56, kRegsSoftmax = 240, kRegsQuery = 112;
-static_assert(128 * (kRegsLow + kRegsSoftmax + kRegsQuery) <= kThreads * 168, "register split");
+constexpr int kRegsLow = 56, kRegsSoftmax = 240, kRegsSoftmaxHalf = 168, kRegsQuery = 112;
+static_assert(128 * (kRegsLow + kRegsSoftmax + kRegsQuery) <= 384 * 168, "register split");
+static_assert(128 * (kRegsLow + 2 * kRegsSoftmaxHalf + kRegsQuery) <= 512 * 128,
+              "register split, rows in two halves");
 
 // D: head dimension; R: the coordinates the transitions act on (R = D for
 // PaTH; R < D for partial PaTH, whose running query changes only in its
@@ -77,10 +85,13 @@ struct TcCfg {
   static constexpr uint32_t kColO = kColQm + R;
   static constexpr uint32_t kColQw = kColO + D;
   static constexpr uint32_t kColP = kColQw + D / 2;
+  // rows in two halves: the second half's O (its own reference max and sum)
+  static constexpr uint32_t kColO2 = kColP + 64;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr size_t kTileBytes = 2 * (kStageBytes + kVBytes) + kYwBytes;
-  static constexpr size_t kSmemBytes = kTileBytes + 1024 /*align*/ + 1280 /*barriers, gate*/;
+  static constexpr size_t kSmemBytes = kTileBytes + 1024 /*align*/ + 2304 /*barriers, gate*/;
   static_assert(kColP + 64 <= kTmemCols, "TMEM budget");
+  static_assert(kColO2 + D <= kTmemCols || D != 64 || kLR, "TMEM budget of the second O");
 };
 
 // Whether the first k-step of the fused logits MMA writes S alone (starting
@@ -97,12 +108,14 @@ struct Bars {
   uint64_t sq_ready, p_full, qk_done, pv_done, final_done;
   uint64_t yw_ready, q_done;  // low-rank form: Y converted; Qm += Y (-UW) done
   uint64_t gate_full[2], gate_empty[2];  // FoX: the gate ring below
+  uint64_t xch_full;  // rows in two halves: the second half's (m, l) published
   uint32_t tmem_base;
   int abort_flag;
   alignas(16) float gate[2][kC];  // FoX: log2-domain gate prefix of a key chunk
+  float xch_m[kC], xch_l[kC];     // rows in two halves: the second half's m and l
 };
 
-static_assert(sizeof(Bars) <= 1280, "barrier block size");
+static_assert(sizeof(Bars) <= 2304, "barrier block size");
 
 // The warp's tcgen05 stores / loads are fenced by each thread before this;
 // the warp then arrives once.
@@ -116,37 +129,40 @@ __device__ __forceinline__ void record_timeout(Bars* bars, int* status) {
   atomicExch(status, PATH_DEV_ERR_TIMEOUT);
 }
 
-// Row max / min of 128 values held as bit patterns: three-input max / min in
+// Row max / min of N values held as bit patterns: three-input max / min in
 // four independent chains (a single chain would put every operation on the
 // path).
-__device__ __forceinline__ float row_max(const uint32_t (&x)[128]) {
+template <int N>
+__device__ __forceinline__ float row_max(const uint32_t (&x)[N]) {
   float m[4];
 #pragma unroll
   for (int u = 0; u < 4; ++u) m[u] = __uint_as_float(x[u]);
 #pragma unroll
-  for (int j = 4; j < 128; j += 2)
+  for (int j = 4; j < N; j += 2)
     m[(j >> 1) & 3] = max3f(m[(j >> 1) & 3], __uint_as_float(x[j]), __uint_as_float(x[j + 1]));
   return max3f(m[0], m[1], fmaxf(m[2], m[3]));
 }
-__device__ __forceinline__ float row_min(const uint32_t (&x)[128]) {
+template <int N>
+__device__ __forceinline__ float row_min(const uint32_t (&x)[N]) {
   float m[4];
 #pragma unroll
   for (int u = 0; u < 4; ++u) m[u] = __uint_as_float(x[u]);
 #pragma unroll
-  for (int j = 4; j < 128; j += 2)
+  for (int j = 4; j < N; j += 2)
     m[(j >> 1) & 3] = min3f(m[(j >> 1) & 3], __uint_as_float(x[j]), __uint_as_float(x[j + 1]));
   return min3f(m[0], m[1], fminf(m[2], m[3]));
 }
 
-// p_j = 2^(mul x_j - m) for 128 values held as bit patterns, as bf16 pairs
-// in pk, returning their sum; the argument and the running sums go two values
+// p_j = 2^(mul x_j - m) for N values held as bit patterns, as bf16 pairs in
+// pk, returning their sum; the argument and the running sums go two values
 // per instruction (four packed partial sums).
-__device__ __forceinline__ float exp_row(const uint32_t (&x)[128], float mul, float m,
-                                         uint32_t (&pk)[64]) {
+template <int N>
+__device__ __forceinline__ float exp_row(const uint32_t (&x)[N], float mul, float m,
+                                         uint32_t (&pk)[N / 2]) {
   const uint64_t mulv = f2(mul, mul), negm = f2(-m, -m);
   uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-  for (int j = 0; j < 128; j += 2) {
+  for (int j = 0; j < N; j += 2) {
     float a0, a1;
     f2_split(f2_fma(f2(__uint_as_float(x[j]), __uint_as_float(x[j + 1])), mulv, negm), a0, a1);
     const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
@@ -159,11 +175,12 @@ __device__ __forceinline__ float exp_row(const uint32_t (&x)[128], float mul, fl
   return ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
 }
 
-// End of every role: all 384 threads meet on named barrier 1, then warp 1
+// End of every role: all NT threads meet on named barrier 1, then warp 1
 // (the allocating warp) frees TMEM.
+template <int NT>
 __device__ __forceinline__ void teardown(int warp, uint32_t tb, uint32_t ncols) {
   tc_fence_before_sync();
-  asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tb, ncols);
@@ -171,7 +188,7 @@ __device__ __forceinline__ void teardown(int warp, uint32_t tb, uint32_t ncols) 
 }
 
 template <int D, bool kGate, int R, bool kLR>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsOf<D, kLR>, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap map_kr,
                    const __grid_constant__ CUtensorMap map_ng,
                    const __grid_constant__ CUtensorMap map_v,
@@ -180,6 +197,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                    __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
                    int* __restrict__ status, int T, int Np, int BH, float sl2) {
   using Cfg = TcCfg<D, R, kLR>;
+  constexpr bool kSplit = kSplitRows<D, kLR>;
+  constexpr int kNT = kThreadsOf<D, kLR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -215,16 +234,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // the next [S | Qm] MMA may go once Qw is refreshed (4 running-query
     // warps) and S has been read and zeroed (4 softmax warps)
-    mbar_init(&bars->sq_ready, 8);
-    mbar_init(&bars->p_full, 4);  // one arrival per warp
+    mbar_init(&bars->sq_ready, kSplit ? 12 : 8);
+    mbar_init(&bars->p_full, kSplit ? 8 : 4);  // one arrival per warp
     mbar_init(&bars->qk_done, 1);
     mbar_init(&bars->pv_done, 1);
     mbar_init(&bars->final_done, 2);  // one commit from each MMA-issuing thread
     mbar_init(&bars->yw_ready, 4);    // low-rank: the 4 running-query warps
     mbar_init(&bars->q_done, 1);
+    mbar_init(&bars->xch_full, 4);  // rows in two halves: the second half's 4 warps
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->gate_full[s], 1);
-      mbar_init(&bars->gate_empty[s], 4);  // the softmax warps, once read
+      mbar_init(&bars->gate_empty[s], kSplit ? 8 : 4);  // the softmax warps, once read
     }
     bars->abort_flag = 0;
     fence_mbar_init();
@@ -390,9 +410,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         const uint32_t v_a = smem_addr(s_v + s * Cfg::kVBytes);
 #pragma unroll
-        for (int k = 0; k < kC / 16; ++k)
-          mma_bf16_ts(tO, tP + k * 8, sdesc_sw128(v_a + k * 2048, kC * 128, 1024), idPV,
-                      (n > 0 || k > 0));
+        for (int k = 0; k < kC / 16; ++k) {
+          // rows in two halves: keys 0-63 into O, keys 64-127 into O2
+          const bool second = kSplit && k >= kC / 32;
+          mma_bf16_ts(second ? tb + Cfg::kColO2 : tO, tP + k * 8,
+                      sdesc_sw128(v_a + k * 2048, kC * 128, 1024), idPV,
+                      (n > 0 || k > (second ? kC / 32 : 0)));
+        }
         mma_commit(&bars->pv_done);
         if (n < b) mma_commit(&bars->v_empty[s]);
       }
@@ -401,17 +425,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(&bars->final_done, 0, nullptr, LIM);
     }
   }
-    teardown(warp, tb, Cfg::kTmemCols);
-  } else if (warp < 8) {
-    regs_inc<kRegsSoftmax>();
+    teardown<kNT>(warp, tb, Cfg::kTmemCols);
+  } else if (warp < 8 || warp >= 12) {
     // ------------------------------------------------------------ softmax
-    const int q4 = warp - 4;
+    // One query row per thread (TMEM lane = row).  With rows in two halves
+    // (d = 64), warps 4-7 take keys 0-63 and warps 12-15 keys 64-127 of the
+    // same rows, each half with its own reference max m, sum l and output
+    // accumulator (O, O2): the halves never wait on each other until the
+    // epilogue, where the second half publishes (m, l) and the first merges.
+    constexpr int NC = kSplit ? 64 : kC;   // keys of a step this thread handles
+    if constexpr (kSplit) regs_inc<kRegsSoftmaxHalf>();
+    else regs_inc<kRegsSoftmax>();
+    const int h = kSplit && warp >= 12 ? 1 : 0;
+    const int col0 = h * 64;
+    const int q4 = warp & 3;
     const int r = q4 * 32 + lane;
     const int t = b * kC + r;
     const uint32_t lb = static_cast<uint32_t>(q4 * 32) << 16;
-    const uint32_t tS = tb + lb + Cfg::kColS, tO = tb + lb + Cfg::kColO,
-                   tP = tb + lb + Cfg::kColP;
-    uint32_t x[128];
+    const uint32_t tS = tb + lb + Cfg::kColS, tP = tb + lb + Cfg::kColP;
+    const uint32_t tO = tb + lb + (h ? Cfg::kColO2 : Cfg::kColO);
+    uint32_t x[NC];
     float m_used, l = 0.f;
     // S is free for the first MMA: started from zero by it, or cleared here
     if constexpr (!kSplitFirst<D, kGate>) {
@@ -419,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int u = 0; u < 32; ++u) z[u] = 0u;
 #pragma unroll
-      for (int cc = 0; cc < kC; cc += 32) tmem_st_x32(tS + cc, z);
+      for (int cc = 0; cc < NC; cc += 32) tmem_st_x32(tS + col0 + cc, z);
       tmem_st_wait();
       tc_fence_before_sync();
     }
@@ -428,12 +461,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       const float* sd = sdt + (static_cast<size_t>(bh) * Np + b) * kC * kC + r;
 #pragma unroll
-      for (int j = 0; j < kC; ++j) x[j] = __float_as_uint(__ldg(sd + j * kC));
+      for (int j = 0; j < NC; ++j) x[j] = __float_as_uint(__ldg(sd + (col0 + j) * kC));
       m_used = row_max(x);
-      uint32_t pk[64];
+      // a half whose keys all lie above the diagonal (rows below 64, second
+      // half) holds only -inf: any finite reference gives it zero weight
+      if (kSplit && m_used == -INFINITY) m_used = 0.f;
+      uint32_t pk[NC / 2];
       l = exp_row(x, 1.f, m_used, pk);
-      tmem_st_x32(tP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      tmem_st_x32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+#pragma unroll
+      for (int cc = 0; cc < NC / 2; cc += 32)
+        tmem_st_x32(tP + h * 32 + cc, *reinterpret_cast<uint32_t(*)[32]>(&pk[cc]));
       tmem_st_wait();
       tc_fence_before_sync();
       warp_arrive(&bars->p_full);
@@ -449,13 +486,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       {
       tc_fence_after_sync();
-      tmem_ld_x128(tS, x);   // S is read; the next MMA starts it from zero, or it is cleared
+      // S is read; the next MMA starts it from zero, or it is cleared
+      if constexpr (NC == 128) {
+        tmem_ld_x128(tS, x);
+      } else {
+        tmem_ld_x64(tS + col0, x);
+      }
       if constexpr (!kSplitFirst<D, kGate>) {
         uint32_t z[32];
 #pragma unroll
         for (int u = 0; u < 32; ++u) z[u] = 0u;
 #pragma unroll
-        for (int cc = 0; cc < kC; cc += 32) tmem_st_x32(tS + cc, z);
+        for (int cc = 0; cc < NC; cc += 32) tmem_st_x32(tS + col0 + cc, z);
         tmem_st_wait();
       }
       tc_fence_before_sync();
@@ -466,10 +508,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(&bars->gate_full[n & 1], (n >> 1) & 1, abort_flag, LIM);
         if (!ok) break;
         // z_j = lam2_j - scale S_j = -y_j, two per instruction; max y = -min z
-        const uint64_t* lg = reinterpret_cast<const uint64_t*>(&bars->gate[n & 1][0]);
+        const uint64_t* lg = reinterpret_cast<const uint64_t*>(&bars->gate[n & 1][col0]);
         const uint64_t nsl = f2(-sl2, -sl2);
 #pragma unroll
-        for (int j = 0; j < kC; j += 2) {
+        for (int j = 0; j < NC; j += 2) {
           float z0, z1;
           f2_split(f2_fma(f2(__uint_as_float(x[j]), __uint_as_float(x[j + 1])), nsl, lg[j >> 1]),
                    z0, z1);
@@ -484,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // 2^9) is the row max taken and the reference moved (lazy rescaling);
       // otherwise the step needs no max at all.  NaN sums take that path too.
       const float mul = kGate ? -1.f : sl2;
-      uint32_t pk[64];
+      uint32_t pk[NC / 2];
       float ls = exp_row(x, mul, m_used, pk);
       bool need = false;
       float alpha = 1.f;
@@ -520,40 +562,71 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st_x32(tO + cc, o);
         }
       }
-      tmem_st_x32(tP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      tmem_st_x32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+#pragma unroll
+      for (int cc = 0; cc < NC / 2; cc += 32)
+        tmem_st_x32(tP + h * 32 + cc, *reinterpret_cast<uint32_t(*)[32]>(&pk[cc]));
       tmem_st_wait();
       tc_fence_before_sync();
       warp_arrive(&bars->p_full);
       }  // pv_done
       }  // qk_done
     }
-    // epilogue: out = O / l, lse = (m + log2 l) ln 2
+    // epilogue: out = O / l, lse = (m + log2 l) ln 2; with rows in two halves
+    // the second half publishes (m, l) and the first merges the two partial
+    // softmaxes (O and O2 weighted by 2^(m_h - M), M the larger reference)
     if (ok) ok = mbar_wait(&bars->pv_done, b & 1, abort_flag, LIM);
-    if (ok) {
-      tc_fence_after_sync();
-      const float inv = 1.f / l;
-      __nv_bfloat16* orow = out + (static_cast<size_t>(bh) * T + t) * D;
-#pragma unroll
-      for (int cc = 0; cc < D; cc += 32) {
-        uint32_t o[32];
-        tmem_ld_x32(tO + cc, o);
-        uint32_t pk[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u)
-          pk[u] = pack_bf16x2(__uint_as_float(o[2 * u]) * inv, __uint_as_float(o[2 * u + 1]) * inv);
-        if (t < T) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + cc);
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+    if (kSplit && h == 1) {
+      if (ok) {
+        bars->xch_m[r] = m_used;
+        bars->xch_l[r] = l;
+        warp_arrive(&bars->xch_full);
+      } else {
+        record_timeout(bars, status);
+      }
+    } else {
+      float s0 = 1.f, s1 = 0.f, M = m_used;
+      if (kSplit && ok) {
+        ok = mbar_wait(&bars->xch_full, 0, abort_flag, LIM);
+        if (ok) {
+          const float m1 = bars->xch_m[r], l1 = bars->xch_l[r];
+          M = fmaxf(m_used, m1);
+          s0 = ex2_approx(m_used - M);
+          s1 = ex2_approx(m1 - M);
+          l = l * s0 + l1 * s1;
         }
       }
-      if (lse && t < T) lse[static_cast<size_t>(bh) * T + t] = (m_used + lrow + log2f(l)) * kLn2;
-    } else {
-      record_timeout(bars, status);
+      if (ok) {
+        tc_fence_after_sync();
+        const float inv = 1.f / l;
+        __nv_bfloat16* orow = out + (static_cast<size_t>(bh) * T + t) * D;
+#pragma unroll
+        for (int cc = 0; cc < D; cc += 32) {
+          uint32_t o[32];
+          tmem_ld_x32(tO + cc, o);
+          if constexpr (kSplit) {
+            uint32_t o2[32];
+            tmem_ld_x32(tb + lb + Cfg::kColO2 + cc, o2);
+#pragma unroll
+            for (int u = 0; u < 32; ++u)
+              o[u] = __float_as_uint(__uint_as_float(o[u]) * s0 + __uint_as_float(o2[u]) * s1);
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int u = 0; u < 16; ++u)
+            pk[u] = pack_bf16x2(__uint_as_float(o[2 * u]) * inv, __uint_as_float(o[2 * u + 1]) * inv);
+          if (t < T) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + cc);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          }
+        }
+        if (lse && t < T) lse[static_cast<size_t>(bh) * T + t] = (M + lrow + log2f(l)) * kLn2;
+      } else {
+        record_timeout(bars, status);
+      }
     }
-    teardown(warp, tb, Cfg::kTmemCols);
+    teardown<kNT>(warp, tb, Cfg::kTmemCols);
   } else {
     regs_dec<kRegsQuery>();
     // ------------------------------------------------------------ running query
@@ -636,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) record_timeout(bars, status);
     }
-    teardown(warp, tb, Cfg::kTmemCols);
+    teardown<kNT>(warp, tb, Cfg::kTmemCols);
   }
 }
 
@@ -695,7 +768,7 @@ cudaError_t launch_tc(const Geom& g, const Inputs& in, const Workspace& ws, int*
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(Cfg::kSmemBytes));
   if (e != cudaSuccess) return e;
-  kern<<<g.nch, kThreads, Cfg::kSmemBytes, st>>>(
+  kern<<<g.nch, kThreadsOf<D, kLR>, Cfg::kSmemBytes, st>>>(
       mkr, mng, mv, muw, ws.ql, ws.sdt, kGate ? ws.lam2 : nullptr,
       static_cast<__nv_bfloat16*>(in.out), in.lse, status, g.T, g.Np, g.BH, in.scale * kLog2e);
   return cudaGetLastError();
