@@ -89,7 +89,10 @@ struct TcCfg {
   static constexpr uint32_t kColO2 = kColP + 64;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr size_t kTileBytes = 2 * (kStageBytes + kVBytes) + kYwBytes;
-  static constexpr size_t kSmemBytes = kTileBytes + 1024 /*align*/ + 2304 /*barriers, gate*/;
+  // rows in two halves: the second half's (m, l) per row, after the barriers
+  static constexpr size_t kXchOffset = kTileBytes + 1280;
+  static constexpr size_t kSmemBytes =
+      kTileBytes + 1024 /*align*/ + 1280 /*barriers, gate*/ + (D == 64 && !kLR ? 2 * kC * 4 : 0);
   static_assert(kColP + 64 <= kTmemCols, "TMEM budget");
   static_assert(kColO2 + D <= kTmemCols || D != 64 || kLR, "TMEM budget of the second O");
 };
@@ -112,10 +115,9 @@ struct Bars {
   uint32_t tmem_base;
   int abort_flag;
   alignas(16) float gate[2][kC];  // FoX: log2-domain gate prefix of a key chunk
-  float xch_m[kC], xch_l[kC];     // rows in two halves: the second half's m and l
 };
 
-static_assert(sizeof(Bars) <= 2304, "barrier block size");
+static_assert(sizeof(Bars) <= 1280, "barrier block size");
 
 // The warp's tcgen05 stores / loads are fenced by each thread before this;
 // the warp then arrives once.
@@ -206,6 +208,9 @@ __global__ void __launch_bounds__(kThreadsOf<D, kLR>, 1)
   uint8_t* s_v = base + 2 * Cfg::kStageBytes;             // [2][kVBytes]
   uint8_t* s_yw = s_v + 2 * Cfg::kVBytes;                 // low-rank: [kYwBytes]
   Bars* bars = reinterpret_cast<Bars*>(base + Cfg::kTileBytes);
+  // rows in two halves: the second half's m and l of each row
+  float* xch_m = reinterpret_cast<float*>(base + Cfg::kXchOffset);
+  float* xch_l = xch_m + kC;
   volatile int* abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -577,8 +582,8 @@ __global__ void __launch_bounds__(kThreadsOf<D, kLR>, 1)
     if (ok) ok = mbar_wait(&bars->pv_done, b & 1, abort_flag, LIM);
     if (kSplit && h == 1) {
       if (ok) {
-        bars->xch_m[r] = m_used;
-        bars->xch_l[r] = l;
+        xch_m[r] = m_used;
+        xch_l[r] = l;
         warp_arrive(&bars->xch_full);
       } else {
         record_timeout(bars, status);
@@ -588,7 +593,7 @@ __global__ void __launch_bounds__(kThreadsOf<D, kLR>, 1)
       if (kSplit && ok) {
         ok = mbar_wait(&bars->xch_full, 0, abort_flag, LIM);
         if (ok) {
-          const float m1 = bars->xch_m[r], l1 = bars->xch_l[r];
+          const float m1 = xch_m[r], l1 = xch_l[r];
           M = fmaxf(m_used, m1);
           s0 = ex2_approx(m_used - M);
           s1 = ex2_approx(m1 - M);
