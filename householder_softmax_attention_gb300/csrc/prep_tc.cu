@@ -1,7 +1,7 @@
 // prep_tc.cu -- chunk preparation for bf16 inputs (d = 64 or 128) on tcgen05.
 //
-// One CTA (8 warps) per chunk of C = 128 tokens; the outputs and their algebra
-// are those listed in prep.cu (from "PaTH Attention: Position Encoding via
+// One persistent CTA (8 warps) per SM walks chunks of C = 128 tokens; the
+// outputs and their algebra are those listed in prep.cu (from "PaTH Attention: Position Encoding via
 // Accumulating Householder Transformations", frames "A triangular
 // representation makes paths computable" and "Backup: fix orientation before
 // implementing UT products").  Phases:
@@ -22,10 +22,17 @@
 //   P6b [sd' | ql'] = -lower(Q W^T) [TK | UW]   (A from TMEM, three terms)
 //       sdt = log2(e) (scale (Q K^T + sd') + gate) transposed, ql = Q + ql'
 //
+// Between chunks: the next chunk's W and K arrive by TMA while P6b runs, its
+// Q once P6b has read the region Q goes to; the diagonal logits sdt of a
+// chunk are held in registers and stored once the next chunk's Gram products
+// have been issued, so that those stores drain while the tensor cores work.
+//
 // A computed fp32 operand x enters an MMA as x_hi + x_lo with x_hi = bf16(x)
 // and x_lo = bf16(x - x_hi) (about 16 significant bits); products of two
 // computed operands drop only the lo*lo term.  All accumulation is fp32 in
 // TMEM.  Every wait is bounded (records a timeout in the status word).
+#include <algorithm>
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -84,6 +91,81 @@ __device__ __forceinline__ bool wait_mma(Bars* bars, uint32_t parity, int* statu
   return false;
 }
 
+// The chunk's beta and gate prefix into shared memory (threads 0 .. kC-1).
+template <bool kGate>
+__device__ __forceinline__ void load_chunk_scalars(float* sBeta, float* sLam, const float* beta,
+                                                   const float* lam2, int ch, int Np, int T,
+                                                   int tid) {
+  if (tid < kC) {
+    const int bh = ch / Np, t0 = (ch - bh * Np) * kC;
+    sBeta[tid] = t0 + tid < T ? beta[static_cast<size_t>(bh) * T + t0 + tid] : 0.f;
+    if (kGate) sLam[tid] = lam2[static_cast<size_t>(bh) * Np * kC + t0 + tid];
+  }
+}
+
+// TMA loads of a chunk's W and K rows (two 64-column halves each, stacked per
+// half as W | K) and of its Q rows into their own region.
+template <int D>
+__device__ __forceinline__ void load_wk(uint8_t* base, const CUtensorMap* mw, const CUtensorMap* mk,
+                                        int ch, int Np, uint64_t* bar) {
+  const int bh = ch / Np, t0 = (ch - bh * Np) * kC;
+  for (int h = 0; h < D / 64; ++h) {
+    tma_load_3d(base + kRWK + h * 2 * kHalf, mw, h * 64, t0, bh, bar);
+    tma_load_3d(base + kRWK + h * 2 * kHalf + kHalf, mk, h * 64, t0, bh, bar);
+  }
+}
+template <int D>
+__device__ __forceinline__ void load_q(uint8_t* base, const CUtensorMap* mq, int ch, int Np,
+                                       uint64_t* bar) {
+  const int bh = ch / Np, t0 = (ch - bh * Np) * kC;
+  for (int h = 0; h < D / 64; ++h) tma_load_3d(base + kRQS + h * kHalf, mq, h * 64, t0, bh, bar);
+}
+
+// The last epilogue of a chunk, in three parts.  The chunk's Q rows, loaded
+// from global memory before the last product is waited for (rows past T as
+// zero; element group e = tid + r * kThreads holds row e / (D/4), features
+// 4 (e % (D/4)) ..), so that their latency hides behind it:
+template <int D>
+__device__ __forceinline__ void load_q_rows(uint2 (&qv)[kC * D / 4 / kThreads],
+                                            const __nv_bfloat16* __restrict__ q, int ch, int Np,
+                                            int T, int tid) {
+  const int bh = ch / Np, t0 = (ch - bh * Np) * kC;
+  const __nv_bfloat16* qc = q + (static_cast<size_t>(bh) * T + t0) * D;
+#pragma unroll
+  for (int r = 0; r < kC * D / 4 / kThreads; ++r) {
+    const int e = tid + r * kThreads, i = e / (D / 4), n4 = (e % (D / 4)) * 4;
+    qv[r] = t0 + i < T ? __ldg(reinterpret_cast<const uint2*>(qc + static_cast<size_t>(i) * D + n4))
+                       : make_uint2(0u, 0u);
+  }
+}
+// ql = Q + ql' (ql' staged in shared memory), as coalesced rows:
+template <int D>
+__device__ __forceinline__ void store_ql(const uint2 (&qv)[kC * D / 4 / kThreads], const float* sq,
+                                         float* __restrict__ ql, int ch, int tid) {
+  float* out = ql + static_cast<size_t>(ch) * kC * D;
+#pragma unroll
+  for (int r = 0; r < kC * D / 4 / kThreads; ++r) {
+    const int e = tid + r * kThreads, i = e / (D / 4), n4 = (e % (D / 4)) * 4;
+    float4 o = *reinterpret_cast<const float4*>(sq + i * kSL + n4);
+    const __nv_bfloat162 q01 = *reinterpret_cast<const __nv_bfloat162*>(&qv[r].x);
+    const __nv_bfloat162 q23 = *reinterpret_cast<const __nv_bfloat162*>(&qv[r].y);
+    o.x += __low2float(q01);
+    o.y += __high2float(q01);
+    o.z += __low2float(q23);
+    o.w += __high2float(q23);
+    *reinterpret_cast<float4*>(out + i * D + n4) = o;
+  }
+}
+// and the diagonal logits sdt[j][i] (64 keys j of row i per thread, -inf
+// above the diagonal), coalesced over the rows i:
+__device__ __forceinline__ void store_sdt(const float (&tv)[64], float* __restrict__ sdt, int ch,
+                                          int row, int halfc) {
+  float* out = sdt + static_cast<size_t>(ch) * kC * kC + row;
+#pragma unroll
+  for (int u = 0; u < 64; ++u) out[static_cast<size_t>(64 * halfc + u) * kC] = tv[u];
+}
+
+// CTA b prepares chunks b, b + gridDim.x, ... (gridDim.x at most the SM count).
 template <int D, bool kGate>
 __global__ void __launch_bounds__(kThreads, 1)
     prep_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_k,
@@ -91,8 +173,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const uint8_t* q_raw, const float* __restrict__ beta, const float* __restrict__ lam2,
                    __nv_bfloat16* __restrict__ kr, float* __restrict__ ql,
                    __nv_bfloat16* __restrict__ ngt, float* __restrict__ sdt,
-                   __nv_bfloat16* __restrict__ uwn, int* status, int T, int Np, float sl2,
-                   int wr) {
+                   __nv_bfloat16* __restrict__ uwn, int* status, int T, int Np, int nch,
+                   float sl2, int wr) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -101,12 +183,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* sLam = sBeta + kC;
   Bars* bars = reinterpret_cast<Bars*>(sLam + kC);
 
-  const int ch = blockIdx.x, bh = ch / Np, n = ch - bh * Np, t0 = n * kC;
-  const int nrows = min(kC, T - t0);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, halfc = warp >> 2;  // TMEM lane quarter, column half
   const int row = quarter * 32 + lane;              // this thread's TMEM lane
-  const size_t row0 = static_cast<size_t>(bh) * T + t0;
+  const int grid = static_cast<int>(gridDim.x);
+  const __nv_bfloat16* q_bf = reinterpret_cast<const __nv_bfloat16*>(q_raw);
 
   if (tid == 0) {
     mbar_init(&bars->tma, 1);
@@ -114,11 +195,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->mma_q, 1);
     bars->abort_flag = 0;
     fence_mbar_init();
+    // the first chunk's inputs
+    mbar_arrive_expect_tx(&bars->tma, 3 * kC * D * 2);
+    load_wk<D>(base, &map_w, &map_k, blockIdx.x, Np, &bars->tma);
+    load_q<D>(base, &map_q, blockIdx.x, Np, &bars->tma);
   }
-  if (tid < kC) {
-    sBeta[tid] = tid < nrows ? beta[row0 + tid] : 0.f;
-    if (kGate) sLam[tid] = lam2[static_cast<size_t>(bh) * Np * kC + t0 + tid];
-  }
+  load_chunk_scalars<kGate>(sBeta, sLam, beta, lam2, blockIdx.x, Np, T, tid);
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, 512);
     tmem_relinquish();
@@ -128,22 +210,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tb = bars->tmem_base;
   const uint32_t lb = static_cast<uint32_t>(quarter * 32) << 16;
-  uint32_t mma_phase = 0;
-  bool ok = true;
+  uint32_t mma_phase = 0, q_phase = 0, tma_phase = 0;
+  bool ok = true, tma_pending = true;   // tma_pending: thread 0's view
+  float tv[64];                         // the previous chunk's diagonal logits
+  int prev = -1;
 
-  // ---- P1: TMA loads, then the Gram blocks
+  for (int ch = blockIdx.x; ch < nch; ch += grid) {
+  const int next = ch + grid;
+
+  // ---- P1: the Gram blocks, once the inputs have landed
   if (tid == 0) {
-    mbar_arrive_expect_tx(&bars->tma, 3 * kC * D * 2);
-    for (int h = 0; h < D / 64; ++h) {
-      tma_load_3d(base + kRWK + h * 2 * kHalf, &map_w, h * 64, t0, bh, &bars->tma);
-      tma_load_3d(base + kRWK + h * 2 * kHalf + kHalf, &map_k, h * 64, t0, bh, &bars->tma);
-      tma_load_3d(base + kRQS + h * kHalf, &map_q, h * 64, t0, bh, &bars->tma);
-    }
-    // the chunk one wave ahead (one CTA per SM, CTAs started in index order):
-    // its w, k and q rows into L2 while this chunk computes
-    const int ch2 = ch + static_cast<int>(sm_count());
-    if (ch2 < static_cast<int>(gridDim.x)) {
-      const int bh2 = ch2 / Np, t2 = (ch2 - bh2 * Np) * kC;
+    // the next chunk's rows into L2 (its TMA copies are issued late in this
+    // chunk, so that they then read from L2)
+    if (next < nch) {
+      const int bh2 = next / Np, t2 = (next - bh2 * Np) * kC;
       const size_t off = (static_cast<size_t>(bh2) * T + t2) * D * 2;
       const uint32_t bytes = static_cast<uint32_t>(min(kC, T - t2)) * D * 2;
       // w has wr columns (wr = D, or r for partial PaTH)
@@ -153,7 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bulk_prefetch_l2(k_raw + off, bytes);
       bulk_prefetch_l2(q_raw + off, bytes);
     }
-    ok = mbar_wait(&bars->tma, 0, &bars->abort_flag, kWaitLimitNs);
+    ok = ok && mbar_wait(&bars->tma, tma_phase, &bars->abort_flag, kWaitLimitNs);
+    tma_pending = false;
     if (ok) {
       tc_fence_after_sync();
       constexpr uint32_t id = idesc_bf16_f32(128, 256, false, false);
@@ -180,7 +261,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&bars->mma_q);
     }
   }
-  ok = wait_mma(bars, mma_phase, status);
+  tma_phase ^= 1;
+  // the previous chunk's diagonal logits, while the Gram products run
+  if (prev >= 0) store_sdt(tv, sdt, prev, row, halfc);
+  __syncthreads();   // this chunk's beta / gate prefix
+  ok = wait_mma(bars, mma_phase, status) && ok;
   mma_phase ^= 1;
   tc_fence_after_sync();
 
@@ -230,7 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();   // the fp32 blocks are read; the tiles overwrite them
     // S = strictLower(W K^T) -> bf16 hi/lo (MN-major B) over Q, once the query
     // Gram product that reads Q is done
-    ok = wait_mma(bars, 0, status, &bars->mma_q) && ok;
+    ok = wait_mma(bars, q_phase, status, &bars->mma_q) && ok;
+    q_phase ^= 1;
     tc_fence_after_sync();
 #pragma unroll
     for (int cc = 0; cc < 64; cc += 32) {
@@ -534,11 +620,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before_sync();
   __syncthreads();
 
-  // Q again, into the W | K region (free from here on), for the final pass
-  if (tid == 0) {
-    mbar_arrive_expect_tx(&bars->tma, kC * D * 2);
-    for (int h = 0; h < D / 64; ++h)
-      tma_load_3d(base + kRWK + h * kHalf, &map_q, h * 64, t0, bh, &bars->tma);
+  // the next chunk's W and K into the W | K region (free from here on)
+  if (tid == 0 && next < nch && ok) {
+    mbar_arrive_expect_tx(&bars->tma, 3 * kC * D * 2);
+    load_wk<D>(base, &map_w, &map_k, next, Np, &bars->tma);
+    tma_pending = true;
   }
 
   // ---- P6b: [sd' | ql'] = -lower(Q W^T) [TK | UW], A from TMEM (hi, lo)
@@ -565,27 +651,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int u = 0; u < D / 2; u += 8) st_global_v8(out + u, &orow[u]);
   }
+  uint2 qv[kC * D / 4 / kThreads];   // this chunk's Q rows, read while P6b runs
+  load_q_rows<D>(qv, q_bf, ch, Np, T, tid);
   ok = wait_mma(bars, mma_phase, status) && ok;
   mma_phase ^= 1;
   tc_fence_after_sync();
-  // epilogue, each warp half of its rows' columns: sdt[j][i] from Q K^T + sd'
-  // for keys j in [64 halfc, 64 halfc + 64) (coalesced over the rows i), and
-  // ql' for features [D/2 halfc, D/2 (halfc + 1)) to shared memory (the lo
-  // tiles are dead once the MMA is done)
+  // the region of [TK | UW] hi is free: the next chunk's Q
+  if (tid == 0 && next < nch && tma_pending) load_q<D>(base, &map_q, next, Np, &bars->tma);
+  // last epilogue, read out of the tensor memory: the diagonal logits sdt[j][i]
+  // from Q K^T + sd' for keys j in [64 halfc, 64 halfc + 64) into registers
+  // (stored after the next chunk's Gram products have been issued), ql' for
+  // features [D/2 halfc, D/2 (halfc + 1)) to shared memory (the lo tiles are
+  // dead once the MMA is done) for the coalesced ql rows
   {
     const int i = row;
-    float* out = sdt + static_cast<size_t>(ch) * kC * kC + i;
     const float li = kGate ? sLam[i] : 0.f;
 #pragma unroll
-    for (int cc = 64 * halfc; cc < 64 * halfc + 64; cc += 32) {
+    for (int cc = 0; cc < 64; cc += 32) {
       uint32_t v[32], qk[32];
-      tmem_ld_x32(tb + lb + cc, v);
-      tmem_ld_x32(tb + lb + 384 + cc, qk);
+      tmem_ld_x32(tb + lb + 64 * halfc + cc, v);
+      tmem_ld_x32(tb + lb + 384 + 64 * halfc + cc, qk);
 #pragma unroll
       for (int u = 0; u < 32; ++u) {
-        const int j = cc + u;
+        const int j = 64 * halfc + cc + u;
         const float gj = kGate ? sLam[j] : 0.f;
-        out[static_cast<size_t>(j) * kC] =
+        tv[cc + u] =
             j <= i ? fmaf(__uint_as_float(qk[u]) + __uint_as_float(v[u]), sl2, li - gj) : -INFINITY;
       }
     }
@@ -601,37 +691,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                         __uint_as_float(v[u + 2]), __uint_as_float(v[u + 3]));
     }
   }
+  prev = ch;
   tc_fence_before_sync();
   __syncthreads();
-  // ql = Q + ql', one row per warp instruction: coalesced stores; Q from the
-  // copy that landed during P6b (rows past T read as zero)
-  if (!mbar_wait(&bars->tma, 1, &bars->abort_flag, kWaitLimitNs)) {
-    bars->abort_flag = 1;
-    atomicExch(status, PATH_DEV_ERR_TIMEOUT);
-  }
-  {
-    const float* sq = sL;
-    float* out = ql + static_cast<size_t>(ch) * kC * D;
-    constexpr int kIter = kC * D / 4 / kThreads;  // 16 at d = 128
-    uint2 qv[kIter];
-#pragma unroll
-    for (int r = 0; r < kIter; ++r) {
-      const int e = tid + r * kThreads, i = e / (D / 4), n4 = (e % (D / 4)) * 4;
-      qv[r] = *reinterpret_cast<const uint2*>(base + kRWK + tile_off(i, n4));
-    }
-#pragma unroll
-    for (int r = 0; r < kIter; ++r) {
-      const int e = tid + r * kThreads, i = e / (D / 4), n4 = (e % (D / 4)) * 4;
-      float4 o = *reinterpret_cast<const float4*>(sq + i * kSL + n4);
-      const __nv_bfloat162 q01 = *reinterpret_cast<const __nv_bfloat162*>(&qv[r].x);
-      const __nv_bfloat162 q23 = *reinterpret_cast<const __nv_bfloat162*>(&qv[r].y);
-      o.x += __low2float(q01);
-      o.y += __high2float(q01);
-      o.z += __low2float(q23);
-      o.w += __high2float(q23);
-      *reinterpret_cast<float4*>(out + i * D + n4) = o;
-    }
-  }
+  store_ql<D>(qv, sL, ql, ch, tid);
+  // the tensor memory, the staging region and the chunk's beta / gate prefix
+  // are free
+  if (__syncthreads_or(bars->abort_flag != 0)) break;
+  if (next < nch) load_chunk_scalars<kGate>(sBeta, sLam, beta, lam2, next, Np, T, tid);
+  }  // chunks
+
+  if (prev >= 0) store_sdt(tv, sdt, prev, row, halfc);
+  // after an expired wait: copies still in flight land before the CTA exits
+  if (tid == 0 && tma_pending) mbar_wait(&bars->tma, tma_phase, nullptr, kWaitLimitNs);
+  tc_fence_before_sync();
+  __syncthreads();
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tb, 512);
@@ -683,11 +757,16 @@ cudaError_t launch_one(const Geom& g, const Inputs& in, const Workspace& ws, int
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
-  kern<<<g.nch, kThreads, kSmemBytes, st>>>(
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int grid = std::min(g.nch, std::max(sms, 1));   // one persistent CTA per SM
+  kern<<<grid, kThreads, kSmemBytes, st>>>(
       mw, mk, mq, static_cast<const uint8_t*>(in.w), static_cast<const uint8_t*>(in.k),
       static_cast<const uint8_t*>(in.q), in.beta, ws.lam2,
       static_cast<__nv_bfloat16*>(ws.kr), ws.ql, static_cast<__nv_bfloat16*>(ws.ngt), ws.sdt,
-      static_cast<__nv_bfloat16*>(ws.uwn), status, g.T, g.Np, in.scale * kLog2e, wr);
+      static_cast<__nv_bfloat16*>(ws.uwn), status, g.T, g.Np, g.nch, in.scale * kLog2e, wr);
   return cudaGetLastError();
 }
 
