@@ -101,8 +101,9 @@ struct TcCfg {
 // it from zero) instead of the softmax warps clearing S after reading it: one
 // more MMA instruction per step, four fewer TMEM stores on the softmax path.
 // Measured: 4% faster at d = 64 and 1.5-2% with the FoX gate, where the
-// softmax weighs most; no difference outside the run-to-run spread for plain
-// d = 128, whose step the tensor pipe bounds (kept on the clearing form).
+// softmax weighs most; 2% slower for plain d = 128 (1.87 -> 1.90 ms at
+// B=2 H=16 T=16384), whose step the tensor pipe bounds (kept on the
+// clearing form).
 template <int D, bool kGate>
 constexpr bool kSplitFirst = D == 64 || kGate;
 
