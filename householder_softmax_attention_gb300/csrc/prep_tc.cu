@@ -384,92 +384,95 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before_sync();
       __syncthreads();
     };
+    // Each product of a level is hi*hi + hi*lo + lo*hi; the first two share
+    // A = hi, so they run as one MMA of width 128 whose B is the hi tile
+    // followed by the lo tile (its second 64-wide atom at the lo tile's
+    // offset): D[:, 0:64) = hi*hi (+ lo*hi, issued after it), D[:, 64:128)
+    // = hi*lo, summed by the readers.  Two instructions per k-step, not three.
+    constexpr uint32_t id128 = idesc_bf16_f32(128, 128, false, true);
+    auto pair_b = [&](uint32_t hi, uint32_t lo_off) { return sdesc_sw128(hi, lo_off, 1024); };
+    auto ld_sum32 = [&](uint32_t col, float (&x)[32]) {   // D[:, col] + D[:, col + 64]
+      uint32_t v[32], w[32];
+      tmem_ld_x32(tb + lb + col, v);
+      tmem_ld_x32(tb + lb + col + 64, w);
+#pragma unroll
+      for (int u = 0; u < 32; ++u) x[u] = __uint_as_float(v[u]) + __uint_as_float(w[u]);
+    };
     // level 32, pairs p = 0, 1 (a = rows 64p.., b = rows 64p + 32..):
-    // E_p = G_ba U_aa -> TMEM cols [64p, 64p + 64) (cols 32.. are zero)
+    // E_p = G_ba U_aa -> TMEM cols [128p, 128p + 128) (cols 32.. of each half are zero)
     mma_round([&] {
       for (int p = 0; p < 2; ++p)
-        for (int term = 0; term < 3; ++term) {
-          const uint32_t at = term == 2 ? ul : uh, bt = term == 1 ? ul : uh;
-          for (int j = 0; j < 2; ++j)
-            mma_bf16_ss(tb + 64 * p, a_desc(at, 4 * p + j),
-                        b_desc(bt + p * kHalf + (4 * p + j) * 2048), id64, term > 0 || j > 0);
+        for (int j = 0; j < 2; ++j) {
+          const uint32_t bo = p * kHalf + (4 * p + j) * 2048;
+          mma_bf16_ss(tb + 128 * p, a_desc(uh, 4 * p + j), pair_b(uh + bo, kTile), id128, j > 0);
+          mma_bf16_ss(tb + 128 * p, a_desc(ul, 4 * p + j), b_desc(uh + bo), id64, 1);
         }
     });
     if (quarter & 1) {   // E_p rows are lanes of quarter 2p + 1 -> MN-major B tile
       const int p = quarter >> 1;
-      uint32_t v[32];
-      tmem_ld_x32(tb + lb + 64 * p + 32 * halfc, v);
+      float x32[32];
+      ld_sum32(128 * p + 32 * halfc, x32);
 #pragma unroll
-      for (int g8 = 0; g8 < 4; ++g8) {
-        float x[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) x[u] = __uint_as_float(v[g8 * 8 + u]);
-        put_hilo8(e_tiles + p * 8192, e_tiles + p * 8192 + 4096, lane, 4 * halfc + g8, x);
-      }
+      for (int g8 = 0; g8 < 4; ++g8)
+        put_hilo8(e_tiles + p * 8192, e_tiles + p * 8192 + 4096, lane, 4 * halfc + g8,
+                  *reinterpret_cast<const float(*)[8]>(&x32[g8 * 8]));
     }
     publish();
-    // U_bb E_p -> TMEM cols [128 + 64p, ...)
+    // U_bb E_p -> TMEM cols [128p, 128p + 128)
     mma_round([&] {
       for (int p = 0; p < 2; ++p)
-        for (int term = 0; term < 3; ++term) {
-          const uint32_t at = term == 2 ? ul : uh;
-          const uint32_t bt = eb + p * 8192 + (term == 1 ? 4096 : 0);
-          for (int j = 0; j < 2; ++j)
-            mma_bf16_ss(tb + 128 + 64 * p, a_desc(at, 4 * p + 2 + j), b_desc(bt + j * 2048), id64,
-                        term > 0 || j > 0);
+        for (int j = 0; j < 2; ++j) {
+          const uint32_t be = eb + p * 8192 + j * 2048;
+          mma_bf16_ss(tb + 128 * p, a_desc(uh, 4 * p + 2 + j), pair_b(be, 4096), id128, j > 0);
+          mma_bf16_ss(tb + 128 * p, a_desc(ul, 4 * p + 2 + j), b_desc(be), id64, 1);
         }
     });
     if (quarter & 1) {   // U_ba = -U_bb E_p, 16 columns per warp
       const int p = quarter >> 1;
-      uint32_t v[16];
-      tmem_ld_x16(tb + lb + 128 + 64 * p + 16 * halfc, v);
+      uint32_t v[16], w[16];
+      tmem_ld_x16(tb + lb + 128 * p + 16 * halfc, v);
+      tmem_ld_x16(tb + lb + 128 * p + 64 + 16 * halfc, w);
 #pragma unroll
       for (int g8 = 0; g8 < 2; ++g8) {
         float x[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) x[u] = -__uint_as_float(v[g8 * 8 + u]);
+        for (int u = 0; u < 8; ++u)
+          x[u] = -(__uint_as_float(v[g8 * 8 + u]) + __uint_as_float(w[g8 * 8 + u]));
         put_hilo8(u_hi, u_lo, row, 8 * p + 2 * halfc + g8, x);
       }
     }
     publish();
-    // level 64: E = G_21 U_11 -> TMEM cols [0, 64)
+    // level 64: E = G_21 U_11 -> TMEM cols [0, 128)
     mma_round([&] {
-      for (int term = 0; term < 3; ++term) {
-        const uint32_t at = term == 2 ? ul : uh, bt = term == 1 ? ul : uh;
-        for (int j = 0; j < 4; ++j)
-          mma_bf16_ss(tb, a_desc(at, j), b_desc(bt + j * 2048), id64, term > 0 || j > 0);
+      for (int j = 0; j < 4; ++j) {
+        mma_bf16_ss(tb, a_desc(uh, j), pair_b(uh + j * 2048, kTile), id128, j > 0);
+        mma_bf16_ss(tb, a_desc(ul, j), b_desc(uh + j * 2048), id64, 1);
       }
     });
     if (quarter >= 2) {
-      uint32_t v[32];
-      tmem_ld_x32(tb + lb + 32 * halfc, v);
+      float x32[32];
+      ld_sum32(32 * halfc, x32);
 #pragma unroll
-      for (int g8 = 0; g8 < 4; ++g8) {
-        float x[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) x[u] = __uint_as_float(v[g8 * 8 + u]);
-        put_hilo8(e_tiles, e_tiles + 8192, row - 64, 4 * halfc + g8, x);
-      }
+      for (int g8 = 0; g8 < 4; ++g8)
+        put_hilo8(e_tiles, e_tiles + 8192, row - 64, 4 * halfc + g8,
+                  *reinterpret_cast<const float(*)[8]>(&x32[g8 * 8]));
     }
     publish();
-    // U_22 E -> TMEM cols [64, 128)
+    // U_22 E -> TMEM cols [128, 256)
     mma_round([&] {
-      for (int term = 0; term < 3; ++term) {
-        const uint32_t at = term == 2 ? ul : uh, bt = eb + (term == 1 ? 8192 : 0);
-        for (int j = 0; j < 4; ++j)
-          mma_bf16_ss(tb + 64, a_desc(at, 4 + j), b_desc(bt + j * 2048), id64, term > 0 || j > 0);
+      for (int j = 0; j < 4; ++j) {
+        mma_bf16_ss(tb + 128, a_desc(uh, 4 + j), pair_b(eb + j * 2048, 8192), id128, j > 0);
+        mma_bf16_ss(tb + 128, a_desc(ul, 4 + j), b_desc(eb + j * 2048), id64, 1);
       }
     });
     if (quarter >= 2) {   // U_21 = -U_22 E
-      uint32_t v[32];
-      tmem_ld_x32(tb + lb + 64 + 32 * halfc, v);
+      float x32[32];
+      ld_sum32(128 + 32 * halfc, x32);
 #pragma unroll
-      for (int g8 = 0; g8 < 4; ++g8) {
-        float x[8];
+      for (int u = 0; u < 32; ++u) x32[u] = -x32[u];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) x[u] = -__uint_as_float(v[g8 * 8 + u]);
-        put_hilo8(u_hi, u_lo, row, 4 * halfc + g8, x);
-      }
+      for (int g8 = 0; g8 < 4; ++g8)
+        put_hilo8(u_hi, u_lo, row, 4 * halfc + g8, *reinterpret_cast<const float(*)[8]>(&x32[g8 * 8]));
     }
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
