@@ -219,15 +219,15 @@ __global__ void __launch_bounds__(kThreadsOf<D, kLR>, 1)
   // (largest b) first, interleaved over the group's heads.  Tiles of one head
   // that run together walk the same kr / ngt / V chunks, which then come
   // from L2; longest-first keeps the tail short.
-  int b, bh;
-  {
-    const int ord = blockIdx.x;
+  auto tile_of = [&](int ord, int& tb_, int& tbh) {
     const int per_group = kHeadGroup * Np;
     const int grp = ord / per_group, r = ord - grp * per_group;
     const int heads = min(kHeadGroup, BH - grp * kHeadGroup);
-    b = Np - 1 - r / heads;
-    bh = grp * kHeadGroup + r % heads;
-  }
+    tb_ = Np - 1 - r / heads;
+    tbh = grp * kHeadGroup + r % heads;
+  };
+  int b, bh;
+  tile_of(blockIdx.x, b, bh);
   const int Tp = Np * kC;
   const uint64_t LIM = kWaitLimitNs;
 
@@ -283,6 +283,20 @@ __global__ void __launch_bounds__(kThreadsOf<D, kLR>, 1)
       bool ok = true;
       for (int n = 0; n <= b && ok; ++n) {
         const int s = n & 1;
+        if (n == max(b - 3, 0)) {
+          // The tile one wave ahead (launch index + SM count) starts about
+          // when this one ends, a few steps from here: its running query and
+          // diagonal logits, written by the preparation and read once, into
+          // L2 now, so that its first loads come from there, not from HBM.
+          const int ord2 = blockIdx.x + static_cast<int>(sm_count());
+          if (ord2 < static_cast<int>(gridDim.x)) {
+            int b2, bh2;
+            tile_of(ord2, b2, bh2);
+            const size_t ch2 = static_cast<size_t>(bh2) * Np + b2;
+            if (b2 > 0) bulk_prefetch_l2(ql + ch2 * kC * D, kC * D * 4);
+            bulk_prefetch_l2(sdt + ch2 * kC * kC, kC * kC * 4);
+          }
+        }
         if (n < b) {
           const int c = b - 1 - n;
           if (n >= 2) ok = mbar_wait(&bars->kg_empty[s], ((n >> 1) - 1) & 1, abort_flag, LIM);
