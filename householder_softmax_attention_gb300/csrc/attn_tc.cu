@@ -502,6 +502,12 @@ __global__ void __launch_bounds__(kThreadsOf<D, kLR>, 1)
     const float lrow = kGate ? lam2[static_cast<size_t>(bh) * Tp + t] : 0.f;
     if (kGate) m_used -= lrow;
     for (int n = 0; n < b; ++n) {
+      // FoX: the chunk's gate prefix (loaded by the producer into the ring,
+      // long before) is waited for here, off the path from S to P
+      if (kGate) {
+        ok = mbar_wait(&bars->gate_full[n & 1], (n >> 1) & 1, abort_flag, LIM);
+        if (!ok) break;
+      }
       ok = mbar_wait(&bars->qk_done, n & 1, abort_flag, LIM);
       if (!ok) break;
       {
@@ -524,9 +530,6 @@ __global__ void __launch_bounds__(kThreadsOf<D, kLR>, 1)
       warp_arrive(&bars->sq_ready);
       float mx = -INFINITY;
       if (kGate) {
-        // the chunk's gate prefix, loaded by the producer into the ring
-        ok = mbar_wait(&bars->gate_full[n & 1], (n >> 1) & 1, abort_flag, LIM);
-        if (!ok) break;
         // z_j = lam2_j - scale S_j = -y_j, two per instruction; max y = -min z
         const uint64_t* lg = reinterpret_cast<const uint64_t*>(&bars->gate[n & 1][col0]);
         const uint64_t nsl = f2(-sl2, -sl2);
